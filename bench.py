@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Throughput of the k-quant MMQ prefill GEMM path (q8_1 quantise + q4_K/q6_K
+GEMM) on GB300, printed as one JSON line.
+
+A step is one prefill pass of a LLaMA-7B-shaped decoder stack's projection
+GEMMs at T tokens: for every layer, the four q8_1 quantisations (attention
+input shared by q/k/v, o input, FFN input shared by gate/up, down input)
+and the seven GEMMs (q, k, o, gate, up, down in q4_K; v in q6_K).  Every
+layer has its own weight buffers in HBM (32 layers = 3.8 GB), so each step
+streams weights far larger than the 129 MB L2: no L2 flush is needed.
+Weights and activations are seeded synthetic data (no checkpoint exists
+here); all layers hold copies of one drawn layer.
+
+Headline `value` is TMAC/s over the step (all GEMM MACs / step time, the
+quantisations included in the time), measured on the device with CUDA
+events around K replays of a CUDA graph of the step.  `e2e` repeats the
+measurement through host buffers: each step copies its activations from
+pinned host memory and reads the seven outputs of the last layer back.
+
+`--impl reference` times the CPU oracle (plain C, one thread) on a bounded
+sample of the same workload: full q8_1 quantisation of the four inputs and
+the first rows of every GEMM's output.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "q4_K×q8_1 MMQ TMAC/s and 7B-layer prefill tok/s at T=512 (fraction of int8 peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mmq", "reference"], default="mmq")
+    ap.add_argument("--tokens", type=int, default=512)
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mmq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def workload_desc(T, layers):
+    return (f"LLaMA-7B decoder-stack projections, prefill T={T}, {layers} layers: per layer q/k/o q4_K 4096x4096, "
+            f"v q6_K 4096x4096, gate/up q4_K 4096->11008, down q4_K 11008->4096, 4 q8_1 quantisations")
+
+
+def build_inputs(T):
+    from quantized_prefill_gemm_mmq_gb300 import synth
+    wl = synth.layer_7b(T)
+    xs = {}
+    for g in wl.gemms:
+        if g.x_seed not in xs:
+            xs[g.x_seed] = g.x()
+    return wl, xs
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def run_oracle_sample(wl, xs, weights, rows_per_gemm):
+    """Quantise every input fully and compute the first rows_per_gemm output
+    columns of each GEMM with the oracle; returns (seconds, MACs)."""
+    import oracle
+    macs = 0
+    t0 = time.perf_counter()
+    q = {s: oracle.quantize_q8_1(x) for s, x in xs.items()}
+    for g in wl.gemms:
+        r = min(rows_per_gemm, g.O)
+        qs, ds = q[g.x_seed]
+        bb = 144 if g.fmt == "q4_K" else 210
+        oracle.gemm(g.fmt, weights[g.name][: r * (g.K // 256) * bb], qs, ds, r)
+        macs += g.T * g.K * r
+    return time.perf_counter() - t0, macs
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl, xs = build_inputs(args.tokens)
+    weights = {g.name: g.weights() for g in wl.gemms}
+    # size each step so the whole run stays within ~2 minutes at ~0.25 GMAC/s
+    budget_s = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    macs_per_row = sum(g.T * g.K for g in wl.gemms)
+    rows = max(1, int(budget_s * 0.25e9 / macs_per_row))
+    for _ in range(args.warmup):
+        run_oracle_sample(wl, xs, weights, rows)
+    total_s, total_macs = 0.0, 0
+    for _ in range(args.steps):
+        s, m = run_oracle_sample(wl, xs, weights, rows)
+        total_s += s
+        total_macs += m
+    value = total_macs / total_s / 1e12
+    sample = (f"per step: q8_1 quantisation of the 4 layer inputs (T={args.tokens}) and the first {rows} output "
+              f"rows of each of the 7 GEMMs of one layer ({total_macs // args.steps} MACs)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TMAC/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32 dots, f32 terms, f64 sum",
+        "data": "synthetic (seeded; no checkpoint)",
+        "config": {"workload": workload_desc(args.tokens, 1) + " (bounded CPU sample)", "tokens": args.tokens},
+        "cpu_baseline": {"value": value, "unit": "TMAC/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TMAC/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- GPU arm ---
+
+def mmq_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    from quantized_prefill_gemm_mmq_gb300 import ops
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    wl, xs = build_inputs(args.tokens)
+    host_w = {g.name: g.weights() for g in wl.gemms}
+    w_layer = {n: torch.from_numpy(w).to(dev) for n, w in host_w.items()}
+    layers = [w_layer] + [{n: t.clone() for n, t in w_layer.items()} for _ in range(args.layers - 1)]
+    x_dev = {s: torch.from_numpy(x).to(dev) for s, x in xs.items()}
+    qbuf = {s: (None, torch.empty((x.shape[0], x.shape[1] // 32), dtype=torch.int32, device=dev),
+                torch.empty(x.shape, dtype=torch.float16, device=dev)) for s, x in xs.items()}
+    ybuf = {g.name: torch.empty((g.T, g.O), dtype=torch.float32, device=dev) for g in wl.gemms}
+    layer_macs = wl.macs
+    step_macs = layer_macs * args.layers
+    launches_per_step = args.layers * (len(xs) + len(wl.gemms))
+
+    ext_events = None   # per-launch events of the q4_K GEMMs, recorded inside the graph
+
+    def step(record=None):
+        for li, lw in enumerate(layers):
+            for s, x in x_dev.items():
+                ops.quantize_q8_1(x, out=qbuf[s])
+            for gi, g in enumerate(wl.gemms):
+                ev = record[li][gi] if record is not None else None
+                if ev is not None:
+                    ev[0].record()
+                _, ds, xh = qbuf[g.x_seed]
+                ops.gemm(g.fmt, lw[g.name], xh, ds, g.O, out=ybuf[g.name])
+                if ev is not None:
+                    ev[1].record()
+
+    # warm-up (eager): builds attributes, checks status
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ops.check_status(dev)
+
+    graph = None
+    timing_mode = "eager"
+    if not args.no_graph:
+        try:
+            ext_events = [[(torch.cuda.Event(enable_timing=True, external=True),
+                            torch.cuda.Event(enable_timing=True, external=True)) if g.fmt == "q4_K" else None
+                           for g in wl.gemms] for _ in layers]
+        except TypeError:
+            ext_events = None
+        graph = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                step(ext_events)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        timing_mode = "cuda graph"
+        for _ in range(max(1, args.warmup)):
+            graph.replay()
+        torch.cuda.synchronize()
+        ops.check_status(dev)
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    # ---------------- timed region (device-resident inputs)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)   # let the sampler start before the timed work
+    cur = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(args.steps):
+        run_step()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ops.check_status(dev)
+    elapsed_ms = e0.elapsed_time(e1)
+
+    # per-launch durations of the dominant kernel (q4_K GEMM)
+    q4_ms, q4_macs = 0.0, 0
+    kernel_timing = None
+    if ext_events is not None:
+        for li in range(len(layers)):
+            for gi, g in enumerate(wl.gemms):
+                ev = ext_events[li][gi]
+                if ev is not None:
+                    q4_ms += ev[0].elapsed_time(ev[1])
+                    q4_macs += g.macs
+        kernel_timing = "events in the captured graph (last replay of the timed region)"
+    if q4_ms <= 0.0:
+        # eager per-launch events over one more step
+        pairs = []
+        for lw in layers:
+            for g in wl.gemms:
+                _, ds, xh = qbuf[g.x_seed]
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(cur)
+                ops.gemm(g.fmt, lw[g.name], xh, ds, g.O, out=ybuf[g.name])
+                b.record(cur)
+                if g.fmt == "q4_K":
+                    pairs.append((a, b, g.macs))
+        torch.cuda.synchronize()
+        q4_ms = sum(a.elapsed_time(b) for a, b, _ in pairs)
+        q4_macs = sum(m for _, _, m in pairs)
+        kernel_timing = "eager per-launch events"
+
+    # ---------------- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = {s: torch.from_numpy(x).pin_memory() for s, x in xs.items()}
+        hy = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in ybuf.items()}
+        h2d = sum(t.numel() * t.element_size() for t in hx.values())
+        d2h = sum(t.numel() * t.element_size() for t in hy.values())
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(cur)
+        for _ in range(args.steps):
+            for s in x_dev:
+                x_dev[s].copy_(hx[s], non_blocking=True)
+            run_step()
+            for n in ybuf:
+                hy[n].copy_(ybuf[n], non_blocking=True)
+        f1.record(cur)
+        torch.cuda.synchronize()
+        e2e_ms = f0.elapsed_time(f1)
+        e2e = {"value": step_macs * args.steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TMAC/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        if e2e is not None:
+            t = torch.tensor([e2e["ms_per_step"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["ms_per_step"] = float(t.item())
+            e2e["value"] = step_macs * world / (e2e["ms_per_step"] * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    ms_step = elapsed_ms / args.steps
+    value = step_macs * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    achieved = 2.0 * q4_macs / (q4_ms * 1e-3) / 1e12 if q4_ms > 0 else None
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "frac": achieved / peak if achieved else None, "traffic": None,
+        "kernel": "mmq_gemm_kernel<q4_K, fold>",
+        "peak_source": f"{peak_src} bf16 dense burst (f16 tensor rate equals bf16)",
+        "timing": kernel_timing,
+        "avg_launch_us": 1e3 * q4_ms / max(1, sum(1 for g in wl.gemms if g.fmt == 'q4_K') * len(layers)),
+    }
+    cpu = None
+    if not args.no_cpu and world == 1:
+        rows = 160
+        secs, macs = run_oracle_sample(wl, xs, host_w, rows)
+        cpu = {"value": macs / secs / 1e12, "unit": "TMAC/s", "cores": 1, "kind": "oracle",
+               "sample": f"q8_1 quantisation of the 4 layer inputs and the first {rows} output rows of each of the "
+                         f"7 GEMMs of one layer ({macs} MACs, {secs:.1f} s, one thread)"}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TMAC/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 tensor-core operands holding exact int8/int4 integers, f32 accumulate and fold",
+        "data": "synthetic (seeded random k-quant weights and N(0,1) activations with 1% x20 outlier channels)",
+        "config": {
+            "workload": workload_desc(args.tokens, args.layers),
+            "tokens": args.tokens, "layers": args.layers, "macs_per_layer": layer_macs,
+            "parallelism": f"replicas x{world} (independent copies per GPU)",
+            "l2": "inputs larger than L2: each layer has its own weight buffers (weights per step "
+                  f"{sum(t.numel() for t in w_layer.values()) * args.layers / 1e9:.2f} GB)",
+            "launch": timing_mode,
+        },
+        "layer_tok_s": args.tokens * args.layers * args.steps * world / (elapsed_ms * 1e-3),
+        "model_tok_s_gemm_only": args.tokens * args.steps * world / (elapsed_ms * 1e-3),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        mmq_arm(args)
+
+
+if __name__ == "__main__":
+    main()

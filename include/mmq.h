@@ -1,0 +1,149 @@
+/*
+ * mmq.h -- C ABI of libmmq: the k-quant "MMQ" prefill GEMM on GB300 (sm_103a)
+ *
+ *     Y[T x O] = X[T x K] . W[O x K]^T
+ *
+ * with W stored in a k-quant format (q4_K or q6_K) and X quantised per
+ * 32-element block to q8_1.  The method is the one described on the
+ * "minfer" CUDA optimisation pages for the q4_K MMQ line:
+ *   - "31 . r28 -- Direction-A raw-nibble NB kernel, 2 blocks/SM", section
+ *     2.3 "The numerics contract": the integer dot of unsigned 4-bit weights
+ *     with int8 activations over each 32-weight sub-block, followed by the
+ *     f32 two-term fold  sum += dx*(d*sc)*C + (dx*ssum)*(-(dmin*m)),
+ *     stored f32 with no f16 between the dot and the store;
+ *   - "19 . r14 -- B fragments via ldmatrix + widened scale reads", 3.2(d):
+ *     the q8_1 activation scale pair (f16 d | int16 block sum);
+ *   - "43 . r40 -- __launch_bounds__(256,3) third resident block", 5:
+ *     q6_K, w = d*sc*(q-32) on 16-weight sub-blocks.
+ *
+ * Conventions for every call
+ * --------------------------
+ *   - All array arguments are DEVICE pointers allocated and owned by the
+ *     caller (for example PyTorch tensors).  The library allocates no
+ *     device memory per call, keeps no pointer after the call returns and
+ *     writes only the output arrays named below.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) on the current device.  A return value of
+ *     MMQ_OK means the work was validated and launched, not that it has
+ *     finished.  Kernel-side failures (a pipeline wait that exceeded its
+ *     time limit) are reported by mmq_check_status().
+ *   - Every pointer must be 16-byte aligned.  Inputs must be finite; the
+ *     result for NaN or Inf inputs is unspecified.
+ *   - The device must be compute capability 10.3 (GB300).
+ *   - Return value: MMQ_OK (0) or a negative MMQ_ERR_* code; on error
+ *     nothing is launched and no output is written.
+ *
+ * Storage formats (little-endian, rows contiguous)
+ * ------------------------------------------------
+ *   q4_K super-block, 144 bytes per 256 weights of one row: f16 d (bytes
+ *     0-1), f16 dmin (2-3), 12 bytes of packed 6-bit sub-block scales and
+ *     mins (4-15, GGUF k-quant packing), 128 bytes of 4-bit quants (16-143);
+ *     sub-block j (weights 32j..32j+31) is the low nibble (j even) or high
+ *     nibble (j odd) of quant bytes 32*(j/2) .. 32*(j/2)+31.
+ *     w = d*sc_j*q - dmin*m_j.
+ *   q6_K super-block, 210 bytes: ql[128], qh[64], int8 scales[16], f16 d
+ *     (GGUF order); w = d*sc_(e/16)*(q-32), q in 0..63.
+ *   W: [O][K/256] super-blocks, O*(K/256)*bytes_per_block bytes in total.
+ *   q8_1 activations, split-plane form of the pages' 40-byte block:
+ *     qs  int8     [T][K]     quantised values, -127..127;
+ *     xh  uint16   [T][K]     the same values as IEEE f16 (exact integers);
+ *                             this is the form the GEMM reads;
+ *     ds  uint32   [T][K/32]  low 16 bits: f16 d of the 32-block,
+ *                             high 16 bits: int16 sum of its 32 values.
+ *   Y: f32 [T][O], row-major, overwritten.
+ */
+#ifndef MMQ_H
+#define MMQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *mmq_stream_t;   /* == cudaStream_t */
+
+enum {
+    MMQ_OK = 0,
+    MMQ_ERR_SHAPE = -1,     /* a size is out of range (see each call)              */
+    MMQ_ERR_ALIGN = -2,     /* a pointer or leading dimension is misaligned        */
+    MMQ_ERR_ARCH = -3,      /* current device is not compute capability 10.3      */
+    MMQ_ERR_LAUNCH = -4,    /* the CUDA runtime refused the launch                 */
+    MMQ_ERR_TIMEOUT = -5,   /* (mmq_check_status) a kernel pipeline wait timed out */
+    MMQ_ERR_NULL = -6,      /* a required pointer is NULL                          */
+    MMQ_ERR_DRIVER = -7,    /* the driver could not build a TMA tensor map         */
+    MMQ_ERR_CUDA = -8       /* (mmq_check_status) a CUDA error is pending          */
+};
+
+/* Library ABI version; bumped on any signature or format change. */
+int mmq_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mmq_status_str(int status);
+
+/*
+ * q8_1 quantisation of activations ("31 . r28", 3.2: the q8_1 blocks
+ * carrying int8 values and the (f16 d | int16 ssum) pair).
+ * For every token t and 32-block b of x[t][0..K):
+ *   amax = max |x|;  d32 = amax/127 (IEEE f32 division);
+ *   q = clamp(round_half_away_from_zero(x/d32), -127, 127) (IEEE division);
+ *   ssum = sum of the 32 q;  stored d = f16(d32), round to nearest even.
+ *   An all-zero block stores d = 0, q = 0, ssum = 0.
+ * x:   f32, T rows of leading dimension ldx elements (ldx >= K, ldx % 4 == 0).
+ * qs:  int8 [T][K] or NULL.   xh: f16 bits [T][K] or NULL (not both NULL).
+ * ds:  uint32 [T][K/32], required.
+ * T >= 0 (T == 0 is a no-op), 32 <= K <= 2^20, K % 32 == 0.
+ */
+int mmq_quantize_q8_1(const float *x, int64_t ldx, int T, int K,
+                      int8_t *qs, uint32_t *ds, uint16_t *xh, mmq_stream_t stream);
+
+/*
+ * q4_K x q8_1 GEMM ("31 . r28", 2.3):  y[t][o] = sum over 32-weight
+ * sub-blocks b of  dx_b*(d*sc_b)*C_b + (dx_b*ssum_b)*(-(dmin*m_b)),
+ * C_b the exact integer dot of the 32 unsigned quants with the 32 int8
+ * activations; accumulation in f32 (rounding order unspecified).
+ * w: O*(K/256)*144 bytes.  xh, ds: as written by mmq_quantize_q8_1.
+ * y: f32 [T][O], overwritten.
+ * T >= 0, O >= 1, 256 <= K <= 2^20, K % 256 == 0.
+ */
+int mmq_gemm_q4K(const void *w, const uint16_t *xh, const uint32_t *ds,
+                 float *y, int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * q6_K x q8_1 GEMM ("43 . r40", 5: 16-weight sub-blocks, two k16 halves
+ * per 32-block):  y[t][o] = sum over 16-weight halves u of
+ * dx_(u/2)*(d*sc_u)*C16_u,  C16_u the exact integer dot of (q-32) with the
+ * int8 activations.  w: O*(K/256)*210 bytes; other arguments as
+ * mmq_gemm_q4K.
+ */
+int mmq_gemm_q6K(const void *w, const uint16_t *xh, const uint32_t *ds,
+                 float *y, int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * Diagnostic: the per-sub-block exact integer dots the GEMMs fold, through
+ * the same tensor-core pipeline.  out: int32 [T][O][K/32] for q4_K
+ * (C_b = sum q*a over 32 weights) or [T][O][K/16] for q6_K
+ * (C16_u = sum (q-32)*a over 16 weights).  Same shape limits as the GEMMs.
+ * Meant for small shapes (the output is K/32 or K/16 times larger than y).
+ */
+int mmq_debug_subdots_q4K(const void *w, const uint16_t *xh, int32_t *out,
+                          int T, int O, int K, mmq_stream_t stream);
+int mmq_debug_subdots_q6K(const void *w, const uint16_t *xh, int32_t *out,
+                          int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * Waits for `stream`, then reports and clears the library's device status
+ * word for the current device: MMQ_OK, MMQ_ERR_TIMEOUT (a kernel's pipeline
+ * wait ran past its limit; the kernel stopped early and its output is
+ * invalid) or MMQ_ERR_CUDA (the stream reported a CUDA error).  If
+ * `detail` is non-NULL it receives 4 ints: code, kernel id, wait site,
+ * linear block index of the first failure.
+ */
+int mmq_check_status(mmq_stream_t stream, int *detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MMQ_H */

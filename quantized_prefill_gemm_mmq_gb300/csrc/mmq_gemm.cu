@@ -1,0 +1,591 @@
+// mmq_gemm.cu -- q4_K / q6_K x q8_1 prefill GEMM on sm_103a tensor cores.
+//
+// Y[t][o] = sum_k W[o][k] X[t][k] in the block-wise integer form of the
+// "minfer" pages ("31 . r28 -- Direction-A raw-nibble NB kernel", 2.3):
+// per 32-weight sub-block b the exact integer dot C_b of the unsigned
+// 4-bit quants with the int8 activations, then the f32 two-term fold
+//     y += dx_b*(d*sc_b)*C_b + (dx_b*ssum_b)*(-(dmin*m_b)).
+// q6_K ("43 . r40 -- __launch_bounds__(256,3)", 5) uses 16-weight halves:
+//     y += dx_(u/2)*(d*sc_u)*C16_u,  C16_u = sum (q-32)*a.
+//
+// GB300 design (prior art on the pages is warp-level IMMA on GB10; sm_103a
+// has no int8 tcgen05 kind, so the dot runs as kind::f16 on exact integers):
+//   * The q8_1 values arrive as f16 (exact for |q| <= 127), K-major [T][K];
+//     TMA copies 128-token x 64-k tiles straight into the 128-byte-swizzled
+//     operand layout (tensor-core operand A, M = tokens).
+//   * Raw weight super-blocks are TMA-staged unmodified (q4_K: one 2-D box of
+//     128 rows x 144 B; q6_K: one 224-byte box per row, since 210-byte blocks
+//     start on 2-byte boundaries and the box must start 16-byte aligned).
+//   * Four unpack warps turn the raw bytes into the f16 operand B tile
+//     (N = 128 weight rows x 64 k, same swizzled layout) and decode the
+//     per-row, per-sub-block scale terms into shared memory.
+//   * One thread issues tcgen05.mma: every sub-block (32 k, or 16 k for
+//     q6_K) goes into a fresh TMEM accumulator of 128 x 128 f32; the products
+//     are integers and every partial sum stays below 2^24, so the f32
+//     accumulator holds the exact integer dot.  Four accumulators rotate.
+//   * Eight epilogue warps tcgen05.ld each accumulator and apply the fold in
+//     f32 registers; Y is written once at the end (f32, no f16 on the way).
+//   * Every pipeline wait is bounded: after a time limit the kernel records
+//     MMQ_ERR_TIMEOUT in the device status word, all roles stop, the MMA
+//     thread drains its tensor-core work and TMEM is freed.
+#include <cuda_fp16.h>
+
+#include "mmq_dev.cuh"
+#include "mmq_host.h"
+
+namespace mmq {
+namespace {
+
+enum { kQ4K = 0, kQ6K = 1 };
+enum { kFold = 0, kSubdots = 1 };
+
+constexpr int BM = 128;           // tokens per tile: MMA M, TMEM lanes
+constexpr int BN = 128;           // weight rows per tile: MMA N, columns per accumulator
+constexpr int BK = 64;            // k per pipeline stage: one 128-byte swizzled f16 row
+constexpr int STAGES = 4;         // operand ring depth
+constexpr int RAW_STAGES = 2;     // raw super-block ring depth
+constexpr int SDS_STAGES = 3;     // decoded scale ring depth
+constexpr int ACC_SLOTS = 4;      // TMEM accumulators (BN columns each)
+constexpr int TMEM_COLS = ACC_SLOTS * BN;
+constexpr int NUM_THREADS = 448;  // 14 warps
+constexpr int UNPACK_WARP0 = 2;   // warps 2..5
+constexpr int EPI_WARP0 = 6;      // warps 6..13
+constexpr int NUM_EPI_WARPS = 8;
+constexpr uint32_t A_BYTES = BM * 128;
+constexpr uint32_t B_BYTES = BN * 128;
+
+template <int FMT>
+struct Fmt;
+template <>
+struct Fmt<kQ4K> {
+    static constexpr int kBlockBytes = 144;
+    static constexpr int kRawRow = 144;     // staged bytes per tile row
+    static constexpr int kKSub = 32;        // k per accumulator
+    static constexpr int kSdsEntry = 8;     // float2 (d*sc, -dmin*m)
+};
+template <>
+struct Fmt<kQ6K> {
+    static constexpr int kBlockBytes = 210;
+    static constexpr int kRawRow = 224;     // 210 bytes + up to 14 bytes of lead-in
+    static constexpr int kKSub = 16;
+    static constexpr int kSdsEntry = 4;     // float d*sc
+};
+
+template <int FMT>
+struct Layout {
+    static constexpr int kSubPerSb = 256 / Fmt<FMT>::kKSub;          // accumulators per super-block
+    static constexpr int kSubPerStage = BK / Fmt<FMT>::kKSub;         // accumulators per stage
+    static constexpr uint32_t kRawBytes = BN * Fmt<FMT>::kRawRow;
+    static constexpr uint32_t kSdsBytes = kSubPerSb * BN * Fmt<FMT>::kSdsEntry;
+    static constexpr uint32_t oA = 0;
+    static constexpr uint32_t oB = oA + STAGES * A_BYTES;
+    static constexpr uint32_t oRaw = oB + STAGES * B_BYTES;
+    static constexpr uint32_t oSds = oRaw + RAW_STAGES * kRawBytes;
+    static constexpr uint32_t oBar = oSds + SDS_STAGES * kSdsBytes;
+    // barriers: a_full, b_full, st_empty [STAGES]; r_full, r_empty [RAW];
+    // s_full, s_empty [SDS]; acc_full, acc_empty [ACC]; mma_done
+    static constexpr int kNumBars = 3 * STAGES + 2 * RAW_STAGES + 2 * SDS_STAGES + 2 * ACC_SLOTS + 1;
+    static constexpr uint32_t oMisc = oBar + kNumBars * 8;
+    static constexpr uint32_t kBytes = oMisc + 16;
+    static constexpr uint32_t kDynSmem = kBytes + 1024;   // slack for 1024-byte alignment
+    static_assert(kDynSmem <= 232448, "shared memory budget");
+    static_assert(oRaw % 1024 == 0 && kRawBytes % 1024 == 0, "raw ring alignment");
+};
+
+struct Params {
+    const uint32_t *ds;   // [T][K/32]
+    float *y;             // [T][O]
+    int32_t *sub;         // [T][O][K/kKSub] (subdots mode)
+    int T, O, K;
+};
+
+// wait sites recorded with a timeout
+enum { SITE_P_RAW = 1, SITE_P_STAGE, SITE_M_A, SITE_M_B, SITE_M_ACC, SITE_U_RAW, SITE_U_SDS,
+       SITE_U_STAGE, SITE_E_SDS, SITE_E_ACC, SITE_DRAIN };
+
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity)
+{
+    // used only on the way out: waits for work already in flight, which
+    // completes on its own; bounded all the same
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// two f16 values from the low nibbles of bytes (sel) of w, exact
+__device__ __forceinline__ uint32_t nib_lo2(uint32_t w, uint32_t sel)
+{
+    const uint32_t p = __byte_perm(w, 0u, sel);                 // bytes -> [b, 0, b', 0]
+    const uint32_t h = (p & 0x000F000Fu) | 0x64006400u;           // 1024 + q in each half
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&h), __half2half2(__ushort_as_half(0x6400)));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// two f16 values from the high nibbles of bytes (sel) of w, exact
+__device__ __forceinline__ uint32_t nib_hi2(uint32_t w, uint32_t sel)
+{
+    const uint32_t p = __byte_perm(w, 0u, sel);
+    const uint32_t h = (p & 0x00F000F0u) | 0x64006400u;           // 1024 + 16 q
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2 *>(&h),
+                              __half2half2(__ushort_as_half(0x2C00)),      // 1/16
+                              __half2half2(__ushort_as_half(0xD400)));     // -64
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_h2(int a, int b)
+{
+    const __half2 h = __halves2half2(__int2half_rn(a), __int2half_rn(b));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int FMT, int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    mmq_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                    const Params p)
+{
+    using F = Fmt<FMT>;
+    using L = Layout<FMT>;
+    constexpr int kKid = 1 + FMT * 2 + MODE;
+    constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o0 = blockIdx.x * BN, t0 = blockIdx.y * BM;
+    const int T = p.T, O = p.O, K = p.K;
+    const int nks = K / BK, nsb = K / 256;
+
+    const uint32_t bar0 = sbase + L::oBar;
+    auto a_full = [&](int s) { return bar0 + 8u * s; };
+    auto b_full = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto st_empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+    auto r_full = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };
+    auto r_empty = [&](int s) { return bar0 + 8u * (3 * STAGES + RAW_STAGES + s); };
+    auto s_full = [&](int s) { return bar0 + 8u * (3 * STAGES + 2 * RAW_STAGES + s); };
+    auto s_empty = [&](int s) { return bar0 + 8u * (3 * STAGES + 2 * RAW_STAGES + SDS_STAGES + s); };
+    auto acc_full = [&](int s) { return bar0 + 8u * (3 * STAGES + 2 * RAW_STAGES + 2 * SDS_STAGES + s); };
+    auto acc_empty = [&](int s) {
+        return bar0 + 8u * (3 * STAGES + 2 * RAW_STAGES + 2 * SDS_STAGES + ACC_SLOTS + s);
+    };
+    const uint32_t mma_done = bar0 + 8u * (L::kNumBars - 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::oMisc);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + L::oMisc + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(a_full(s), 1);
+            mbar_init(b_full(s), 128);
+            mbar_init(st_empty(s), 1);
+        }
+        for (int s = 0; s < RAW_STAGES; ++s) {
+            mbar_init(r_full(s), 1);
+            mbar_init(r_empty(s), 128);
+        }
+        for (int s = 0; s < SDS_STAGES; ++s) {
+            mbar_init(s_full(s), 128);
+            mbar_init(s_empty(s), NUM_EPI_WARPS);
+        }
+        for (int s = 0; s < ACC_SLOTS; ++s) {
+            mbar_init(acc_full(s), 1);
+            mbar_init(acc_empty(s), NUM_EPI_WARPS);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            tma_prefetch(&tmA);
+            tma_prefetch(&tmW);
+        }
+        int n_a = 0, n_r = 0;   // loads issued, for the drain on abort
+        bool ok = true;
+        for (int ks = 0; ks < nks && ok; ++ks) {
+            if ((ks & 3) == 0) {
+                const int sb = ks >> 2, rs = sb % RAW_STAGES;
+                ok = mbar_wait(r_empty(rs), ((sb / RAW_STAGES) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
+                if (!ok) break;
+                const uint32_t dst = sbase + L::oRaw + rs * L::kRawBytes;
+                if (FMT == kQ4K) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(r_full(rs), L::kRawBytes);
+                        tma_load_2d(dst, &tmW, r_full(rs), sb * F::kBlockBytes, o0);
+                    }
+                } else {
+                    const int nrows = min(BN, O - o0);
+                    if (lane == 0) mbar_arrive_expect_tx(r_full(rs), (uint32_t)nrows * F::kRawRow);
+                    __syncwarp();
+                    for (int r = lane; r < nrows; r += 32) {
+                        const long long off = ((long long)(o0 + r) * nsb + sb) * F::kBlockBytes;
+                        tma_load_2d(dst + r * F::kRawRow, &tmW, r_full(rs), (int)(off & ~15ll), 0);
+                    }
+                }
+                ++n_r;
+            }
+            const int s = ks % STAGES;
+            ok = mbar_wait(st_empty(s), ((ks / STAGES) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(a_full(s), A_BYTES);
+                tma_load_2d(sbase + L::oA + s * A_BYTES, &tmA, a_full(s), ks * BK, t0);
+            }
+            ++n_a;
+            __syncwarp();
+        }
+        if (!ok) {
+            // let the copies already issued land before the block can exit
+            for (int i = max(0, n_a - STAGES); i < n_a; ++i) wait_drain(a_full(i % STAGES), (i / STAGES) & 1);
+            for (int i = max(0, n_r - RAW_STAGES); i < n_r; ++i)
+                wait_drain(r_full(i % RAW_STAGES), (i / RAW_STAGES) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            bool ok = true;
+            int acc = 0;
+            for (int ks = 0; ks < nks && ok; ++ks) {
+                const int s = ks % STAGES;
+                const uint32_t par = (ks / STAGES) & 1;
+                ok = mbar_wait(a_full(s), par, abort_flag, kKid, SITE_M_A) &&
+                     mbar_wait(b_full(s), par, abort_flag, kKid, SITE_M_B);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a_base = sbase + L::oA + s * A_BYTES;
+                const uint32_t b_base = sbase + L::oB + s * B_BYTES;
+#pragma unroll
+                for (int g = 0; g < L::kSubPerStage; ++g, ++acc) {
+                    const int slot = acc % ACC_SLOTS;
+                    ok = mbar_wait(acc_empty(slot), ((acc / ACC_SLOTS) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < F::kKSub / 16; ++kk) {
+                        const uint32_t koff = (uint32_t)(g * (F::kKSub / 16) + kk) * 32u;
+                        umma_f16(tmem_base + slot * BN, sdesc_k_sw128(a_base + koff),
+                                 sdesc_k_sw128(b_base + koff), kIdesc, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(acc_full(slot));
+                }
+                if (!ok) break;
+                umma_commit(st_empty(s));
+            }
+            umma_commit(mma_done);
+            if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp < EPI_WARP0) {
+        // ------------------------------------------------------ unpack warps --
+        const int r = threadIdx.x - UNPACK_WARP0 * 32;   // tile row 0..127
+        const int o = o0 + r;
+        const bool row_ok = o < O;
+        bool ok = true;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int rs = sb % RAW_STAGES, ss = sb % SDS_STAGES;
+            ok = mbar_wait(r_full(rs), (sb / RAW_STAGES) & 1, abort_flag, kKid, SITE_U_RAW) &&
+                 mbar_wait(s_empty(ss), ((sb / SDS_STAGES) & 1) ^ 1, abort_flag, kKid, SITE_U_SDS);
+            if (!ok) break;
+            const uint8_t *raw = smem + L::oRaw + rs * L::kRawBytes + r * F::kRawRow;
+            uint8_t *sds = smem + L::oSds + ss * L::kSdsBytes;
+            if (FMT == kQ4K) {
+                // header: d, dmin (f16), 12 bytes of 6-bit scales / mins
+                const uint4 hd = *reinterpret_cast<const uint4 *>(raw);
+                const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+                const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+                const uint32_t s0 = hd.y, s1 = hd.z, s2 = hd.w;
+                float2 *sd2 = reinterpret_cast<float2 *>(sds);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int sc_lo = (s0 >> (8 * j)) & 63, m_lo = (s1 >> (8 * j)) & 63;
+                    const int sc_hi = ((s2 >> (8 * j)) & 15) | (((s0 >> (8 * j + 6)) & 3) << 4);
+                    const int m_hi = ((s2 >> (8 * j + 4)) & 15) | (((s1 >> (8 * j + 6)) & 3) << 4);
+                    sd2[j * BN + r] = make_float2(d * (float)sc_lo, -(dmin * (float)m_lo));
+                    sd2[(j + 4) * BN + r] = make_float2(d * (float)sc_hi, -(dmin * (float)m_hi));
+                }
+            } else {
+                const int lead = (int)((((long long)o * nsb + sb) * F::kBlockBytes) & 15);
+                const uint8_t *blk = raw + lead;
+                float *sd1 = reinterpret_cast<float *>(sds);
+                const float d = row_ok ? __half2float(__ushort_as_half((unsigned short)(blk[208] | (blk[209] << 8))))
+                                       : 0.0f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    sd1[u * BN + r] = row_ok ? d * (float)(int8_t)blk[192 + u] : 0.0f;
+            }
+            mbar_arrive(s_full(ss));
+
+            for (int p4 = 0; p4 < 4; ++p4) {
+                const int ks = sb * 4 + p4, s = ks % STAGES;
+                ok = mbar_wait(st_empty(s), ((ks / STAGES) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
+                if (!ok) break;
+                uint8_t *brow = smem + L::oB + s * B_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+                if (FMT == kQ4K) {
+                    // stage p4 = sub-blocks 2*p4 (low nibbles, k 0..31) and 2*p4+1
+                    // (high nibbles, k 32..63) of quant bytes 32*p4 .. 32*p4+31
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4);
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4 + 16);
+                    const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t wa = wv[2 * (c & 3)], wb = wv[2 * (c & 3) + 1];
+                        uint4 v;
+                        if (c < 4) {
+                            v.x = nib_lo2(wa, 0x4140u);
+                            v.y = nib_lo2(wa, 0x4342u);
+                            v.z = nib_lo2(wb, 0x4140u);
+                            v.w = nib_lo2(wb, 0x4342u);
+                        } else {
+                            v.x = nib_hi2(wa, 0x4140u);
+                            v.y = nib_hi2(wa, 0x4342u);
+                            v.z = nib_hi2(wb, 0x4140u);
+                            v.w = nib_hi2(wb, 0x4342u);
+                        }
+                        *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = v;
+                    }
+                } else {
+                    // stage p4: half h = p4/2, quarters g0 = 2*(p4&1), g0+1; values q-32
+                    const int lead = (int)((((long long)o * nsb + sb) * F::kBlockBytes) & 15);
+                    const uint8_t *blk = raw + lead;
+                    const uint8_t *Lq = blk + 64 * (p4 >> 1);
+                    const uint8_t *Hq = blk + 128 + 32 * (p4 >> 1);
+                    const int g0 = 2 * (p4 & 1);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int g = g0 + (c >> 2), l0 = 8 * (c & 3);
+                        int v[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int l = l0 + i;
+                            const int lb = (g & 1) ? Lq[l + 32] : Lq[l];
+                            const int lo = (g >= 2) ? (lb >> 4) : (lb & 15);
+                            const int hi = (Hq[l] >> (2 * g)) & 3;
+                            v[i] = row_ok ? ((lo | (hi << 4)) - 32) : 0;
+                        }
+                        uint4 q;
+                        q.x = pack_h2(v[0], v[1]);
+                        q.y = pack_h2(v[2], v[3]);
+                        q.z = pack_h2(v[4], v[5]);
+                        q.w = pack_h2(v[6], v[7]);
+                        *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = q;
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(b_full(s));
+            }
+            if (ok) mbar_arrive(r_empty(rs));
+        }
+    } else {
+        // --------------------------------------------------------- epilogue --
+        const int ew = warp - EPI_WARP0;
+        const int quarter = warp & 3;            // TMEM lanes this warp may read
+        const int c0 = (ew >> 2) * 64;           // column half of the tile
+        const int tl = quarter * 32 + lane;      // token within the tile (TMEM lane)
+        const int t = t0 + tl;
+        const bool tok_ok = t < T;
+        float yv[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) yv[i] = 0.0f;
+        bool ok = true;
+        int acc = 0;
+        const int nsub_total = nsb * L::kSubPerSb;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int ss = sb % SDS_STAGES;
+            ok = mbar_wait(s_full(ss), (sb / SDS_STAGES) & 1, abort_flag, kKid, SITE_E_SDS);
+            if (!ok) break;
+            // this token's q8_1 scale words for the super-block (L1-resident)
+            const uint32_t *dsrow = (MODE == kFold && tok_ok) ? p.ds + (size_t)t * (K / 32) + sb * 8 : nullptr;
+            const uint8_t *sds = smem + L::oSds + ss * L::kSdsBytes;
+#pragma unroll 1
+            for (int g = 0; g < L::kSubPerSb; ++g, ++acc) {
+                const int slot = acc % ACC_SLOTS;
+                ok = mbar_wait(acc_full(slot), (acc / ACC_SLOTS) & 1, abort_flag, kKid, SITE_E_ACC);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t dword = dsrow ? __ldg(dsrow + (FMT == kQ4K ? g : (g >> 1))) : 0u;
+                const float dx = __half2float(__ushort_as_half((unsigned short)(dword & 0xFFFFu)));
+                const float dma = dx * (float)(int)(int16_t)(dword >> 16);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t rv[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(slot * BN + c0 + hh * 32), rv);
+                    tmem_ld_wait(rv);
+                    if (hh == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty(slot));
+                    }
+                    const int cbase = c0 + hh * 32;
+                    if (MODE == kFold) {
+                        if (FMT == kQ4K) {
+                            const float2 *sd2 = reinterpret_cast<const float2 *>(sds) + g * BN + cbase;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                const float4 sv = *reinterpret_cast<const float4 *>(sd2 + i);
+                                const float c0v = __uint_as_float(rv[i]), c1v = __uint_as_float(rv[i + 1]);
+                                float a0 = yv[hh * 32 + i], a1 = yv[hh * 32 + i + 1];
+                                a0 = fmaf(dx * sv.x, c0v, a0);
+                                a0 = fmaf(dma, sv.y, a0);
+                                a1 = fmaf(dx * sv.z, c1v, a1);
+                                a1 = fmaf(dma, sv.w, a1);
+                                yv[hh * 32 + i] = a0;
+                                yv[hh * 32 + i + 1] = a1;
+                            }
+                        } else {
+                            const float *sd1 = reinterpret_cast<const float *>(sds) + g * BN + cbase;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                const float4 sv = *reinterpret_cast<const float4 *>(sd1 + i);
+                                yv[hh * 32 + i + 0] = fmaf(dx * sv.x, __uint_as_float(rv[i + 0]), yv[hh * 32 + i + 0]);
+                                yv[hh * 32 + i + 1] = fmaf(dx * sv.y, __uint_as_float(rv[i + 1]), yv[hh * 32 + i + 1]);
+                                yv[hh * 32 + i + 2] = fmaf(dx * sv.z, __uint_as_float(rv[i + 2]), yv[hh * 32 + i + 2]);
+                                yv[hh * 32 + i + 3] = fmaf(dx * sv.w, __uint_as_float(rv[i + 3]), yv[hh * 32 + i + 3]);
+                            }
+                        }
+                    } else if (tok_ok) {
+                        const int bidx = sb * L::kSubPerSb + g;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int oc = o0 + cbase + i;
+                            if (oc < O)
+                                p.sub[((size_t)t * O + oc) * nsub_total + bidx] =
+                                    __float2int_rn(__uint_as_float(rv[i]));
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(s_empty(ss));
+        }
+        if (MODE == kFold && ok && tok_ok) {
+            float *yrow = p.y + (size_t)t * O + o0 + c0;
+            if ((O & 3) == 0 && o0 + c0 + 64 <= O) {
+#pragma unroll
+                for (int i = 0; i < 64; i += 4)
+                    *reinterpret_cast<float4 *>(yrow + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (o0 + c0 + i < O) yrow[i] = yv[i];
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int FMT, int MODE>
+int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int32_t *sub, int T, int O, int K,
+           mmq_stream_t stream)
+{
+    using L = Layout<FMT>;
+    if (T < 0 || O < 1 || K < 256 || K > (1 << 20) || (K & 255)) return MMQ_ERR_SHAPE;
+    const long long nsb = K / 256;
+    const long long wbytes = (long long)O * nsb * Fmt<FMT>::kBlockBytes;
+    if (FMT == kQ6K && wbytes >= (1ll << 31)) return MMQ_ERR_SHAPE;   // 1-D TMA coordinate is s32
+    if (T == 0) return MMQ_OK;
+    if (!w || !xh || (MODE == kFold && (!ds || !y)) || (MODE == kSubdots && !sub)) return MMQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(xh) || (ds && !aligned16(ds)) || (y && !aligned16(y)) ||
+        (sub && !aligned16(sub)))
+        return MMQ_ERR_ALIGN;
+    int rc = check_arch();
+    if (rc != MMQ_OK) return rc;
+
+    CUtensorMap tmA, tmW;
+    rc = make_tmap_2d(&tmA, xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK, BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != MMQ_OK) return rc;
+    if (FMT == kQ4K)
+        rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)(nsb * 144), (uint64_t)O,
+                          (uint64_t)(nsb * 144), 144, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else
+        rc = make_tmap_1d_bytes(&tmW, w, (uint64_t)wbytes, Fmt<kQ6K>::kRawRow);
+    if (rc != MMQ_OK) return rc;
+
+    auto kern = mmq_gemm_kernel<FMT, MODE>;
+    // the shared-memory attribute is set once per device (keeps the launch
+    // path free of attribute calls, e.g. while a stream is being captured)
+    static bool attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynSmem) != cudaSuccess)
+            return launch_status();
+        attr_done[dev] = true;
+    }
+    Params prm;
+    prm.ds = ds;
+    prm.y = y;
+    prm.sub = sub;
+    prm.T = T;
+    prm.O = O;
+    prm.K = K;
+    const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM));
+    kern<<<grid, NUM_THREADS, L::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace mmq
+
+extern "C" int mmq_gemm_q4K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O, int K,
+                            mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ4K, mmq::kFold>(w, xh, ds, y, nullptr, T, O, K, stream);
+}
+
+extern "C" int mmq_gemm_q6K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O, int K,
+                            mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ6K, mmq::kFold>(w, xh, ds, y, nullptr, T, O, K, stream);
+}
+
+extern "C" int mmq_debug_subdots_q4K(const void *w, const uint16_t *xh, int32_t *out, int T, int O, int K,
+                                     mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ4K, mmq::kSubdots>(w, xh, nullptr, nullptr, out, T, O, K, stream);
+}
+
+extern "C" int mmq_debug_subdots_q6K(const void *w, const uint16_t *xh, int32_t *out, int T, int O, int K,
+                                     mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ6K, mmq::kSubdots>(w, xh, nullptr, nullptr, out, T, O, K, stream);
+}
+
+extern "C" int mmq_check_status(mmq_stream_t stream, int *detail)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        if (detail) detail[0] = detail[1] = detail[2] = detail[3] = 0;
+        return MMQ_ERR_CUDA;
+    }
+    int h[4] = {0, 0, 0, 0};
+    if (cudaMemcpyFromSymbol(h, mmq::g_status, sizeof(h)) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_CUDA;
+    }
+    if (h[0] != 0) {
+        const int zero[4] = {0, 0, 0, 0};
+        cudaMemcpyToSymbol(mmq::g_status, zero, sizeof(zero));
+    }
+    if (detail)
+        for (int i = 0; i < 4; ++i) detail[i] = h[i];
+    return h[0];
+}

@@ -1,0 +1,33 @@
+// mmq_host.h -- host-side helpers shared by the libmmq entry points:
+// argument checks, the architecture check, and TMA tensor-map encoding.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mmq.h"
+
+namespace mmq {
+
+// MMQ_OK if the current device is compute capability 10.3 (cached per device).
+int check_arch();
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch-error translation: clears the sticky-free error state and maps it.
+int launch_status();
+
+// 2-D tiled tensor map over a row-major array: `inner` elements per row of
+// `elem_bytes` each, `rows` rows, `row_stride_bytes` apart; box of
+// box_inner x box_rows elements; swizzle as given.  Returns MMQ_OK or
+// MMQ_ERR_DRIVER.
+int make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, uint64_t inner,
+                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                 CUtensorMapSwizzle swizzle);
+
+// Tiled tensor map over `n` contiguous bytes with a box of `box` bytes
+// (addressed as coordinates (x, 0)).
+int make_tmap_1d_bytes(CUtensorMap *map, const void *base, uint64_t n, uint32_t box);
+
+}  // namespace mmq

@@ -1,0 +1,110 @@
+// mmq_quantize.cu -- q8_1 quantisation of f32 activations.
+//
+// Per token t and 32-element block b ("31 . r28 -- Direction-A raw-nibble NB
+// kernel", 3.2: q8_1 blocks of int8 values with an (f16 d | int16 ssum)
+// pair; "19 . r14 -- B fragments via ldmatrix", 3.2(d) for the packing):
+//   amax = max|x|, d32 = amax/127, q = clamp(round_half_away(x/d32), +-127),
+//   ssum = sum q, stored d = f16_rne(d32); all-zero block -> 0, 0, 0.
+// Both divisions are IEEE round-to-nearest (__fdiv_rn) so the result does
+// not depend on fast-math flags.
+//
+// Layout: eight threads own one 32-block, four consecutive floats each
+// (one 16-byte load).  The block's amax and ssum are reduced across the
+// eight lanes with shuffles.  The kernel is a grid-stride loop over all
+// (t, b) blocks; it is purely bandwidth-bound (read 4 B, write up to
+// 3.125 B per element).
+#include <cuda_fp16.h>
+
+#include "mmq_host.h"
+
+namespace mmq {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
+    const float *__restrict__ x, int64_t ldx, int T, int K, int8_t *__restrict__ qs,
+    uint32_t *__restrict__ ds, uint16_t *__restrict__ xh)
+{
+    const int nb = K >> 5;                                   // 32-blocks per token
+    const int64_t nblocks = (int64_t)T * nb;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane & 7;                                 // lane within the block's 8
+    // warp-uniform loop: a warp covers 4 consecutive blocks per iteration, so
+    // every lane reaches every shuffle; lanes past the end only skip stores
+    const int64_t warp_first = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 4;
+    const int64_t warp_step = ((int64_t)gridDim.x * kThreads >> 5) * 4;
+    for (int64_t base = warp_first; base < nblocks; base += warp_step) {
+        const int64_t blk = base + (lane >> 3);
+        const bool live = blk < nblocks;
+        const int t = live ? (int)(blk / nb) : 0;
+        const int b = live ? (int)(blk - (int64_t)t * nb) : 0;
+        const int k = b * 32 + sub * 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) v = __ldg(reinterpret_cast<const float4 *>(x + (int64_t)t * ldx + k));
+        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+        for (int m = 4; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m, 8));
+        int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+        float d32 = 0.0f;
+        if (amax != 0.0f) {
+            d32 = __fdiv_rn(amax, 127.0f);
+            q0 = (int)roundf(__fdiv_rn(v.x, d32));
+            q1 = (int)roundf(__fdiv_rn(v.y, d32));
+            q2 = (int)roundf(__fdiv_rn(v.z, d32));
+            q3 = (int)roundf(__fdiv_rn(v.w, d32));
+            q0 = min(127, max(-127, q0));
+            q1 = min(127, max(-127, q1));
+            q2 = min(127, max(-127, q2));
+            q3 = min(127, max(-127, q3));
+        }
+        int ssum = q0 + q1 + q2 + q3;
+#pragma unroll
+        for (int m = 4; m >= 1; m >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m, 8);
+        if (!live) continue;
+        const int64_t e = (int64_t)t * K + k;
+        if (qs) {
+            const uint32_t packed = (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) |
+                                    ((uint32_t)(uint8_t)q2 << 16) | ((uint32_t)(uint8_t)q3 << 24);
+            *reinterpret_cast<uint32_t *>(qs + e) = packed;
+        }
+        if (xh) {
+            const __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+            const __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+            uint2 hv;
+            hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+            hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+            *reinterpret_cast<uint2 *>(xh + e) = hv;
+        }
+        if (sub == 0) {
+            const uint16_t dh = __half_as_ushort(__float2half_rn(d32));
+            ds[blk] = (uint32_t)dh | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
+        }
+    }
+}
+
+}  // namespace
+}  // namespace mmq
+
+extern "C" int mmq_quantize_q8_1(const float *x, int64_t ldx, int T, int K, int8_t *qs, uint32_t *ds,
+                                 uint16_t *xh, mmq_stream_t stream)
+{
+    using namespace mmq;
+    if (T < 0 || K < 32 || K > (1 << 20) || (K & 31) || ldx < K) return MMQ_ERR_SHAPE;
+    if (T == 0) return MMQ_OK;
+    if (!x || !ds || (!qs && !xh)) return MMQ_ERR_NULL;
+    if (!aligned16(x) || (ldx & 3) || !aligned16(ds) || (qs && !aligned16(qs)) || (xh && !aligned16(xh)))
+        return MMQ_ERR_ALIGN;
+    const int a = check_arch();
+    if (a != MMQ_OK) return a;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t threads = ((int64_t)T * (K / 32) + 3) / 4 * 32;
+    int64_t grid = (threads + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 8;   // 8 resident blocks per SM
+    if (grid > cap) grid = cap;
+    quantize_q8_1_kernel<<<(unsigned)grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        x, ldx, T, K, qs, ds, xh);
+    return launch_status();
+}

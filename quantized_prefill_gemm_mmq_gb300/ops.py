@@ -1,0 +1,132 @@
+"""Thin PyTorch binding over libmmq's C ABI (argument marshalling only).
+
+Every function checks device, dtype, shape and contiguity, passes raw device
+pointers and the current CUDA stream to the library, and raises MMQError on
+a non-zero status.  No arithmetic of the method happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import MMQError, load
+
+BLOCK_BYTES = {"q4_K": 144, "q6_K": 210}
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _check(call: str, status: int):
+    if status != 0:
+        raise MMQError(call, status)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libmmq ops need CUDA tensors")
+
+
+def quantize_q8_1(x: torch.Tensor, want_qs: bool = True, want_xh: bool = True, out=None):
+    """q8_1-quantise activations x [T][K] f32 (row stride may exceed K).
+
+    Returns (qs, ds, xh): qs int8 [T][K] or None; ds int32 [T][K/32] holding
+    the library's uint32 words (f16 d | int16 block sum); xh float16 [T][K]
+    holding the same integer values as qs, or None.  `out` may supply the
+    three buffers (any of qs / xh may be None).
+    """
+    _need_cuda(x)
+    if x.dtype != torch.float32 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D float32 tensor with unit column stride")
+    T, K = x.shape
+    dev = x.device
+    if out is not None:
+        qs, ds, xh = out
+        for t, dt, shape in ((qs, torch.int8, (T, K)), (ds, torch.int32, (T, K // 32)), (xh, torch.float16, (T, K))):
+            if t is not None and (t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous()):
+                raise ValueError("bad output buffer")
+        if ds is None:
+            raise ValueError("ds buffer required")
+    else:
+        qs = torch.empty((T, K), dtype=torch.int8, device=dev) if want_qs else None
+        xh = torch.empty((T, K), dtype=torch.float16, device=dev) if want_xh else None
+        ds = torch.empty((T, K // 32), dtype=torch.int32, device=dev)
+    _need_cuda(qs, ds, xh)
+    with torch.cuda.device(dev):
+        st = load().mmq_quantize_q8_1(_ptr(x), x.stride(0), T, K, _ptr(qs), _ptr(ds), _ptr(xh), _stream(dev))
+    _check("mmq_quantize_q8_1", st)
+    return qs, ds, xh
+
+
+def _check_gemm_args(fmt: str, w: torch.Tensor, xh: torch.Tensor, O: int):
+    _need_cuda(w, xh)
+    if fmt not in BLOCK_BYTES:
+        raise ValueError(f"unknown format {fmt!r}")
+    if xh.dtype != torch.float16 or xh.dim() != 2 or not xh.is_contiguous():
+        raise ValueError("xh must be a contiguous [T][K] float16 tensor (q8_1 values)")
+    T, K = xh.shape
+    if w.dtype != torch.uint8 or not w.is_contiguous() or w.numel() != O * (K // 256) * BLOCK_BYTES[fmt]:
+        raise ValueError("w must be contiguous uint8 holding O*(K/256) super-blocks")
+    if w.device != xh.device:
+        raise ValueError("w and xh must be on the same device")
+    return T, K
+
+
+def gemm(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
+         out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y [T][O] f32 = q8_1(X) . W^T with W in `fmt` ("q4_K" or "q6_K")."""
+    T, K = _check_gemm_args(fmt, w, xh, O)
+    if ds.dtype != torch.int32 or tuple(ds.shape) != (T, K // 32) or not ds.is_contiguous():
+        raise ValueError("ds must be contiguous int32 [T][K/32]")
+    if out is None:
+        out = torch.empty((T, O), dtype=torch.float32, device=xh.device)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (T, O) or not out.is_contiguous():
+        raise ValueError("out must be contiguous float32 [T][O]")
+    fn = load().mmq_gemm_q4K if fmt == "q4_K" else load().mmq_gemm_q6K
+    with torch.cuda.device(xh.device):
+        st = fn(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
+    _check(f"mmq_gemm_{fmt.replace('_', '')}", st)
+    return out
+
+
+def gemm_q4K(w, xh, ds, O, out=None):
+    return gemm("q4_K", w, xh, ds, O, out)
+
+
+def gemm_q6K(w, xh, ds, O, out=None):
+    return gemm("q6_K", w, xh, ds, O, out)
+
+
+def debug_subdots(fmt: str, w: torch.Tensor, xh: torch.Tensor, O: int) -> torch.Tensor:
+    """Per-sub-block integer dots: int32 [T][O][K/32] (q4_K) or [T][O][K/16] (q6_K)."""
+    T, K = _check_gemm_args(fmt, w, xh, O)
+    nsub = K // 32 if fmt == "q4_K" else K // 16
+    out = torch.empty((T, O, nsub), dtype=torch.int32, device=xh.device)
+    fn = load().mmq_debug_subdots_q4K if fmt == "q4_K" else load().mmq_debug_subdots_q6K
+    with torch.cuda.device(xh.device):
+        st = fn(_ptr(w), _ptr(xh), _ptr(out), T, O, K, _stream(xh.device))
+    _check("mmq_debug_subdots", st)
+    return out
+
+
+def check_status(device: torch.device | None = None):
+    """Synchronise the current stream and raise if a kernel reported an error."""
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    detail = (ctypes.c_int * 4)()
+    with torch.cuda.device(dev):
+        st = load().mmq_check_status(_stream(dev), detail)
+    if st != 0:
+        raise MMQError(f"kernel (id {detail[1]}, site {detail[2]}, block {detail[3]})", st)
+
+
+def mmq_forward(fmt: str, w: torch.Tensor, x: torch.Tensor, O: int) -> torch.Tensor:
+    """Quantise x [T][K] to q8_1 and run the GEMM: the whole hot path."""
+    _, ds, xh = quantize_q8_1(x, want_qs=False, want_xh=True)
+    return gemm(fmt, w, xh, ds, O)

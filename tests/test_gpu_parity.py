@@ -1,0 +1,210 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: q8_1 values, scale words and per-sub-block integer dots bit-exact;
+Y within max|Y_gpu - Y_ref| <= 2e-4 * max|Y_ref| (f32 accumulation order
+differs from the oracle's f64 sum; f32 rounding alone stays near 1e-6).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from quantized_prefill_gemm_mmq_gb300 import synth  # noqa: E402
+from tests.kquant_pack import pack_q4K_block, pack_q6K_block  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-4
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_prefill_gemm_mmq_gb300 import ops as _ops
+    from quantized_prefill_gemm_mmq_gb300 import _lib
+    _lib.load()
+    return _ops
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _gpu_quant(ops, x):
+    qs, ds, xh = ops.quantize_q8_1(_dev(x))
+    return qs, ds, xh
+
+
+def _to_np_ds(ds):
+    return ds.cpu().numpy().view(np.uint32)
+
+
+def _rel_err(y, ref):
+    scale = float(np.abs(ref).max())
+    return float(np.abs(y.astype(np.float64) - ref.astype(np.float64)).max()) / max(scale, 1e-30)
+
+
+# -------------------------------------------------------------- q8_1 ----
+
+@pytest.mark.parametrize("T,K,seed,outl", [(64, 512, 0, False), (37, 256, 1, True), (512, 4096, 10, True),
+                                           (3, 11008, 21, True), (130, 768, 5, True)])
+def test_quantize_bit_exact(ops, orc, T, K, seed, outl):
+    x = synth.make_x(T, K, seed, outl)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    qs, ds, xh = _gpu_quant(ops, x)
+    ops.check_status()
+    assert np.array_equal(qs.cpu().numpy(), qs_r)
+    assert np.array_equal(_to_np_ds(ds), ds_r)
+    assert np.array_equal(xh.cpu().numpy().astype(np.float32), qs_r.astype(np.float32))
+
+
+def test_quantize_special_blocks(ops, orc):
+    x = np.zeros((4, 128), np.float32)
+    x[1, :32] = 127.0
+    x[1, 1:6] = [2.5, -2.5, 0.5, -0.5, 1.5]
+    x[2, 32:64] = np.float32(3e-7)              # tiny: d rounds into f16 subnormals
+    x[2, 64] = -1e-30
+    x[3, :] = np.linspace(-1000, 1000, 128, dtype=np.float32)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    qs, ds, xh = _gpu_quant(ops, x)
+    assert np.array_equal(qs.cpu().numpy(), qs_r)
+    assert np.array_equal(_to_np_ds(ds), ds_r)
+
+
+def test_quantize_strided_rows(ops, orc):
+    xfull = synth.make_x(50, 1024 + 64, 3)
+    xt = _dev(xfull)[:, :1024]
+    qs, ds, xh = ops.quantize_q8_1(xt)
+    qs_r, ds_r = orc.quantize_q8_1(xfull[:, :1024])
+    assert np.array_equal(qs.cpu().numpy(), qs_r)
+    assert np.array_equal(_to_np_ds(ds), ds_r)
+
+
+# ---------------------------------------------------- sub-block dots ----
+
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K"])
+@pytest.mark.parametrize("T,O,K", [(1, 1, 256), (64, 256, 512), (130, 200, 768), (200, 129, 256)])
+def test_subdots_bit_exact(ops, orc, fmt, T, O, K):
+    w = synth.make_weights(fmt, O, K, seed=T + O + K)
+    x = synth.make_x(T, K, seed=O)
+    qs_r, _ = orc.quantize_q8_1(x)
+    _, _, xh = _gpu_quant(ops, x)
+    got = ops.debug_subdots(fmt, _dev(w), xh, O)
+    ops.check_status()
+    ref = orc.subdots(fmt, w, qs_r, O)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_subdots_extremes(ops, orc):
+    # all-15 nibbles against all +-127 activations: the largest sub-block dots
+    O, K, T = 3, 256, 4
+    q = np.full(256, 15)
+    w4 = np.concatenate([pack_q4K_block(1.0, 1.0, [63] * 8, [63] * 8, q)] * O)
+    w6 = np.concatenate([pack_q6K_block(1.0, [-128] * 16, np.full(256, 63 if o % 2 else 0)) for o in range(O)])
+    x = np.full((T, K), 127.0, np.float32)
+    x[1] *= -1
+    x[2, ::2] *= -1
+    x[3, :] = 127.0 * ((np.arange(K) % 3) - 1)
+    qs_r, _ = orc.quantize_q8_1(x)
+    _, _, xh = _gpu_quant(ops, x)
+    assert np.array_equal(ops.debug_subdots("q4_K", _dev(w4), xh, O).cpu().numpy(), orc.subdots("q4_K", w4, qs_r, O))
+    assert np.array_equal(ops.debug_subdots("q6_K", _dev(w6), xh, O).cpu().numpy(), orc.subdots("q6_K", w6, qs_r, O))
+
+
+# -------------------------------------------------------------- GEMM ----
+
+def _run_gemm(ops, fmt, w, x, O):
+    qs, ds, xh = _gpu_quant(ops, x)
+    y = ops.gemm(fmt, _dev(w), xh, ds, O)
+    ops.check_status()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K"])
+@pytest.mark.parametrize("T,O,K", [(64, 256, 512), (1, 1, 256), (130, 300, 768), (129, 129, 1280),
+                                   (256, 512, 2048)])
+def test_gemm_full_small(ops, orc, fmt, T, O, K):
+    w = synth.make_weights(fmt, O, K, seed=7 * T + O)
+    x = synth.make_x(T, K, seed=K + T, outliers=T > 1)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm(fmt, w, qs_r, ds_r, O)
+    y = _run_gemm(ops, fmt, w, x, O)
+    assert y.shape == ref.shape
+    assert _rel_err(y, ref) <= TOL
+
+
+def test_gemm_config0_tiny(ops, orc):
+    g = synth.config(0).gemms[0]
+    w, x = g.weights(), g.x()
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm(g.fmt, w, qs_r, ds_r, g.O)
+    y = _run_gemm(ops, g.fmt, w, x, g.O)
+    assert _rel_err(y, ref) <= TOL
+
+
+def test_gemm_closed_form_superblock(ops):
+    sc = [63, 1, 32, 17, 48, 5, 60, 33]
+    m = [0, 63, 16, 47, 31, 62, 2, 40]
+    q = np.array([(i % 32) % 16 for i in range(256)])
+    w = pack_q4K_block(1.0, 1.0, sc, m, q)
+    x = np.full((1, 256), 127.0, np.float32)
+    y = _run_gemm(ops, "q4_K", w, x, 1)
+    assert y[0, 0] == 6833616.0
+
+
+def _sample_points(rng, T, O, n=1500):
+    ti = rng.integers(0, T, n)
+    oi = rng.integers(0, O, n)
+    # always include the corners and the ragged tails
+    ti = np.concatenate([ti, [0, 0, T - 1, T - 1]])
+    oi = np.concatenate([oi, [0, O - 1, 0, O - 1]])
+    return ti.astype(np.int32), oi.astype(np.int32)
+
+
+@pytest.mark.parametrize("cfg,T", [(1, None), (2, None), (3, None), (4, 16), (4, 64), (4, 256), (4, 1024), (4, 4096)])
+def test_gemm_full_size_sampled(ops, orc, cfg, T):
+    wl = synth.config(cfg, T)
+    rng = np.random.default_rng(cfg * 10000 + (T or 0))
+    xs = {}
+    for g in wl.gemms:
+        if g.x_seed not in xs:
+            xs[g.x_seed] = g.x()
+        x = xs[g.x_seed]
+        w = g.weights()
+        qs_r, ds_r = orc.quantize_q8_1(x)
+        qs, ds, xh = _gpu_quant(ops, x)
+        assert np.array_equal(qs.cpu().numpy(), qs_r)
+        assert np.array_equal(_to_np_ds(ds), ds_r)
+        y = ops.gemm(g.fmt, _dev(w), xh, ds, g.O)
+        ops.check_status()
+        ti, oi = _sample_points(rng, g.T, g.O)
+        ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
+        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
+        assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
+        assert torch.isfinite(y).all()
+
+
+def test_gemm_repeatable(ops):
+    g = synth.config(1).gemms[0]
+    w = _dev(g.weights())
+    _, ds, xh = ops.quantize_q8_1(_dev(g.x()))
+    y1 = ops.gemm(g.fmt, w, xh, ds, g.O)
+    y2 = ops.gemm(g.fmt, w, xh, ds, g.O)
+    ops.check_status()
+    assert torch.equal(y1, y2)
+
+
+def test_gpu_argument_errors(ops):
+    from quantized_prefill_gemm_mmq_gb300._lib import MMQError
+    w = torch.zeros(144 * 2, dtype=torch.uint8, device="cuda")
+    xh = torch.zeros((4, 512), dtype=torch.float16, device="cuda")
+    ds = torch.zeros((4, 16), dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        ops.gemm("q4_K", w, xh, ds, 2)        # wrong weight size for O=2, K=512 is 576 bytes
+    w2 = torch.zeros(144 * 4 + 4, dtype=torch.uint8, device="cuda")[4:]
+    with pytest.raises(MMQError) as e:
+        ops.gemm("q4_K", w2, xh, ds, 2)       # misaligned weight pointer
+    assert e.value.status == -2
