@@ -100,6 +100,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Warp-collective form: every lane waits, and the result is made uniform
+// across the warp so that warp-synchronous code after it never diverges.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
+                                               int kernel_id, int site)
+{
+    const bool ok = mbar_wait(bar, parity, abort, kernel_id, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // -------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch(const void *tmap)
 {
@@ -114,6 +123,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Non-tensor bulk copy global -> shared, completing `bytes` of transaction
+// on the mbarrier.  src and dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 // generic-proxy shared-memory writes -> visible to the tensor core's reads

@@ -13,9 +13,11 @@
 //   * The q8_1 values arrive as f16 (exact for |q| <= 127), K-major [T][K];
 //     TMA copies 128-token x 64-k tiles straight into the 128-byte-swizzled
 //     operand layout (tensor-core operand A, M = tokens).
-//   * Raw weight super-blocks are TMA-staged unmodified (q4_K: one 2-D box of
-//     128 rows x 144 B; q6_K: one 224-byte box per row, since 210-byte blocks
-//     start on 2-byte boundaries and the box must start 16-byte aligned).
+//   * Raw weight super-blocks are staged unmodified: q4_K with one 2-D TMA
+//     box of 128 rows x 144 B; q6_K with one bulk copy per row of the
+//     224-byte, 16-byte-aligned window around its 210-byte block (blocks
+//     start on 2-byte boundaries; the last few bytes of the buffer, past its
+//     final full 16-byte granule, are copied with byte loads instead).
 //   * Four unpack warps turn the raw bytes into the f16 operand B tile
 //     (N = 128 weight rows x 64 k, same swizzled layout) and decode the
 //     per-row, per-sub-block scale terms into shared memory.
@@ -29,6 +31,8 @@
 //     MMQ_ERR_TIMEOUT in the device status word, all roles stop, the MMA
 //     thread drains its tensor-core work and TMEM is freed.
 #include <cuda_fp16.h>
+
+#include <cstring>
 
 #include "mmq_dev.cuh"
 #include "mmq_host.h"
@@ -93,6 +97,7 @@ struct Layout {
 };
 
 struct Params {
+    const uint8_t *w;     // raw weights (q6_K bulk copies)
     const uint32_t *ds;   // [T][K/32]
     float *y;             // [T][O]
     int32_t *sub;         // [T][O][K/kKSub] (subdots mode)
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(st_empty(s), 1);
         }
         for (int s = 0; s < RAW_STAGES; ++s) {
-            mbar_init(r_full(s), 1);
+            mbar_init(r_full(s), FMT == kQ4K ? 1 : 32);   // q6_K: every producer lane arrives
             mbar_init(r_empty(s), 128);
         }
         for (int s = 0; s < SDS_STAGES; ++s) {
@@ -209,14 +214,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------ TMA producer --
         if (lane == 0) {
             tma_prefetch(&tmA);
-            tma_prefetch(&tmW);
+            if (FMT == kQ4K) tma_prefetch(&tmW);
         }
         int n_a = 0, n_r = 0;   // loads issued, for the drain on abort
         bool ok = true;
         for (int ks = 0; ks < nks && ok; ++ks) {
             if ((ks & 3) == 0) {
                 const int sb = ks >> 2, rs = sb % RAW_STAGES;
-                ok = mbar_wait(r_empty(rs), ((sb / RAW_STAGES) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
+                ok = mbar_wait_warp(r_empty(rs), ((sb / RAW_STAGES) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
                 if (!ok) break;
                 const uint32_t dst = sbase + L::oRaw + rs * L::kRawBytes;
                 if (FMT == kQ4K) {
@@ -225,18 +230,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tma_load_2d(dst, &tmW, r_full(rs), sb * F::kBlockBytes, o0);
                     }
                 } else {
+                    // one bulk copy per row: the 16-byte-aligned 224-byte window
+                    // holding the row's 210-byte block (its lead-in is skipped
+                    // by the unpack); past the buffer's last full 16-byte
+                    // granule the bytes are copied one by one
                     const int nrows = min(BN, O - o0);
-                    if (lane == 0) mbar_arrive_expect_tx(r_full(rs), (uint32_t)nrows * F::kRawRow);
-                    __syncwarp();
+                    const long long nbytes = (long long)O * nsb * F::kBlockBytes;
+                    uint32_t mine = 0;
                     for (int r = lane; r < nrows; r += 32) {
-                        const long long off = ((long long)(o0 + r) * nsb + sb) * F::kBlockBytes;
-                        tma_load_2d(dst + r * F::kRawRow, &tmW, r_full(rs), (int)(off & ~15ll), 0);
+                        const long long start = ((long long)(o0 + r) * nsb + sb) * F::kBlockBytes;
+                        const long long a = start & ~15ll;
+                        uint32_t sz = F::kRawRow;
+                        if (a + F::kRawRow > nbytes) {
+                            sz = (uint32_t)((nbytes - a) & ~15ll);
+                            uint8_t *drow = smem + L::oRaw + rs * L::kRawBytes + r * F::kRawRow;
+                            for (long long i = a + sz; i < start + F::kBlockBytes; ++i) drow[i - a] = p.w[i];
+                        }
+                        mine += sz;
+                    }
+                    mbar_arrive_expect_tx(r_full(rs), mine);
+                    for (int r = lane; r < nrows; r += 32) {
+                        const long long start = ((long long)(o0 + r) * nsb + sb) * F::kBlockBytes;
+                        const long long a = start & ~15ll;
+                        uint32_t sz = F::kRawRow;
+                        if (a + F::kRawRow > nbytes) sz = (uint32_t)((nbytes - a) & ~15ll);
+                        bulk_load(dst + r * F::kRawRow, p.w + a, sz, r_full(rs));
                     }
                 }
                 ++n_r;
             }
             const int s = ks % STAGES;
-            ok = mbar_wait(st_empty(s), ((ks / STAGES) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
+            ok = mbar_wait_warp(st_empty(s), ((ks / STAGES) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
             if (!ok) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(a_full(s), A_BYTES);
@@ -402,7 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int nsub_total = nsb * L::kSubPerSb;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int ss = sb % SDS_STAGES;
-            ok = mbar_wait(s_full(ss), (sb / SDS_STAGES) & 1, abort_flag, kKid, SITE_E_SDS);
+            ok = mbar_wait_warp(s_full(ss), (sb / SDS_STAGES) & 1, abort_flag, kKid, SITE_E_SDS);
             if (!ok) break;
             // this token's q8_1 scale words for the super-block (L1-resident)
             const uint32_t *dsrow = (MODE == kFold && tok_ok) ? p.ds + (size_t)t * (K / 32) + sb * 8 : nullptr;
@@ -410,7 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
             for (int g = 0; g < L::kSubPerSb; ++g, ++acc) {
                 const int slot = acc % ACC_SLOTS;
-                ok = mbar_wait(acc_full(slot), (acc / ACC_SLOTS) & 1, abort_flag, kKid, SITE_E_ACC);
+                ok = mbar_wait_warp(acc_full(slot), (acc / ACC_SLOTS) & 1, abort_flag, kKid, SITE_E_ACC);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t dword = dsrow ? __ldg(dsrow + (FMT == kQ4K ? g : (g >> 1))) : 0u;
@@ -497,8 +521,6 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
     using L = Layout<FMT>;
     if (T < 0 || O < 1 || K < 256 || K > (1 << 20) || (K & 255)) return MMQ_ERR_SHAPE;
     const long long nsb = K / 256;
-    const long long wbytes = (long long)O * nsb * Fmt<FMT>::kBlockBytes;
-    if (FMT == kQ6K && wbytes >= (1ll << 31)) return MMQ_ERR_SHAPE;   // 1-D TMA coordinate is s32
     if (T == 0) return MMQ_OK;
     if (!w || !xh || (MODE == kFold && (!ds || !y)) || (MODE == kSubdots && !sub)) return MMQ_ERR_NULL;
     if (!aligned16(w) || !aligned16(xh) || (ds && !aligned16(ds)) || (y && !aligned16(y)) ||
@@ -511,12 +533,13 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
     rc = make_tmap_2d(&tmA, xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK, BM,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MMQ_OK) return rc;
-    if (FMT == kQ4K)
+    if (FMT == kQ4K) {
         rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)(nsb * 144), (uint64_t)O,
                           (uint64_t)(nsb * 144), 144, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
-    else
-        rc = make_tmap_1d_bytes(&tmW, w, (uint64_t)wbytes, Fmt<kQ6K>::kRawRow);
-    if (rc != MMQ_OK) return rc;
+        if (rc != MMQ_OK) return rc;
+    } else {
+        std::memset(&tmW, 0, sizeof(tmW));   // q6_K stages its rows with plain bulk copies
+    }
 
     auto kern = mmq_gemm_kernel<FMT, MODE>;
     // the shared-memory attribute is set once per device (keeps the launch
@@ -531,6 +554,7 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
         attr_done[dev] = true;
     }
     Params prm;
+    prm.w = static_cast<const uint8_t *>(w);
     prm.ds = ds;
     prm.y = y;
     prm.sub = sub;

@@ -87,15 +87,6 @@ int make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, 
     return r == CUDA_SUCCESS ? MMQ_OK : MMQ_ERR_DRIVER;
 }
 
-int make_tmap_1d_bytes(CUtensorMap *map, const void *base, uint64_t n, uint32_t box)
-{
-    // The driver refuses rank-1 tiled maps, so the buffer is described as a
-    // single row of n bytes (rank 2, one row); the row stride is never used
-    // but must be a multiple of 16.
-    return make_tmap_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, n, 1, (n + 15) & ~uint64_t(15), box, 1,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
 }  // namespace mmq
 
 extern "C" int mmq_version(void) { return 1; }

@@ -26,8 +26,4 @@ int make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, 
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                  CUtensorMapSwizzle swizzle);
 
-// Tiled tensor map over `n` contiguous bytes with a box of `box` bytes
-// (addressed as coordinates (x, 0)).
-int make_tmap_1d_bytes(CUtensorMap *map, const void *base, uint64_t n, uint32_t box);
-
 }  // namespace mmq
