@@ -181,6 +181,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] . B[smem]^T, tf32 inputs, f32 accumulate.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // arrive on an mbarrier once every previously issued tcgen05 op of this thread completes
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
@@ -197,6 +209,34 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
            | (0u << 15) | (0u << 16)          // A, B K-major
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// Instruction descriptor for kind::tf32: tf32 A and B (K-major), f32 D.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N)
+{
+    return (1u << 4)                          // D format: f32
+           | (2u << 7) | (2u << 10)           // A, B format: tf32
+           | ((uint32_t)(N >> 3) << 17)
+           | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for a K-major operand without swizzle:
+// 8-row x 16-byte core matrices, `lbo` bytes apart along K and `sbo` bytes
+// apart along M/N.
+__device__ __forceinline__ uint64_t sdesc_k_none(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4)
+           | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16)
+           | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32)
+           | ((uint64_t)1 << 46);                   // version; layout 0 = no swizzle
+}
+
+// f32 rounded to tf32 (round to nearest, ties away), low 13 bits cleared
+__device__ __forceinline__ float to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
 }
 
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
@@ -243,6 +283,26 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
                    "+r"(r[31])
                  :
                  : "memory");
+}
+
+// 32 TMEM lanes x 32 consecutive 32-bit columns from registers (the inverse of
+// tmem_ld32); complete with tmem_st_wait() before reading the columns back.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 }  // namespace mmq

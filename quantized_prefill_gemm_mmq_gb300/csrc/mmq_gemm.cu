@@ -514,6 +514,436 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// =========================================================================
+// q4_K GEMM, production form.
+//
+// Same pipeline as above, with the fold restructured so that the per-(token,
+// row, sub-block) work left on the CUDA cores is one packed FMA:
+//   * the unpack warps multiply each 4-bit quant by its 6-bit sub-block scale
+//     while converting it (sc*q <= 945 is exact in f16), so the tensor core
+//     produces C'_b = sum (sc_b*q)*a = sc_b*C_b exactly;
+//   * the epilogue accumulates acc = sum_b dx_b*C'_b over the 8 sub-blocks of
+//     a super-block (dx_b is per token = per TMEM lane, so it is a scalar of
+//     the thread) and adds d*acc into a TMEM-resident running output Y once
+//     per super-block;
+//   * the min term sum_b (dx_b*ssum_b)*(-(dmin*m_b)) is a small GEMM over the
+//     sub-block index (K/32 deep).  It runs on the tensor core in tf32 with
+//     each factor split into a high and a low tf32 part (both exact products
+//     of f16 values and small integers are exact in f32, so the split loses
+//     only the low*low term, ~2^-22 relative), accumulated in its own TMEM
+//     columns across the whole K and added to Y at the end.
+// TMEM columns: [0,256) two sub-block accumulators, [256,384) Y,
+// [384,512) the min-term accumulator.
+// =========================================================================
+namespace q4 {
+
+constexpr int STG = 4;
+constexpr int RSTG = 2;
+constexpr int SSTG = 3;
+constexpr int NACC = 2;
+constexpr uint32_t TM_ACC = 0, TM_Y = 256, TM_MIN = 384;
+constexpr uint32_t RAW_BYTES = BN * 144;
+constexpr uint32_t MIN_OP_BYTES = 128 * 64;                 // 128 rows x 16 tf32 (8 hi, 8 lo)
+constexpr uint32_t SDS_BYTES = 2 * MIN_OP_BYTES + BN * 4;   // A_min, B_min, d[BN]
+constexpr uint32_t oA = 0;
+constexpr uint32_t oB = oA + STG * A_BYTES;
+constexpr uint32_t oRaw = oB + STG * B_BYTES;
+constexpr uint32_t oSds = oRaw + RSTG * RAW_BYTES;
+constexpr uint32_t oBar = oSds + SSTG * SDS_BYTES;
+constexpr int kNumBars = 3 * STG + 2 * RSTG + 2 * SSTG + 2 * NACC + 1;
+constexpr uint32_t oMisc = oBar + kNumBars * 8;
+constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
+static_assert(kDynSmem <= 232448, "shared memory budget");
+static_assert(oSds % 16 == 0 && SDS_BYTES % 16 == 0, "min operands must be 16-byte aligned");
+
+// One row of a min-term operand in the no-swizzle K-major layout: 16 tf32
+// (hi[0..7], lo[0..7]) as four 16-byte core-matrix rows; core matrices are
+// 128 bytes apart along K and 8-row groups 512 bytes apart.
+__device__ __forceinline__ void put_min_row(uint8_t *base, int r, const float (&h)[8], const float (&l)[8])
+{
+    uint8_t *q = base + (r >> 3) * 512 + (r & 7) * 16;
+    *reinterpret_cast<float4 *>(q + 0) = make_float4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<float4 *>(q + 128) = make_float4(h[4], h[5], h[6], h[7]);
+    *reinterpret_cast<float4 *>(q + 256) = make_float4(l[0], l[1], l[2], l[3]);
+    *reinterpret_cast<float4 *>(q + 384) = make_float4(l[4], l[5], l[6], l[7]);
+}
+
+__device__ __forceinline__ uint32_t h2bits(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
+
+// (1024 + q) * m + a for the two nibbles selected into the 16-bit halves
+__device__ __forceinline__ uint32_t nib2(uint32_t w, uint32_t sel, uint32_t mask, __half2 m, __half2 a)
+{
+    const uint32_t pr = __byte_perm(w, 0u, sel);
+    const uint32_t h = (pr & mask) | 0x64006400u;
+    return h2bits(__hfma2(*reinterpret_cast<const __half2 *>(&h), m, a));
+}
+
+}  // namespace q4
+
+__global__ void __maxnreg__(144)
+    mmq_q4K_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                   const Params p)
+{
+    using namespace q4;
+    constexpr int kKid = 7;
+    constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
+    constexpr uint32_t kIdescTf32 = idesc_tf32_f32(BM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o0 = blockIdx.x * BN, t0 = blockIdx.y * BM;
+    const int T = p.T, K = p.K, O = p.O;
+    const int nks = K / BK, nsb = K / 256;
+
+    const uint32_t bar0 = sbase + oBar;
+    auto a_full = [&](int s) { return bar0 + 8u * s; };
+    auto b_full = [&](int s) { return bar0 + 8u * (STG + s); };
+    auto st_empty = [&](int s) { return bar0 + 8u * (2 * STG + s); };
+    auto r_full = [&](int s) { return bar0 + 8u * (3 * STG + s); };
+    auto r_empty = [&](int s) { return bar0 + 8u * (3 * STG + RSTG + s); };
+    auto s_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + s); };
+    auto s_empty = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + SSTG + s); };
+    auto acc_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + s); };
+    auto acc_empty = [&](int s) {
+        return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + NACC + s);
+    };
+    const uint32_t mma_done = bar0 + 8u * (kNumBars - 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + oMisc);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + oMisc + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STG; ++s) {
+            mbar_init(a_full(s), 1);
+            mbar_init(b_full(s), 128);
+            mbar_init(st_empty(s), 1);
+        }
+        for (int s = 0; s < RSTG; ++s) {
+            mbar_init(r_full(s), 1);
+            mbar_init(r_empty(s), 128);
+        }
+        for (int s = 0; s < SSTG; ++s) {
+            mbar_init(s_full(s), 128);
+            mbar_init(s_empty(s), NUM_EPI_WARPS + 1);   // epilogue warps + the MMA's commit
+        }
+        for (int s = 0; s < NACC; ++s) {
+            mbar_init(acc_full(s), 1);
+            mbar_init(acc_empty(s), NUM_EPI_WARPS);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            tma_prefetch(&tmA);
+            tma_prefetch(&tmW);
+        }
+        int n_a = 0, n_r = 0;
+        bool ok = true;
+        for (int ks = 0; ks < nks && ok; ++ks) {
+            if ((ks & 3) == 0) {
+                const int sb = ks >> 2, rs = sb % RSTG;
+                ok = mbar_wait_warp(r_empty(rs), ((sb / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(r_full(rs), RAW_BYTES);
+                    tma_load_2d(sbase + oRaw + rs * RAW_BYTES, &tmW, r_full(rs), sb * 144, o0);
+                }
+                ++n_r;
+            }
+            const int s = ks % STG;
+            ok = mbar_wait_warp(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(a_full(s), A_BYTES);
+                tma_load_2d(sbase + oA + s * A_BYTES, &tmA, a_full(s), ks * BK, t0);
+            }
+            ++n_a;
+            __syncwarp();
+        }
+        if (!ok) {
+            for (int i = max(0, n_a - STG); i < n_a; ++i) wait_drain(a_full(i % STG), (i / STG) & 1);
+            for (int i = max(0, n_r - RSTG); i < n_r; ++i)
+                wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            bool ok = true;
+            int acc = 0;
+            for (int ks = 0; ks < nks && ok; ++ks) {
+                const int s = ks % STG;
+                const uint32_t par = (ks / STG) & 1;
+                ok = mbar_wait(a_full(s), par, abort_flag, kKid, SITE_M_A) &&
+                     mbar_wait(b_full(s), par, abort_flag, kKid, SITE_M_B);
+                if (!ok) break;
+                const int sb = ks >> 2, ss = sb % SSTG;
+                if ((ks & 3) == 0) {
+                    // min term of this super-block: D_min += A_min . B_min^T
+                    ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
+                    const uint32_t dmin = tmem_base + TM_MIN;
+                    umma_tf32(dmin, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32,
+                              sb > 0 ? 1u : 0u);                                              // hi . hi
+                    umma_tf32(dmin, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(dmin, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
+                }
+                tc_fence_after();
+                const uint32_t a_base = sbase + oA + s * A_BYTES;
+                const uint32_t b_base = sbase + oB + s * B_BYTES;
+#pragma unroll
+                for (int g = 0; g < 2; ++g, ++acc) {
+                    const int slot = acc % NACC;
+                    ok = mbar_wait(acc_empty(slot), ((acc / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint32_t koff = (uint32_t)(2 * g + kk) * 32u;
+                        umma_f16(tmem_base + TM_ACC + slot * BN, sdesc_k_sw128(a_base + koff),
+                                 sdesc_k_sw128(b_base + koff), kIdesc, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(acc_full(slot));
+                }
+                if (!ok) break;
+                umma_commit(st_empty(s));
+                if ((ks & 3) == 3) umma_commit(s_empty(ss));
+            }
+            umma_commit(mma_done);
+            if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp < EPI_WARP0) {
+        // ------------------------------------------------------ unpack warps --
+        const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row (B) and token row (A_min)
+        const int t = t0 + r;
+        bool ok = true;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int rs = sb % RSTG, ss = sb % SSTG;
+            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW) &&
+                 mbar_wait(s_empty(ss), ((sb / SSTG) & 1) ^ 1, abort_flag, kKid, SITE_U_SDS);
+            if (!ok) break;
+            const uint8_t *raw = smem + oRaw + rs * RAW_BYTES + r * 144;
+            uint8_t *slot = smem + oSds + ss * SDS_BYTES;
+            const uint4 hd = *reinterpret_cast<const uint4 *>(raw);
+            const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+            const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+            int sc[8], mm[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sc[j] = (hd.y >> (8 * j)) & 63;
+                mm[j] = (hd.z >> (8 * j)) & 63;
+                sc[j + 4] = ((hd.w >> (8 * j)) & 15) | (((hd.y >> (8 * j + 6)) & 3) << 4);
+                mm[j + 4] = ((hd.w >> (8 * j + 4)) & 15) | (((hd.z >> (8 * j + 6)) & 3) << 4);
+            }
+            reinterpret_cast<float *>(slot + 2 * MIN_OP_BYTES)[r] = d;
+            {
+                float h[8], l[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float v = -(dmin * (float)mm[j]);      // exact: 11-bit x 6-bit
+                    h[j] = to_tf32(v);
+                    l[j] = to_tf32(v - h[j]);
+                }
+                put_min_row(slot + MIN_OP_BYTES, r, h, l);
+            }
+            {
+                float h[8], l[8];
+                if (t < T) {
+                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + sb * 8);
+                    const uint4 u0 = __ldg(dp), u1 = __ldg(dp + 1);
+                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float dx = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
+                        const float v = dx * (float)(int)(int16_t)(w[j] >> 16);   // exact: 11-bit x 12-bit
+                        h[j] = to_tf32(v);
+                        l[j] = to_tf32(v - h[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) h[j] = l[j] = 0.0f;
+                }
+                put_min_row(slot, r, h, l);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(s_full(ss));
+
+#pragma unroll
+            for (int p4 = 0; p4 < 4; ++p4) {
+                const int ks = sb * 4 + p4, s = ks % STG;
+                ok = mbar_wait(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
+                if (!ok) break;
+                // sub-block 2*p4 (low nibbles, k 0..31): (1024+q)*sc - 1024*sc
+                // sub-block 2*p4+1 (high nibbles, k 32..63): (1024+16q)*(sc/16) - 64*sc
+                const float slo = (float)sc[2 * p4], shi = (float)sc[2 * p4 + 1];
+                const __half2 mlo = __float2half2_rn(slo), alo = __float2half2_rn(-1024.0f * slo);
+                const __half2 mhi = __float2half2_rn(shi * 0.0625f), ahi = __float2half2_rn(-64.0f * shi);
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4 + 16);
+                const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint8_t *brow = smem + oB + s * B_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t wa = wv[2 * (c & 3)], wb = wv[2 * (c & 3) + 1];
+                    const uint32_t mask = c < 4 ? 0x000F000Fu : 0x00F000F0u;
+                    const __half2 m2 = c < 4 ? mlo : mhi, a2 = c < 4 ? alo : ahi;
+                    uint4 v;
+                    v.x = nib2(wa, 0x4140u, mask, m2, a2);
+                    v.y = nib2(wa, 0x4342u, mask, m2, a2);
+                    v.z = nib2(wb, 0x4140u, mask, m2, a2);
+                    v.w = nib2(wb, 0x4342u, mask, m2, a2);
+                    *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(b_full(s));
+            }
+            if (ok) mbar_arrive(r_empty(rs));
+        }
+    } else {
+        // --------------------------------------------------------- epilogue --
+        const int ew = warp - EPI_WARP0;
+        const int quarter = warp & 3;
+        const int c0 = (ew >> 2) * 64;
+        const int t = t0 + quarter * 32 + lane;
+        const bool tok_ok = t < T;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        float acc[64];
+        bool ok = true;
+        const uint32_t *dsrow = p.ds + (size_t)(tok_ok ? t : 0) * (K / 32);
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int ss = sb % SSTG;
+            uint32_t dsw[8];
+            if (tok_ok) {
+                const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(dsrow + sb * 8));
+                const uint4 u1 = __ldg(reinterpret_cast<const uint4 *>(dsrow + sb * 8) + 1);
+                dsw[0] = u0.x; dsw[1] = u0.y; dsw[2] = u0.z; dsw[3] = u0.w;
+                dsw[4] = u1.x; dsw[5] = u1.y; dsw[6] = u1.z; dsw[7] = u1.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dsw[j] = 0u;
+            }
+            ok = mbar_wait_warp(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
+            if (!ok) break;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const int slot = g & 1;              // accumulator index sb*8+g, two slots
+                ok = mbar_wait_warp(acc_full(slot), (g >> 1) & 1, abort_flag, kKid, SITE_E_ACC);
+                if (!ok) break;
+                tc_fence_after();
+                const float dx = __half2float(__ushort_as_half((unsigned short)(dsw[g] & 0xFFFFu)));
+                const float2 dx2 = make_float2(dx, dx);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t rv[32];
+                    tmem_ld32(tmem_base + lane_off + TM_ACC + slot * BN + c0 + hh * 32, rv);
+                    tmem_ld_wait(rv);
+                    if (hh == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty(slot));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 cv = make_float2(__uint_as_float(rv[i]), __uint_as_float(rv[i + 1]));
+                        float2 a = make_float2(acc[hh * 32 + i], acc[hh * 32 + i + 1]);
+                        a = (g == 0) ? __fmul2_rn(cv, dx2) : __ffma2_rn(cv, dx2, a);
+                        acc[hh * 32 + i] = a.x;
+                        acc[hh * 32 + i + 1] = a.y;
+                    }
+                }
+            }
+            if (!ok) break;
+            // Y += d * acc, with Y resident in TMEM
+            const float *dv = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + 2 * MIN_OP_BYTES) + c0;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t yv[32];
+                const uint32_t ya = tmem_base + lane_off + TM_Y + c0 + hh * 32;
+                if (sb > 0) {
+                    tmem_ld32(ya, yv);
+                    tmem_ld_wait(yv);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dv + hh * 32 + i);
+                    const float2 a0 = make_float2(acc[hh * 32 + i], acc[hh * 32 + i + 1]);
+                    const float2 a1 = make_float2(acc[hh * 32 + i + 2], acc[hh * 32 + i + 3]);
+                    float2 y0, y1;
+                    if (sb > 0) {
+                        y0 = __ffma2_rn(a0, make_float2(d4.x, d4.y),
+                                        make_float2(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1])));
+                        y1 = __ffma2_rn(a1, make_float2(d4.z, d4.w),
+                                        make_float2(__uint_as_float(yv[i + 2]), __uint_as_float(yv[i + 3])));
+                    } else {
+                        y0 = __fmul2_rn(a0, make_float2(d4.x, d4.y));
+                        y1 = __fmul2_rn(a1, make_float2(d4.z, d4.w));
+                    }
+                    yv[i] = __float_as_uint(y0.x);
+                    yv[i + 1] = __float_as_uint(y0.y);
+                    yv[i + 2] = __float_as_uint(y1.x);
+                    yv[i + 3] = __float_as_uint(y1.y);
+                }
+                tmem_st32(ya, yv);
+            }
+            tmem_st_wait();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty(ss));
+        }
+        if (ok) {
+            // Y + min term -> global
+            float *yrow = p.y + (size_t)(tok_ok ? t : 0) * O + o0 + c0;
+            const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t yv[32], mv[32];
+                tmem_ld32(tmem_base + lane_off + TM_Y + c0 + hh * 32, yv);
+                tmem_ld32(tmem_base + lane_off + TM_MIN + c0 + hh * 32, mv);
+                tmem_ld_wait(yv);
+                tmem_ld_wait(mv);
+                if (tok_ok) {
+                    if (vec) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(yrow + hh * 32 + i) =
+                                make_float4(__uint_as_float(yv[i]) + __uint_as_float(mv[i]),
+                                            __uint_as_float(yv[i + 1]) + __uint_as_float(mv[i + 1]),
+                                            __uint_as_float(yv[i + 2]) + __uint_as_float(mv[i + 2]),
+                                            __uint_as_float(yv[i + 3]) + __uint_as_float(mv[i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (o0 + c0 + hh * 32 + i < O)
+                                yrow[hh * 32 + i] = __uint_as_float(yv[i]) + __uint_as_float(mv[i]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
 template <int FMT, int MODE>
 int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int32_t *sub, int T, int O, int K,
            mmq_stream_t stream)
@@ -541,7 +971,9 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
         std::memset(&tmW, 0, sizeof(tmW));   // q6_K stages its rows with plain bulk copies
     }
 
-    auto kern = mmq_gemm_kernel<FMT, MODE>;
+    const bool prod_q4K = (FMT == kQ4K && MODE == kFold);
+    auto kern = prod_q4K ? mmq_q4K_kernel : mmq_gemm_kernel<FMT, MODE>;
+    const uint32_t dyn_smem = prod_q4K ? q4::kDynSmem : L::kDynSmem;
     // the shared-memory attribute is set once per device (keeps the launch
     // path free of attribute calls, e.g. while a stream is being captured)
     static bool attr_done[64];
@@ -549,7 +981,7 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) != cudaSuccess)
             return launch_status();
         attr_done[dev] = true;
     }
@@ -562,7 +994,7 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
     prm.O = O;
     prm.K = K;
     const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM));
-    kern<<<grid, NUM_THREADS, L::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
+    kern<<<grid, NUM_THREADS, dyn_smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
     return launch_status();
 }
 
