@@ -580,7 +580,7 @@ __device__ __forceinline__ uint32_t nib2(uint32_t w, uint32_t sel, uint32_t mask
 
 }  // namespace q4
 
-__global__ void __maxnreg__(144)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     mmq_q4K_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const Params p)
 {
