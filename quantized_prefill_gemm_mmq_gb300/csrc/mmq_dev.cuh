@@ -100,13 +100,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Warp-collective form: every lane waits, and the result is made uniform
-// across the warp so that warp-synchronous code after it never diverges.
+// Warp-collective form: lane 0 polls, the result is broadcast, and the warp
+// reconverges, so that warp-synchronous code after it never diverges (the
+// other lanes are ordered after lane 0's acquire by the warp barrier).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
                                                int kernel_id, int site)
 {
-    const bool ok = mbar_wait(bar, parity, abort, kernel_id, site);
-    return __all_sync(0xffffffffu, ok);
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, kernel_id, site);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // -------------------------------------------------------------------- TMA --

@@ -544,7 +544,7 @@ constexpr int NACC = 2;
 constexpr uint32_t TM_ACC = 0, TM_Y = 256, TM_MIN = 384;
 constexpr uint32_t RAW_BYTES = BN * 144;
 constexpr uint32_t MIN_OP_BYTES = 128 * 64;                 // 128 rows x 16 tf32 (8 hi, 8 lo)
-constexpr uint32_t SDS_BYTES = 2 * MIN_OP_BYTES + BN * 4;   // A_min, B_min, d[BN]
+constexpr uint32_t SDS_BYTES = 2 * MIN_OP_BYTES + BN * 4 + 8 * BM * 4;   // A_min, B_min, d[BN], dx[8][BM]
 constexpr uint32_t oA = 0;
 constexpr uint32_t oB = oA + STG * A_BYTES;
 constexpr uint32_t oRaw = oB + STG * B_BYTES;
@@ -691,18 +691,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      mbar_wait(b_full(s), par, abort_flag, kKid, SITE_M_B);
                 if (!ok) break;
                 const int sb = ks >> 2, ss = sb % SSTG;
-                if ((ks & 3) == 0) {
-                    // min term of this super-block: D_min += A_min . B_min^T
-                    ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
-                    const uint32_t dmin = tmem_base + TM_MIN;
-                    umma_tf32(dmin, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32,
-                              sb > 0 ? 1u : 0u);                                              // hi . hi
-                    umma_tf32(dmin, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
-                    umma_tf32(dmin, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
-                }
                 tc_fence_after();
                 const uint32_t a_base = sbase + oA + s * A_BYTES;
                 const uint32_t b_base = sbase + oB + s * B_BYTES;
@@ -722,7 +710,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
                 umma_commit(st_empty(s));
-                if ((ks & 3) == 3) umma_commit(s_empty(ss));
+                if ((ks & 3) == 3) {
+                    // min term of this super-block: D_min += A_min . B_min^T
+                    ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
+                    const uint32_t dmn = tmem_base + TM_MIN;
+                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32,
+                              sb > 0 ? 1u : 0u);                                              // hi . hi
+                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(dmn, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
+                    umma_commit(s_empty(ss));
+                }
             }
             umma_commit(mma_done);
             if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
@@ -732,6 +732,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------ unpack warps --
         const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row (B) and token row (A_min)
         const int t = t0 + r;
+        uint4 dsn0 = make_uint4(0u, 0u, 0u, 0u), dsn1 = dsn0;
+        if (t < T) {
+            const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32));
+            dsn0 = __ldg(dp);
+            dsn1 = __ldg(dp + 1);
+        }
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int rs = sb % RSTG, ss = sb % SSTG;
@@ -764,22 +770,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             {
                 float h[8], l[8];
-                if (t < T) {
-                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + sb * 8);
-                    const uint4 u0 = __ldg(dp), u1 = __ldg(dp + 1);
-                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                float *dxs = reinterpret_cast<float *>(slot + 2 * MIN_OP_BYTES + BN * 4);
+                const uint32_t w[8] = {dsn0.x, dsn0.y, dsn0.z, dsn0.w, dsn1.x, dsn1.y, dsn1.z, dsn1.w};
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float dx = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
-                        const float v = dx * (float)(int)(int16_t)(w[j] >> 16);   // exact: 11-bit x 12-bit
-                        h[j] = to_tf32(v);
-                        l[j] = to_tf32(v - h[j]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) h[j] = l[j] = 0.0f;
+                for (int j = 0; j < 8; ++j) {
+                    const float dx = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
+                    const float v = dx * (float)(int)(int16_t)(w[j] >> 16);   // exact: 11-bit x 12-bit
+                    h[j] = to_tf32(v);
+                    l[j] = to_tf32(v - h[j]);
+                    dxs[j * BM + r] = dx;
                 }
                 put_min_row(slot, r, h, l);
+                // next super-block's scale words, loaded while this one is unpacked
+                if (t < T && sb + 1 < nsb) {
+                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + (sb + 1) * 8);
+                    dsn0 = __ldg(dp);
+                    dsn1 = __ldg(dp + 1);
+                }
             }
             fence_proxy_async_smem();
             mbar_arrive(s_full(ss));
@@ -825,28 +832,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         float acc[64];
         bool ok = true;
-        const uint32_t *dsrow = p.ds + (size_t)(tok_ok ? t : 0) * (K / 32);
+        const int tl = quarter * 32 + lane;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int ss = sb % SSTG;
-            uint32_t dsw[8];
-            if (tok_ok) {
-                const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(dsrow + sb * 8));
-                const uint4 u1 = __ldg(reinterpret_cast<const uint4 *>(dsrow + sb * 8) + 1);
-                dsw[0] = u0.x; dsw[1] = u0.y; dsw[2] = u0.z; dsw[3] = u0.w;
-                dsw[4] = u1.x; dsw[5] = u1.y; dsw[6] = u1.z; dsw[7] = u1.w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) dsw[j] = 0u;
-            }
             ok = mbar_wait_warp(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
             if (!ok) break;
+            const float *dxs = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + 2 * MIN_OP_BYTES + BN * 4);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
                 const int slot = g & 1;              // accumulator index sb*8+g, two slots
                 ok = mbar_wait_warp(acc_full(slot), (g >> 1) & 1, abort_flag, kKid, SITE_E_ACC);
                 if (!ok) break;
                 tc_fence_after();
-                const float dx = __half2float(__ushort_as_half((unsigned short)(dsw[g] & 0xFFFFu)));
+                const float dx = dxs[g * BM + tl];
                 const float2 dx2 = make_float2(dx, dx);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
