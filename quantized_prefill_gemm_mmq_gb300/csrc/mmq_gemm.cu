@@ -540,8 +540,10 @@ namespace q4 {
 constexpr int STG = 4;
 constexpr int RSTG = 2;
 constexpr int SSTG = 3;
-constexpr int NACC = 2;
-constexpr uint32_t TM_ACC = 0, TM_Y = 256, TM_MIN = 384;
+constexpr int NACC = 3;                          // rotating accumulators (BN columns each)
+constexpr int ACC_PER_SB = 9;                    // 8 sub-blocks + the min term, per super-block
+constexpr uint32_t TM_ACC = 0, TM_Y = NACC * BN;  // Y after the accumulators
+static_assert(TM_Y + BN <= 512, "TMEM budget");
 constexpr uint32_t RAW_BYTES = BN * 144;
 constexpr uint32_t MIN_OP_BYTES = 128 * 64;                 // 128 rows x 16 tf32 (8 hi, 8 lo)
 constexpr uint32_t SDS_BYTES = 2 * MIN_OP_BYTES + BN * 4 + 8 * BM * 4;   // A_min, B_min, d[BN], dx[8][BM]
@@ -681,6 +683,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer --
+        // accumulator sequence per super-block: sub-blocks 0..7, then the min
+        // term; accumulator n lives in slot n % NACC
         if (lane == 0) {
             bool ok = true;
             int acc = 0;
@@ -711,24 +715,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!ok) break;
                 umma_commit(st_empty(s));
                 if ((ks & 3) == 3) {
-                    // min term of this super-block: D_min += A_min . B_min^T
-                    ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
+                    // min term of this super-block: A_min . B_min^T as three
+                    // split-tf32 products (hi.hi + hi.lo + lo.hi)
+                    const int slot = acc % NACC;
+                    ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS) &&
+                         mbar_wait(acc_empty(slot), ((acc / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
-                    const uint32_t dmn = tmem_base + TM_MIN;
-                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32,
-                              sb > 0 ? 1u : 0u);                                              // hi . hi
+                    const uint32_t dmn = tmem_base + TM_ACC + slot * BN;
+                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 0u);
                     umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
                     umma_tf32(dmn, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
+                    umma_commit(acc_full(slot));
                     umma_commit(s_empty(ss));
+                    ++acc;
                 }
             }
             umma_commit(mma_done);
             if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
         }
         __syncwarp();
-    } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------ unpack warps --
         const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row (B) and token row (A_min)
         const int t = t0 + r;
@@ -824,15 +831,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // --------------------------------------------------------- epilogue --
+        // Thread = one token (TMEM lane) x 64 weight rows (columns).
+        //   per sub-block b:   acc += dx_b * C'_b            (packed FMA)
+        //   per super-block:   Y = Y + d*acc + min      (Y kept in TMEM; the last
+        //                      super-block writes Y to global memory instead)
         const int ew = warp - EPI_WARP0;
         const int quarter = warp & 3;
         const int c0 = (ew >> 2) * 64;
         const int t = t0 + quarter * 32 + lane;
         const bool tok_ok = t < T;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const int tl = quarter * 32 + lane;
         float acc[64];
         bool ok = true;
-        const int tl = quarter * 32 + lane;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int ss = sb % SSTG;
             ok = mbar_wait_warp(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
@@ -840,8 +851,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float *dxs = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + 2 * MIN_OP_BYTES + BN * 4);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
-                const int slot = g & 1;              // accumulator index sb*8+g, two slots
-                ok = mbar_wait_warp(acc_full(slot), (g >> 1) & 1, abort_flag, kKid, SITE_E_ACC);
+                const int slot = g % NACC;                   // accumulator 9*sb + g
+                ok = mbar_wait_warp(acc_full(slot), (sb + g / NACC) & 1, abort_flag, kKid, SITE_E_ACC);
                 if (!ok) break;
                 tc_fence_after();
                 const float dx = dxs[g * BM + tl];
@@ -867,69 +878,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            // Y += d * acc, with Y resident in TMEM
+            // the min-term accumulator (9th of the super-block, always slot 8 % NACC)
+            constexpr int kMinSlot = 8 % NACC;
+            ok = mbar_wait_warp(acc_full(kMinSlot), (sb + 8 / NACC) & 1, abort_flag, kKid, SITE_E_ACC);
+            if (!ok) break;
+            tc_fence_after();
             const float *dv = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + 2 * MIN_OP_BYTES) + c0;
+            const bool last = sb == nsb - 1;
+            float *yrow = p.y + (size_t)(tok_ok ? t : 0) * O + o0 + c0;
+            const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t yv[32];
-                const uint32_t ya = tmem_base + lane_off + TM_Y + c0 + hh * 32;
-                if (sb > 0) {
-                    tmem_ld32(ya, yv);
-                    tmem_ld_wait(yv);
+            for (int q = 0; q < 4; ++q) {          // 16-column chunks: Y = Y + d*acc + min
+                uint32_t yv[16], mv[16];
+                const uint32_t col = c0 + q * 16;
+                tmem_ld16(tmem_base + lane_off + TM_ACC + kMinSlot * BN + col, mv);
+                if (sb > 0) tmem_ld16(tmem_base + lane_off + TM_Y + col, yv);
+                else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) yv[i] = 0u;
                 }
+                tmem_ld_wait2(mv, yv);
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(dv + hh * 32 + i);
-                    const float2 a0 = make_float2(acc[hh * 32 + i], acc[hh * 32 + i + 1]);
-                    const float2 a1 = make_float2(acc[hh * 32 + i + 2], acc[hh * 32 + i + 3]);
-                    float2 y0, y1;
-                    if (sb > 0) {
-                        y0 = __ffma2_rn(a0, make_float2(d4.x, d4.y),
-                                        make_float2(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1])));
-                        y1 = __ffma2_rn(a1, make_float2(d4.z, d4.w),
-                                        make_float2(__uint_as_float(yv[i + 2]), __uint_as_float(yv[i + 3])));
-                    } else {
-                        y0 = __fmul2_rn(a0, make_float2(d4.x, d4.y));
-                        y1 = __fmul2_rn(a1, make_float2(d4.z, d4.w));
-                    }
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dv + q * 16 + i);
+                    const float2 y0 = __ffma2_rn(make_float2(acc[q * 16 + i], acc[q * 16 + i + 1]),
+                                                 make_float2(d4.x, d4.y),
+                                                 make_float2(__uint_as_float(yv[i]) + __uint_as_float(mv[i]),
+                                                             __uint_as_float(yv[i + 1]) + __uint_as_float(mv[i + 1])));
+                    const float2 y1 = __ffma2_rn(make_float2(acc[q * 16 + i + 2], acc[q * 16 + i + 3]),
+                                                 make_float2(d4.z, d4.w),
+                                                 make_float2(__uint_as_float(yv[i + 2]) + __uint_as_float(mv[i + 2]),
+                                                             __uint_as_float(yv[i + 3]) + __uint_as_float(mv[i + 3])));
                     yv[i] = __float_as_uint(y0.x);
                     yv[i + 1] = __float_as_uint(y0.y);
                     yv[i + 2] = __float_as_uint(y1.x);
                     yv[i + 3] = __float_as_uint(y1.y);
                 }
-                tmem_st32(ya, yv);
-            }
-            tmem_st_wait();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty(ss));
-        }
-        if (ok) {
-            // Y + min term -> global
-            float *yrow = p.y + (size_t)(tok_ok ? t : 0) * O + o0 + c0;
-            const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t yv[32], mv[32];
-                tmem_ld32(tmem_base + lane_off + TM_Y + c0 + hh * 32, yv);
-                tmem_ld32(tmem_base + lane_off + TM_MIN + c0 + hh * 32, mv);
-                tmem_ld_wait(yv);
-                tmem_ld_wait(mv);
-                if (tok_ok) {
+                if (!last) {
+                    tmem_st16(tmem_base + lane_off + TM_Y + col, yv);
+                } else if (tok_ok) {
                     if (vec) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(yrow + hh * 32 + i) =
-                                make_float4(__uint_as_float(yv[i]) + __uint_as_float(mv[i]),
-                                            __uint_as_float(yv[i + 1]) + __uint_as_float(mv[i + 1]),
-                                            __uint_as_float(yv[i + 2]) + __uint_as_float(mv[i + 2]),
-                                            __uint_as_float(yv[i + 3]) + __uint_as_float(mv[i + 3]));
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(yrow + q * 16 + i) =
+                                make_float4(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1]),
+                                            __uint_as_float(yv[i + 2]), __uint_as_float(yv[i + 3]));
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (o0 + c0 + hh * 32 + i < O)
-                                yrow[hh * 32 + i] = __uint_as_float(yv[i]) + __uint_as_float(mv[i]);
+                        for (int i = 0; i < 16; ++i)
+                            if (o0 + c0 + q * 16 + i < O) yrow[q * 16 + i] = __uint_as_float(yv[i]);
                     }
                 }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(acc_empty(kMinSlot));
+                mbar_arrive(s_empty(ss));
             }
         }
     }
