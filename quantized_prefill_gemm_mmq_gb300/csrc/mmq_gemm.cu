@@ -736,6 +736,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
         }
         __syncwarp();
+    } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------ unpack warps --
         const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row (B) and token row (A_min)
         const int t = t0 + r;
