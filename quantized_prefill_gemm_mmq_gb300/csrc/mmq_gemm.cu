@@ -517,45 +517,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // =========================================================================
 // q4_K GEMM, production form.
 //
-// Same pipeline as above, with the fold restructured so that the per-(token,
-// row, sub-block) work left on the CUDA cores is one packed FMA:
-//   * the unpack warps multiply each 4-bit quant by its 6-bit sub-block scale
+// Same data flow as above, restructured so that the per-(token, row,
+// sub-block) work left on the CUDA cores is one packed FMA and no role waits
+// on another's bookkeeping:
+//   * unpack warps multiply each 4-bit quant by its 6-bit sub-block scale
 //     while converting it (sc*q <= 945 is exact in f16), so the tensor core
 //     produces C'_b = sum (sc_b*q)*a = sc_b*C_b exactly;
 //   * the epilogue accumulates acc = sum_b dx_b*C'_b over the 8 sub-blocks of
-//     a super-block (dx_b is per token = per TMEM lane, so it is a scalar of
-//     the thread) and adds d*acc into a TMEM-resident running output Y once
-//     per super-block;
-//   * the min term sum_b (dx_b*ssum_b)*(-(dmin*m_b)) is a small GEMM over the
-//     sub-block index (K/32 deep).  It runs on the tensor core in tf32 with
-//     each factor split into a high and a low tf32 part (both exact products
-//     of f16 values and small integers are exact in f32, so the split loses
-//     only the low*low term, ~2^-22 relative), accumulated in its own TMEM
-//     columns across the whole K and added to Y at the end.
-// TMEM columns: [0,256) two sub-block accumulators, [256,384) Y,
-// [384,512) the min-term accumulator.
+//     a super-block (dx_b is per token = per TMEM lane, a scalar of the
+//     thread) and adds d*acc into the running output Y once per super-block;
+//   * the min term sum_b (dx_b*ssum_b)*(-(dmin*m_b)) is a GEMM over the
+//     sub-block index.  It runs on the tensor core in tf32 with each factor
+//     split into a high and a low tf32 part (both factors are exact f32
+//     products of an f16 value and a small integer, so the split loses only
+//     the low*low term, ~2^-22 relative) and accumulates straight into Y's
+//     TMEM columns: the first super-block's min term also initialises Y;
+//   * two scale warps build the min-term operands and the per-row d and
+//     per-token dx of super-block sb+1 while sb is being multiplied.
+// TMEM columns: [0,384) three rotating sub-block accumulators, [384,512) Y.
+// Warps: 0 TMA producer, 1 MMA issuer, 2-5 unpack, 6-13 epilogue, 14-15 scale.
 // =========================================================================
 namespace q4 {
 
-constexpr int STG = 4;
-constexpr int RSTG = 2;
-constexpr int SSTG = 3;
-constexpr int NACC = 3;                          // rotating accumulators (BN columns each)
-constexpr int ACC_PER_SB = 9;                    // 8 sub-blocks + the min term, per super-block
-constexpr uint32_t TM_ACC = 0, TM_Y = NACC * BN;  // Y after the accumulators
+constexpr int NWARPS = 16;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int SCALE_WARP0 = 14;
+constexpr int STG = 4;                           // operand ring (A and B tiles)
+constexpr int RSTG = 3;                          // raw super-block ring
+constexpr int SSTG = 2;                          // scale / min-operand ring
+constexpr int NACC = 3;                          // rotating sub-block accumulators
+constexpr uint32_t TM_ACC = 0, TM_Y = NACC * BN;
 static_assert(TM_Y + BN <= 512, "TMEM budget");
 constexpr uint32_t RAW_BYTES = BN * 144;
-constexpr uint32_t MIN_OP_BYTES = 128 * 64;                 // 128 rows x 16 tf32 (8 hi, 8 lo)
-constexpr uint32_t SDS_BYTES = 2 * MIN_OP_BYTES + BN * 4 + 8 * BM * 4;   // A_min, B_min, d[BN], dx[8][BM]
+constexpr uint32_t MIN_OP_BYTES = 128 * 64;                       // 128 rows x 16 tf32 (8 hi, 8 lo)
+constexpr uint32_t SDS_D = 2 * MIN_OP_BYTES;                      // d[BN] f32
+constexpr uint32_t SDS_DX = SDS_D + BN * 4;                       // dx[8][BM] f32
+constexpr uint32_t SDS_BYTES = SDS_DX + 8 * BM * 4;
 constexpr uint32_t oA = 0;
 constexpr uint32_t oB = oA + STG * A_BYTES;
 constexpr uint32_t oRaw = oB + STG * B_BYTES;
 constexpr uint32_t oSds = oRaw + RSTG * RAW_BYTES;
 constexpr uint32_t oBar = oSds + SSTG * SDS_BYTES;
-constexpr int kNumBars = 3 * STG + 2 * RSTG + 2 * SSTG + 2 * NACC + 1;
+// a_full, b_full, st_empty [STG]; r_full, r_empty [RSTG]; s_full, s_empty
+// [SSTG]; acc_full, acc_empty [NACC]; y_ready, y_free; mma_done
+constexpr int kNumBars = 3 * STG + 2 * RSTG + 2 * SSTG + 2 * NACC + 3;
 constexpr uint32_t oMisc = oBar + kNumBars * 8;
 constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
 static_assert(kDynSmem <= 232448, "shared memory budget");
+static_assert(oRaw % 1024 == 0 && RAW_BYTES % 1024 == 0, "raw ring alignment");
 static_assert(oSds % 16 == 0 && SDS_BYTES % 16 == 0, "min operands must be 16-byte aligned");
 
 // One row of a min-term operand in the no-swizzle K-major layout: 16 tf32
@@ -580,9 +589,23 @@ __device__ __forceinline__ uint32_t nib2(uint32_t w, uint32_t sel, uint32_t mask
     return h2bits(__hfma2(*reinterpret_cast<const __half2 *>(&h), m, a));
 }
 
+// the 6-bit scale (sc) and min (mm) of sub-block j from the 12 packed bytes
+// held in three words s0 (bytes 0-3), s1 (4-7), s2 (8-11)
+__device__ __forceinline__ void q4K_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int &sc, int &mm)
+{
+    if (j < 4) {
+        sc = (s0 >> (8 * j)) & 63;
+        mm = (s1 >> (8 * j)) & 63;
+    } else {
+        const int i = j - 4;
+        sc = ((s2 >> (8 * i)) & 15) | (((s0 >> (8 * i + 6)) & 3) << 4);
+        mm = ((s2 >> (8 * i + 4)) & 15) | (((s1 >> (8 * i + 6)) & 3) << 4);
+    }
+}
+
 }  // namespace q4
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(q4::NTHREADS, 1)
     mmq_q4K_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                    const Params p)
 {
@@ -609,9 +632,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto s_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + s); };
     auto s_empty = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + SSTG + s); };
     auto acc_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + s); };
-    auto acc_empty = [&](int s) {
-        return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + NACC + s);
-    };
+    auto acc_empty = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + NACC + s); };
+    const uint32_t y_ready = bar0 + 8u * (kNumBars - 3);
+    const uint32_t y_free = bar0 + 8u * (kNumBars - 2);
     const uint32_t mma_done = bar0 + 8u * (kNumBars - 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + oMisc);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + oMisc + 4);
@@ -624,16 +647,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int s = 0; s < RSTG; ++s) {
             mbar_init(r_full(s), 1);
-            mbar_init(r_empty(s), 128);
+            mbar_init(r_empty(s), 128 + 64);                // unpack and scale threads
         }
         for (int s = 0; s < SSTG; ++s) {
-            mbar_init(s_full(s), 128);
-            mbar_init(s_empty(s), NUM_EPI_WARPS + 1);   // epilogue warps + the MMA's commit
+            mbar_init(s_full(s), 64);                       // scale threads
+            mbar_init(s_empty(s), NUM_EPI_WARPS + 1);       // epilogue warps + the MMA's commit
         }
         for (int s = 0; s < NACC; ++s) {
             mbar_init(acc_full(s), 1);
             mbar_init(acc_empty(s), NUM_EPI_WARPS);
         }
+        mbar_init(y_ready, 1);
+        mbar_init(y_free, NUM_EPI_WARPS);
         mbar_init(mma_done, 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -649,22 +674,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer --
+        // raw super-block sb+1 is requested when stage 4*sb is, so its scales
+        // can be prepared a super-block ahead of the multiplications
         if (lane == 0) {
             tma_prefetch(&tmA);
             tma_prefetch(&tmW);
         }
         int n_a = 0, n_r = 0;
         bool ok = true;
+        auto issue_raw = [&](int sb) -> bool {
+            const int rs = sb % RSTG;
+            if (!mbar_wait_warp(r_empty(rs), ((sb / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW)) return false;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(r_full(rs), RAW_BYTES);
+                tma_load_2d(sbase + oRaw + rs * RAW_BYTES, &tmW, r_full(rs), sb * 144, o0);
+            }
+            ++n_r;
+            return true;
+        };
+        ok = issue_raw(0);
         for (int ks = 0; ks < nks && ok; ++ks) {
-            if ((ks & 3) == 0) {
-                const int sb = ks >> 2, rs = sb % RSTG;
-                ok = mbar_wait_warp(r_empty(rs), ((sb / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
+            if ((ks & 3) == 0 && (ks >> 2) + 1 < nsb) {
+                ok = issue_raw((ks >> 2) + 1);
                 if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(r_full(rs), RAW_BYTES);
-                    tma_load_2d(sbase + oRaw + rs * RAW_BYTES, &tmW, r_full(rs), sb * 144, o0);
-                }
-                ++n_r;
             }
             const int s = ks % STG;
             ok = mbar_wait_warp(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
@@ -678,23 +710,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) {
             for (int i = max(0, n_a - STG); i < n_a; ++i) wait_drain(a_full(i % STG), (i / STG) & 1);
-            for (int i = max(0, n_r - RSTG); i < n_r; ++i)
-                wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
+            for (int i = max(0, n_r - RSTG); i < n_r; ++i) wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer --
-        // accumulator sequence per super-block: sub-blocks 0..7, then the min
-        // term; accumulator n lives in slot n % NACC
         if (lane == 0) {
             bool ok = true;
-            int acc = 0;
+            int acc = 0;   // sub-block accumulator n lives in slot n % NACC
             for (int ks = 0; ks < nks && ok; ++ks) {
                 const int s = ks % STG;
                 const uint32_t par = (ks / STG) & 1;
                 ok = mbar_wait(a_full(s), par, abort_flag, kKid, SITE_M_A) &&
                      mbar_wait(b_full(s), par, abort_flag, kKid, SITE_M_B);
                 if (!ok) break;
-                const int sb = ks >> 2, ss = sb % SSTG;
                 tc_fence_after();
                 const uint32_t a_base = sbase + oA + s * A_BYTES;
                 const uint32_t b_base = sbase + oB + s * B_BYTES;
@@ -715,21 +743,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!ok) break;
                 umma_commit(st_empty(s));
                 if ((ks & 3) == 3) {
-                    // min term of this super-block: A_min . B_min^T as three
-                    // split-tf32 products (hi.hi + hi.lo + lo.hi)
-                    const int slot = acc % NACC;
+                    // min term of super-block sb straight into Y:
+                    // Y (+)= A_min . B_min^T as hi.hi + hi.lo + lo.hi
+                    const int sb = ks >> 2, ss = sb % SSTG;
                     ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS) &&
-                         mbar_wait(acc_empty(slot), ((acc / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC);
+                         (sb == 0 || mbar_wait(y_free, (sb - 1) & 1, abort_flag, kKid, SITE_M_ACC));
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
-                    const uint32_t dmn = tmem_base + TM_ACC + slot * BN;
-                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 0u);
-                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
-                    umma_tf32(dmn, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
-                    umma_commit(acc_full(slot));
+                    const uint32_t ya = tmem_base + TM_Y;
+                    umma_tf32(ya, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32,
+                              sb > 0 ? 1u : 0u);
+                    umma_tf32(ya, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(ya, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
+                    umma_commit(y_ready);
                     umma_commit(s_empty(ss));
-                    ++acc;
                 }
             }
             umma_commit(mma_done);
@@ -738,79 +766,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
     } else if (warp < EPI_WARP0) {
         // ------------------------------------------------------ unpack warps --
-        const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row (B) and token row (A_min)
-        const int t = t0 + r;
-        uint4 dsn0 = make_uint4(0u, 0u, 0u, 0u), dsn1 = dsn0;
-        if (t < T) {
-            const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32));
-            dsn0 = __ldg(dp);
-            dsn1 = __ldg(dp + 1);
-        }
+        const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row of the B tile
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
-            const int rs = sb % RSTG, ss = sb % SSTG;
-            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW) &&
-                 mbar_wait(s_empty(ss), ((sb / SSTG) & 1) ^ 1, abort_flag, kKid, SITE_U_SDS);
+            const int rs = sb % RSTG;
+            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW);
             if (!ok) break;
             const uint8_t *raw = smem + oRaw + rs * RAW_BYTES + r * 144;
-            uint8_t *slot = smem + oSds + ss * SDS_BYTES;
             const uint4 hd = *reinterpret_cast<const uint4 *>(raw);
-            const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
-            const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-            int sc[8], mm[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                sc[j] = (hd.y >> (8 * j)) & 63;
-                mm[j] = (hd.z >> (8 * j)) & 63;
-                sc[j + 4] = ((hd.w >> (8 * j)) & 15) | (((hd.y >> (8 * j + 6)) & 3) << 4);
-                mm[j + 4] = ((hd.w >> (8 * j + 4)) & 15) | (((hd.z >> (8 * j + 6)) & 3) << 4);
-            }
-            reinterpret_cast<float *>(slot + 2 * MIN_OP_BYTES)[r] = d;
-            {
-                float h[8], l[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float v = -(dmin * (float)mm[j]);      // exact: 11-bit x 6-bit
-                    h[j] = to_tf32(v);
-                    l[j] = to_tf32(v - h[j]);
-                }
-                put_min_row(slot + MIN_OP_BYTES, r, h, l);
-            }
-            {
-                float h[8], l[8];
-                float *dxs = reinterpret_cast<float *>(slot + 2 * MIN_OP_BYTES + BN * 4);
-                const uint32_t w[8] = {dsn0.x, dsn0.y, dsn0.z, dsn0.w, dsn1.x, dsn1.y, dsn1.z, dsn1.w};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float dx = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
-                    const float v = dx * (float)(int)(int16_t)(w[j] >> 16);   // exact: 11-bit x 12-bit
-                    h[j] = to_tf32(v);
-                    l[j] = to_tf32(v - h[j]);
-                    dxs[j * BM + r] = dx;
-                }
-                put_min_row(slot, r, h, l);
-                // next super-block's scale words, loaded while this one is unpacked
-                if (t < T && sb + 1 < nsb) {
-                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + (sb + 1) * 8);
-                    dsn0 = __ldg(dp);
-                    dsn1 = __ldg(dp + 1);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(s_full(ss));
-
 #pragma unroll
             for (int p4 = 0; p4 < 4; ++p4) {
                 const int ks = sb * 4 + p4, s = ks % STG;
-                ok = mbar_wait(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
-                if (!ok) break;
+                int sc_lo, sc_hi, unused;
+                q4K_scale_min(hd.y, hd.z, hd.w, 2 * p4, sc_lo, unused);
+                q4K_scale_min(hd.y, hd.z, hd.w, 2 * p4 + 1, sc_hi, unused);
                 // sub-block 2*p4 (low nibbles, k 0..31): (1024+q)*sc - 1024*sc
                 // sub-block 2*p4+1 (high nibbles, k 32..63): (1024+16q)*(sc/16) - 64*sc
-                const float slo = (float)sc[2 * p4], shi = (float)sc[2 * p4 + 1];
+                const float slo = (float)sc_lo, shi = (float)sc_hi;
                 const __half2 mlo = __float2half2_rn(slo), alo = __float2half2_rn(-1024.0f * slo);
                 const __half2 mhi = __float2half2_rn(shi * 0.0625f), ahi = __float2half2_rn(-64.0f * shi);
                 const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4);
                 const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4 + 16);
+                ok = mbar_wait(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
+                if (!ok) break;
                 const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                 uint8_t *brow = smem + oB + s * B_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
@@ -830,30 +808,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (ok) mbar_arrive(r_empty(rs));
         }
-    } else {
+    } else if (warp < SCALE_WARP0) {
         // --------------------------------------------------------- epilogue --
         // Thread = one token (TMEM lane) x 64 weight rows (columns).
-        //   per sub-block b:   acc += dx_b * C'_b            (packed FMA)
-        //   per super-block:   Y = Y + d*acc + min      (Y kept in TMEM; the last
-        //                      super-block writes Y to global memory instead)
+        //   per sub-block b:  acc += dx_b * C'_b             (packed FMA)
+        //   per super-block:  Y = Y + d*acc  with Y in TMEM already holding
+        //                     the min terms; the last super-block writes Y
+        //                     to global memory instead
         const int ew = warp - EPI_WARP0;
         const int quarter = warp & 3;
         const int c0 = (ew >> 2) * 64;
-        const int t = t0 + quarter * 32 + lane;
+        const int tl = quarter * 32 + lane;
+        const int t = t0 + tl;
         const bool tok_ok = t < T;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const int tl = quarter * 32 + lane;
         float acc[64];
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int ss = sb % SSTG;
             ok = mbar_wait_warp(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
             if (!ok) break;
-            const float *dxs = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + 2 * MIN_OP_BYTES + BN * 4);
+            const float *dxs = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + SDS_DX);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
-                const int slot = g % NACC;                   // accumulator 9*sb + g
-                ok = mbar_wait_warp(acc_full(slot), (sb + g / NACC) & 1, abort_flag, kKid, SITE_E_ACC);
+                const int n = sb * 8 + g;
+                const int slot = n % NACC;
+                ok = mbar_wait_warp(acc_full(slot), (n / NACC) & 1, abort_flag, kKid, SITE_E_ACC);
                 if (!ok) break;
                 tc_fence_after();
                 const float dx = dxs[g * BM + tl];
@@ -861,7 +841,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t rv[32];
-                    tmem_ld32(tmem_base + lane_off + TM_ACC + slot * BN + c0 + hh * 32, rv);
+                    tmem_ld32(tmem_base + lane_off + TM_ACC + (uint32_t)(slot * BN + c0 + hh * 32), rv);
                     tmem_ld_wait(rv);
                     if (hh == 1) {
                         tc_fence_before();
@@ -879,44 +859,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            // the min-term accumulator (9th of the super-block, always slot 8 % NACC)
-            constexpr int kMinSlot = 8 % NACC;
-            ok = mbar_wait_warp(acc_full(kMinSlot), (sb + 8 / NACC) & 1, abort_flag, kKid, SITE_E_ACC);
+            ok = mbar_wait_warp(y_ready, sb & 1, abort_flag, kKid, SITE_E_ACC);
             if (!ok) break;
             tc_fence_after();
-            const float *dv = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + 2 * MIN_OP_BYTES) + c0;
+            const float *dv = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + SDS_D) + c0;
             const bool last = sb == nsb - 1;
             float *yrow = p.y + (size_t)(tok_ok ? t : 0) * O + o0 + c0;
             const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {          // 16-column chunks: Y = Y + d*acc + min
-                uint32_t yv[16], mv[16];
-                const uint32_t col = c0 + q * 16;
-                tmem_ld16(tmem_base + lane_off + TM_ACC + kMinSlot * BN + col, mv);
-                if (sb > 0) tmem_ld16(tmem_base + lane_off + TM_Y + col, yv);
-                else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) yv[i] = 0u;
-                }
-                tmem_ld_wait2(mv, yv);
+            for (int q = 0; q < 4; ++q) {          // 16-column chunks: Y = Y + d*acc
+                uint32_t yv[16];
+                const uint32_t ya = tmem_base + lane_off + TM_Y + c0 + q * 16;
+                tmem_ld16(ya, yv);
+                tmem_ld_wait16(yv);
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
                     const float4 d4 = *reinterpret_cast<const float4 *>(dv + q * 16 + i);
                     const float2 y0 = __ffma2_rn(make_float2(acc[q * 16 + i], acc[q * 16 + i + 1]),
                                                  make_float2(d4.x, d4.y),
-                                                 make_float2(__uint_as_float(yv[i]) + __uint_as_float(mv[i]),
-                                                             __uint_as_float(yv[i + 1]) + __uint_as_float(mv[i + 1])));
+                                                 make_float2(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1])));
                     const float2 y1 = __ffma2_rn(make_float2(acc[q * 16 + i + 2], acc[q * 16 + i + 3]),
                                                  make_float2(d4.z, d4.w),
-                                                 make_float2(__uint_as_float(yv[i + 2]) + __uint_as_float(mv[i + 2]),
-                                                             __uint_as_float(yv[i + 3]) + __uint_as_float(mv[i + 3])));
+                                                 make_float2(__uint_as_float(yv[i + 2]), __uint_as_float(yv[i + 3])));
                     yv[i] = __float_as_uint(y0.x);
                     yv[i + 1] = __float_as_uint(y0.y);
                     yv[i + 2] = __float_as_uint(y1.x);
                     yv[i + 3] = __float_as_uint(y1.y);
                 }
                 if (!last) {
-                    tmem_st16(tmem_base + lane_off + TM_Y + col, yv);
+                    tmem_st16(ya, yv);
                 } else if (tok_ok) {
                     if (vec) {
 #pragma unroll
@@ -935,9 +906,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(acc_empty(kMinSlot));
+                mbar_arrive(y_free);
                 mbar_arrive(s_empty(ss));
             }
+        }
+    } else {
+        // ------------------------------------------------------- scale warps --
+        // Per super-block, for weight rows r and r+64 of the tile: d (f32) and
+        // the min-term operand row (-(dmin*m_j) split hi/lo); for tokens r and
+        // r+64: dx_j (f32) and the min-term operand row (dx_j*ssum_j split
+        // hi/lo).  The q8_1 words are fetched a super-block ahead.
+        const int sr = threadIdx.x - SCALE_WARP0 * 32;   // 0..63
+        uint4 dsn[2][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = t0 + sr + 64 * h;
+            dsn[h][0] = dsn[h][1] = make_uint4(0u, 0u, 0u, 0u);
+            if (t < T) {
+                const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32));
+                dsn[h][0] = __ldg(dp);
+                dsn[h][1] = __ldg(dp + 1);
+            }
+        }
+        bool ok = true;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int rs = sb % RSTG, ss = sb % SSTG;
+            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW) &&
+                 mbar_wait(s_empty(ss), ((sb / SSTG) & 1) ^ 1, abort_flag, kKid, SITE_U_SDS);
+            if (!ok) break;
+            uint8_t *slot = smem + oSds + ss * SDS_BYTES;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = sr + 64 * h;
+                const uint4 hd = *reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + r * 144);
+                const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+                const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+                reinterpret_cast<float *>(slot + SDS_D)[r] = d;
+                float bh[8], bl[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    int sc, mm;
+                    q4K_scale_min(hd.y, hd.z, hd.w, j, sc, mm);
+                    const float v = -(dmin * (float)mm);            // exact: 11-bit x 6-bit
+                    bh[j] = to_tf32(v);
+                    bl[j] = to_tf32(v - bh[j]);
+                }
+                put_min_row(slot + MIN_OP_BYTES, r, bh, bl);
+                const uint32_t w[8] = {dsn[h][0].x, dsn[h][0].y, dsn[h][0].z, dsn[h][0].w,
+                                       dsn[h][1].x, dsn[h][1].y, dsn[h][1].z, dsn[h][1].w};
+                float ah[8], al[8];
+                float *dxs = reinterpret_cast<float *>(slot + SDS_DX);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float dx = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
+                    const float v = dx * (float)(int)(int16_t)(w[j] >> 16);   // exact: 11-bit x 12-bit
+                    ah[j] = to_tf32(v);
+                    al[j] = to_tf32(v - ah[j]);
+                    dxs[j * BM + r] = dx;
+                }
+                put_min_row(slot, r, ah, al);
+                const int t = t0 + r;
+                if (t < T && sb + 1 < nsb) {
+                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + (sb + 1) * 8);
+                    dsn[h][0] = __ldg(dp);
+                    dsn[h][1] = __ldg(dp + 1);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(s_full(ss));
+            mbar_arrive(r_empty(rs));
         }
     }
 
@@ -999,7 +1036,8 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
     prm.O = O;
     prm.K = K;
     const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM));
-    kern<<<grid, NUM_THREADS, dyn_smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
+    kern<<<grid, prod_q4K ? q4::NTHREADS : NUM_THREADS, dyn_smem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW,
+                                                                                                    prm);
     return launch_status();
 }
 
