@@ -46,8 +46,13 @@
  *   W: [O][K/256] super-blocks, O*(K/256)*bytes_per_block bytes in total.
  *   q8_1 activations, split-plane form of the pages' 40-byte block:
  *     qs  int8     [T][K]     quantised values, -127..127;
- *     xh  uint16   [T][K]     the same values as IEEE f16 (exact integers);
- *                             this is the form the GEMM reads;
+ *     xh  uint16   [T][K]     the same values as IEEE f16 (exact integers):
+ *                             the operand of the per-sub-block kernels;
+ *     xa  uint16   [2][T][K]  the dequantised value v = f32(d)*q as two f16
+ *                             planes, hi = f16(v) then lo = f16(v - hi); both
+ *                             are exact and hi + lo == v (v is a multiple of
+ *                             2^-24 with at most 18 significant bits): the
+ *                             operand of the production GEMMs;
  *     ds  uint32   [T][K/32]  low 16 bits: f16 d of the 32-block,
  *                             high 16 bits: int16 sum of its 32 values.
  *   Y: f32 [T][O], row-major, overwritten.
@@ -91,31 +96,46 @@ const char *mmq_status_str(int status);
  *   ssum = sum of the 32 q;  stored d = f16(d32), round to nearest even.
  *   An all-zero block stores d = 0, q = 0, ssum = 0.
  * x:   f32, T rows of leading dimension ldx elements (ldx >= K, ldx % 4 == 0).
- * qs:  int8 [T][K] or NULL.   xh: f16 bits [T][K] or NULL (not both NULL).
+ * qs:  int8 [T][K] or NULL.   xh: f16 bits [T][K] or NULL.
+ * xa:  f16 bits [2][T][K] or NULL.   (at least one of qs, xh, xa)
  * ds:  uint32 [T][K/32], required.
  * T >= 0 (T == 0 is a no-op), 32 <= K <= 2^20, K % 32 == 0.
  */
 int mmq_quantize_q8_1(const float *x, int64_t ldx, int T, int K,
-                      int8_t *qs, uint32_t *ds, uint16_t *xh, mmq_stream_t stream);
+                      int8_t *qs, uint32_t *ds, uint16_t *xh, uint16_t *xa, mmq_stream_t stream);
 
 /*
  * q4_K x q8_1 GEMM ("31 . r28", 2.3):  y[t][o] = sum over 32-weight
  * sub-blocks b of  dx_b*(d*sc_b)*C_b + (dx_b*ssum_b)*(-(dmin*m_b)),
  * C_b the exact integer dot of the 32 unsigned quants with the 32 int8
- * activations; accumulation in f32 (rounding order unspecified).
- * w: O*(K/256)*144 bytes.  xh, ds: as written by mmq_quantize_q8_1.
+ * activations, i.e. sum_k dequant(W)[o][k]*dequant(X)[t][k]; accumulation
+ * in f32 (rounding order unspecified).
+ * Production form: the tensor core accumulates each 256-weight super-block
+ * from the exact operands v = f32(d)*q (xa, hi + lo) and sc*q; d and the
+ * dmin*m term are applied per super-block.
+ * w: O*(K/256)*144 bytes.  xa, ds: as written by mmq_quantize_q8_1.
  * y: f32 [T][O], overwritten.
  * T >= 0, O >= 1, 256 <= K <= 2^20, K % 256 == 0.
  */
-int mmq_gemm_q4K(const void *w, const uint16_t *xh, const uint32_t *ds,
+int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *ds,
                  float *y, int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * The same q4_K GEMM in the pages' per-sub-block form: the tensor core forms
+ * every 32-weight sub-block's exact integer dot (times its 6-bit scale) in
+ * its own TMEM accumulator and the f32 fold dx_b*C'_b runs per sub-block
+ * ("31 . r28", 2.3 and 3.2).  xh: the int8 values as f16 (mmq_quantize_q8_1).
+ * Same limits and result (up to f32 summation order) as mmq_gemm_q4K.
+ */
+int mmq_gemm_q4K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds,
+                          float *y, int T, int O, int K, mmq_stream_t stream);
 
 /*
  * q6_K x q8_1 GEMM ("43 . r40", 5: 16-weight sub-blocks, two k16 halves
  * per 32-block):  y[t][o] = sum over 16-weight halves u of
  * dx_(u/2)*(d*sc_u)*C16_u,  C16_u the exact integer dot of (q-32) with the
- * int8 activations.  w: O*(K/256)*210 bytes; other arguments as
- * mmq_gemm_q4K.
+ * int8 activations.  w: O*(K/256)*210 bytes; xh, ds and the other
+ * arguments as for mmq_gemm_q4K_subblock.
  */
 int mmq_gemm_q6K(const void *w, const uint16_t *xh, const uint32_t *ds,
                  float *y, int T, int O, int K, mmq_stream_t stream);
@@ -131,6 +151,16 @@ int mmq_debug_subdots_q4K(const void *w, const uint16_t *xh, int32_t *out,
                           int T, int O, int K, mmq_stream_t stream);
 int mmq_debug_subdots_q6K(const void *w, const uint16_t *xh, int32_t *out,
                           int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * Diagnostic: measured warp-level tensor throughput of the current device,
+ * in TMAC/s (10^12 multiply-accumulates per second), for kind 0 = int8
+ * (mma.sync m16n8k32 s8*s8->s32, the only int8 tensor path on sm_103a) or
+ * kind 1 = f16 (mma.sync m16n8k16, f32 accumulate).  Synchronous: runs a
+ * few hundred microseconds of probe kernels on `stream` and waits for them.
+ * The reported figure is the denominator of "fraction of int8 peak".
+ */
+int mmq_probe_tensor_peak(int kind, double *tmacs, mmq_stream_t stream);
 
 /*
  * Waits for `stream`, then reports and clears the library's device status

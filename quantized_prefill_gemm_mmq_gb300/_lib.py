@@ -22,12 +22,14 @@ _I64 = ctypes.c_int64
 SIGNATURES = {
     "mmq_version": (_I, []),
     "mmq_status_str": (ctypes.c_char_p, [_I]),
-    "mmq_quantize_q8_1": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P]),
+    "mmq_quantize_q8_1": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "mmq_gemm_q4K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_gemm_q4K_subblock": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q4K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q6K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_check_status": (_I, [_P, _P]),
+    "mmq_probe_tensor_peak": (_I, [_I, _P, _P]),
 }
 
 _lib = None

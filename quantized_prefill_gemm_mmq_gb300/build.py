@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmmq.so")
-SOURCES = ["mmq_host.cu", "mmq_quantize.cu", "mmq_gemm.cu"]
+SOURCES = ["mmq_host.cu", "mmq_quantize.cu", "mmq_gemm.cu", "mmq_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

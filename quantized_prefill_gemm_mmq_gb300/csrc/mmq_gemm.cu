@@ -986,6 +986,437 @@ __global__ void __launch_bounds__(q4::NTHREADS, 1)
     }
 }
 
+// =========================================================================
+// q4_K GEMM with super-block accumulation (production).
+//
+// The sum over a super-block's 8 sub-blocks of dx_b*sc_b*C_b is computed by
+// the tensor core itself: the activation operand is the dequantised q8_1
+// value v = f32(d16)*q split into two exact f16 planes (v = hi + lo, see the
+// quantiser), the weight operand is sc*q (exact), so each product is exact in
+// f32 and one TMEM accumulator per super-block receives
+//     D_sb[t][o] = sum_{k in sb} v[t][k] * sc_b(o)*q[o][k]
+// through two MMAs per 16-k step (hi plane, lo plane).  The epilogue then
+// needs one packed FMA per output per super-block, Y += d*D_sb (Y held in
+// registers), and the min term (split-tf32 tensor-core GEMM over the
+// sub-block index, as in the kernel above) accumulates in its own TMEM
+// columns across K and is added at the end.  The per-sub-block integer dots
+// are not formed here (see mmq_q4K_kernel / the sub-block diagnostics for
+// those); the result differs from them only in f32 summation order.
+// TMEM: [0,384) three rotating super-block accumulators, [384,512) min term.
+// Warps: 0 TMA producer, 1 MMA issuer, 2-5 unpack, 6-13 epilogue, 14-15 scale.
+// =========================================================================
+namespace q4s {
+
+constexpr int NWARPS = 16;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int SCALE_WARP0 = 14;
+constexpr int STG = 3;                            // operand ring (A hi, A lo, B tiles)
+constexpr int RSTG = 2;                           // raw super-block ring
+constexpr int SSTG = 2;                           // scale / min-operand ring
+constexpr int NACC = 3;                           // rotating super-block accumulators
+constexpr uint32_t TM_ACC = 0, TM_MIN = NACC * BN;
+static_assert(TM_MIN + BN <= 512, "TMEM budget");
+constexpr uint32_t A_STAGE = 2 * A_BYTES;         // hi and lo planes
+constexpr uint32_t RAW_BYTES = BN * 144;
+constexpr uint32_t MIN_OP_BYTES = 128 * 64;
+constexpr uint32_t SDS_D = 2 * MIN_OP_BYTES;
+constexpr uint32_t SDS_BYTES = SDS_D + BN * 4;
+constexpr uint32_t oA = 0;
+constexpr uint32_t oB = oA + STG * A_STAGE;
+constexpr uint32_t oRaw = oB + STG * B_BYTES;
+constexpr uint32_t oSds = oRaw + RSTG * RAW_BYTES;
+constexpr uint32_t oBar = oSds + SSTG * SDS_BYTES;
+// a_full, b_full, st_empty [STG]; r_full, r_empty [RSTG]; s_full, s_empty
+// [SSTG]; acc_full, acc_empty [NACC]; mma_done
+constexpr int kNumBars = 3 * STG + 2 * RSTG + 2 * SSTG + 2 * NACC + 1;
+constexpr uint32_t oMisc = oBar + kNumBars * 8;
+constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
+static_assert(kDynSmem <= 232448, "shared memory budget");
+static_assert(oB % 1024 == 0 && oRaw % 1024 == 0 && RAW_BYTES % 1024 == 0, "ring alignment");
+static_assert(oSds % 16 == 0 && SDS_BYTES % 16 == 0, "min operands must be 16-byte aligned");
+
+}  // namespace q4s
+
+__global__ void __launch_bounds__(q4s::NTHREADS, 1)
+    mmq_q4K_sb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                      const Params p)
+{
+    using namespace q4s;
+    constexpr int kKid = 9;
+    constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
+    constexpr uint32_t kIdescTf32 = idesc_tf32_f32(BM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o0 = blockIdx.x * BN, t0 = blockIdx.y * BM;
+    const int T = p.T, K = p.K, O = p.O;
+    const int nks = K / BK, nsb = K / 256;
+
+    const uint32_t bar0 = sbase + oBar;
+    auto a_full = [&](int s) { return bar0 + 8u * s; };
+    auto b_full = [&](int s) { return bar0 + 8u * (STG + s); };
+    auto st_empty = [&](int s) { return bar0 + 8u * (2 * STG + s); };
+    auto r_full = [&](int s) { return bar0 + 8u * (3 * STG + s); };
+    auto r_empty = [&](int s) { return bar0 + 8u * (3 * STG + RSTG + s); };
+    auto s_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + s); };
+    auto s_empty = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + SSTG + s); };
+    auto acc_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + s); };
+    auto acc_empty = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + NACC + s); };
+    const uint32_t mma_done = bar0 + 8u * (kNumBars - 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + oMisc);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + oMisc + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STG; ++s) {
+            mbar_init(a_full(s), 1);
+            mbar_init(b_full(s), 128);
+            mbar_init(st_empty(s), 1);
+        }
+        for (int s = 0; s < RSTG; ++s) {
+            mbar_init(r_full(s), 1);
+            mbar_init(r_empty(s), 128 + 64);                // unpack and scale threads
+        }
+        for (int s = 0; s < SSTG; ++s) {
+            mbar_init(s_full(s), 64);                       // scale threads
+            mbar_init(s_empty(s), NUM_EPI_WARPS + 1);       // epilogue warps (d) + the MMA's commit
+        }
+        for (int s = 0; s < NACC; ++s) {
+            mbar_init(acc_full(s), 1);
+            mbar_init(acc_empty(s), NUM_EPI_WARPS);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            tma_prefetch(&tmA);
+            tma_prefetch(&tmW);
+        }
+        int n_a = 0, n_r = 0;
+        bool ok = true;
+        auto issue_raw = [&](int sb) -> bool {
+            const int rs = sb % RSTG;
+            if (!mbar_wait_warp(r_empty(rs), ((sb / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW)) return false;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(r_full(rs), RAW_BYTES);
+                tma_load_2d(sbase + oRaw + rs * RAW_BYTES, &tmW, r_full(rs), sb * 144, o0);
+            }
+            ++n_r;
+            return true;
+        };
+        ok = issue_raw(0);
+        for (int ks = 0; ks < nks && ok; ++ks) {
+            if ((ks & 3) == 0 && (ks >> 2) + 1 < nsb) {
+                ok = issue_raw((ks >> 2) + 1);
+                if (!ok) break;
+            }
+            const int s = ks % STG;
+            ok = mbar_wait_warp(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
+            if (!ok) break;
+            if (lane == 0) {
+                // the activation tensor is [2T][K]: hi plane rows 0..T-1, lo plane rows T..2T-1
+                mbar_arrive_expect_tx(a_full(s), A_STAGE);
+                tma_load_2d(sbase + oA + s * A_STAGE, &tmA, a_full(s), ks * BK, t0);
+                tma_load_2d(sbase + oA + s * A_STAGE + A_BYTES, &tmA, a_full(s), ks * BK, T + t0);
+            }
+            ++n_a;
+            __syncwarp();
+        }
+        if (!ok) {
+            for (int i = max(0, n_a - STG); i < n_a; ++i) wait_drain(a_full(i % STG), (i / STG) & 1);
+            for (int i = max(0, n_r - RSTG); i < n_r; ++i) wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            bool ok = true;
+            for (int ks = 0; ks < nks && ok; ++ks) {
+                const int s = ks % STG;
+                const uint32_t par = (ks / STG) & 1;
+                const int sb = ks >> 2, p4 = ks & 3, slot = sb % NACC;
+                ok = mbar_wait(a_full(s), par, abort_flag, kKid, SITE_M_A) &&
+                     mbar_wait(b_full(s), par, abort_flag, kKid, SITE_M_B) &&
+                     (p4 != 0 || mbar_wait(acc_empty(slot), ((sb / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a_hi = sbase + oA + s * A_STAGE, a_lo = a_hi + A_BYTES;
+                const uint32_t b_base = sbase + oB + s * B_BYTES;
+                const uint32_t d_acc = tmem_base + TM_ACC + slot * BN;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t koff = (uint32_t)kk * 32u;
+                    const uint64_t bd = sdesc_k_sw128(b_base + koff);
+                    umma_f16(d_acc, sdesc_k_sw128(a_hi + koff), bd, kIdesc, (p4 == 0 && kk == 0) ? 0u : 1u);
+                    umma_f16(d_acc, sdesc_k_sw128(a_lo + koff), bd, kIdesc, 1u);
+                }
+                umma_commit(st_empty(s));
+                if (p4 == 3) {
+                    // min term of this super-block, accumulated across K
+                    const int ss = sb % SSTG;
+                    ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
+                    const uint32_t dmn = tmem_base + TM_MIN;
+                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32,
+                              sb > 0 ? 1u : 0u);
+                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(dmn, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
+                    umma_commit(acc_full(slot));
+                    umma_commit(s_empty(ss));
+                }
+            }
+            umma_commit(mma_done);
+            if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp < EPI_WARP0) {
+        // ------------------------------------------------------ unpack warps --
+        const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row of the B tile
+        bool ok = true;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int rs = sb % RSTG;
+            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW);
+            if (!ok) break;
+            const uint8_t *raw = smem + oRaw + rs * RAW_BYTES + r * 144;
+            const uint4 hd = *reinterpret_cast<const uint4 *>(raw);
+#pragma unroll
+            for (int p4 = 0; p4 < 4; ++p4) {
+                const int ks = sb * 4 + p4, s = ks % STG;
+                int sc_lo, sc_hi, unused;
+                q4::q4K_scale_min(hd.y, hd.z, hd.w, 2 * p4, sc_lo, unused);
+                q4::q4K_scale_min(hd.y, hd.z, hd.w, 2 * p4 + 1, sc_hi, unused);
+                const float slo = (float)sc_lo, shi = (float)sc_hi;
+                const __half2 mlo = __float2half2_rn(slo), alo = __float2half2_rn(-1024.0f * slo);
+                const __half2 mhi = __float2half2_rn(shi * 0.0625f), ahi = __float2half2_rn(-64.0f * shi);
+                const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4);
+                const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4 + 16);
+                ok = mbar_wait(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
+                if (!ok) break;
+                const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint8_t *brow = smem + oB + s * B_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t wa = wv[2 * (c & 3)], wb = wv[2 * (c & 3) + 1];
+                    const uint32_t mask = c < 4 ? 0x000F000Fu : 0x00F000F0u;
+                    const __half2 m2 = c < 4 ? mlo : mhi, a2 = c < 4 ? alo : ahi;
+                    uint4 v;
+                    v.x = q4::nib2(wa, 0x4140u, mask, m2, a2);
+                    v.y = q4::nib2(wa, 0x4342u, mask, m2, a2);
+                    v.z = q4::nib2(wb, 0x4140u, mask, m2, a2);
+                    v.w = q4::nib2(wb, 0x4342u, mask, m2, a2);
+                    *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = v;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(b_full(s));
+            }
+            if (ok) mbar_arrive(r_empty(rs));
+        }
+    } else if (warp < SCALE_WARP0) {
+        // --------------------------------------------------------- epilogue --
+        // Thread = one token (TMEM lane) x 64 weight rows; Y += d*D_sb per
+        // super-block in registers, plus the min term at the end.
+        const int ew = warp - EPI_WARP0;
+        const int quarter = warp & 3;
+        const int c0 = (ew >> 2) * 64;
+        const int tl = quarter * 32 + lane;
+        const int t = t0 + tl;
+        const bool tok_ok = t < T;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        float yv[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) yv[i] = 0.0f;
+        bool ok = true;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int slot = sb % NACC, ss = sb % SSTG;
+            ok = mbar_wait_warp(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS) &&
+                 mbar_wait_warp(acc_full(slot), (sb / NACC) & 1, abort_flag, kKid, SITE_E_ACC);
+            if (!ok) break;
+            tc_fence_after();
+            const float *dv = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + SDS_D) + c0;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t rv[32];
+                tmem_ld32(tmem_base + lane_off + TM_ACC + (uint32_t)(slot * BN + c0 + hh * 32), rv);
+                tmem_ld_wait(rv);
+                if (hh == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty(slot));
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dv + hh * 32 + i);
+                    const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(rv[i]), __uint_as_float(rv[i + 1])),
+                                                 make_float2(d4.x, d4.y),
+                                                 make_float2(yv[hh * 32 + i], yv[hh * 32 + i + 1]));
+                    const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3])),
+                                                 make_float2(d4.z, d4.w),
+                                                 make_float2(yv[hh * 32 + i + 2], yv[hh * 32 + i + 3]));
+                    yv[hh * 32 + i] = y0.x;
+                    yv[hh * 32 + i + 1] = y0.y;
+                    yv[hh * 32 + i + 2] = y1.x;
+                    yv[hh * 32 + i + 3] = y1.y;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty(ss));
+        }
+        if (ok) {
+            // every min-term MMA was issued before the last accumulator's commit
+            float *yrow = p.y + (size_t)(tok_ok ? t : 0) * O + o0 + c0;
+            const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t mv[32];
+                tmem_ld32(tmem_base + lane_off + TM_MIN + c0 + hh * 32, mv);
+                tmem_ld_wait(mv);
+                if (tok_ok) {
+                    if (vec) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(yrow + hh * 32 + i) =
+                                make_float4(yv[hh * 32 + i] + __uint_as_float(mv[i]),
+                                            yv[hh * 32 + i + 1] + __uint_as_float(mv[i + 1]),
+                                            yv[hh * 32 + i + 2] + __uint_as_float(mv[i + 2]),
+                                            yv[hh * 32 + i + 3] + __uint_as_float(mv[i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (o0 + c0 + hh * 32 + i < O) yrow[hh * 32 + i] = yv[hh * 32 + i] + __uint_as_float(mv[i]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------- scale warps --
+        // Per super-block, for weight rows r and r+64: d and the min-term
+        // operand row (-(dmin*m_j) split hi/lo); for tokens r and r+64: the
+        // min-term operand row (dx_j*ssum_j split hi/lo).  The q8_1 scale words
+        // are fetched one super-block ahead.
+        const int sr = threadIdx.x - SCALE_WARP0 * 32;   // 0..63
+        uint4 dsn[2][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = t0 + sr + 64 * h;
+            dsn[h][0] = dsn[h][1] = make_uint4(0u, 0u, 0u, 0u);
+            if (t < T) {
+                const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32));
+                dsn[h][0] = __ldg(dp);
+                dsn[h][1] = __ldg(dp + 1);
+            }
+        }
+        bool ok = true;
+        for (int sb = 0; sb < nsb && ok; ++sb) {
+            const int rs = sb % RSTG, ss = sb % SSTG;
+            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW) &&
+                 mbar_wait(s_empty(ss), ((sb / SSTG) & 1) ^ 1, abort_flag, kKid, SITE_U_SDS);
+            if (!ok) break;
+            uint8_t *slot = smem + oSds + ss * SDS_BYTES;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = sr + 64 * h;
+                const uint4 hd = *reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + r * 144);
+                const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
+                const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
+                reinterpret_cast<float *>(slot + SDS_D)[r] = d;
+                float bh[8], bl[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    int sc, mm;
+                    q4::q4K_scale_min(hd.y, hd.z, hd.w, j, sc, mm);
+                    const float v = -(dmin * (float)mm);
+                    bh[j] = to_tf32(v);
+                    bl[j] = to_tf32(v - bh[j]);
+                }
+                q4::put_min_row(slot + MIN_OP_BYTES, r, bh, bl);
+                const uint32_t w[8] = {dsn[h][0].x, dsn[h][0].y, dsn[h][0].z, dsn[h][0].w,
+                                       dsn[h][1].x, dsn[h][1].y, dsn[h][1].z, dsn[h][1].w};
+                float ah[8], al[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float dx = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
+                    const float v = dx * (float)(int)(int16_t)(w[j] >> 16);
+                    ah[j] = to_tf32(v);
+                    al[j] = to_tf32(v - ah[j]);
+                }
+                q4::put_min_row(slot, r, ah, al);
+                const int t = t0 + r;
+                if (t < T && sb + 1 < nsb) {
+                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + (sb + 1) * 8);
+                    dsn[h][0] = __ldg(dp);
+                    dsn[h][1] = __ldg(dp + 1);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(s_full(ss));
+            mbar_arrive(r_empty(rs));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// Production q4_K launch: activations as the [2T][K] f16 hi/lo planes.
+int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K,
+                  mmq_stream_t stream)
+{
+    if (T < 0 || O < 1 || K < 256 || K > (1 << 20) || (K & 255)) return MMQ_ERR_SHAPE;
+    if (T == 0) return MMQ_OK;
+    if (!w || !xa || !ds || !y) return MMQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(xa) || !aligned16(ds) || !aligned16(y)) return MMQ_ERR_ALIGN;
+    int rc = check_arch();
+    if (rc != MMQ_OK) return rc;
+    const long long nsb = K / 256;
+    CUtensorMap tmA, tmW;
+    rc = make_tmap_2d(&tmA, xa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, 2ull * (uint64_t)T, (uint64_t)K * 2, BK,
+                      BM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != MMQ_OK) return rc;
+    rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)(nsb * 144), (uint64_t)O, (uint64_t)(nsb * 144),
+                      144, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != MMQ_OK) return rc;
+    static bool attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(mmq_q4K_sb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q4s::kDynSmem) !=
+            cudaSuccess)
+            return launch_status();
+        attr_done[dev] = true;
+    }
+    Params prm;
+    prm.w = static_cast<const uint8_t *>(w);
+    prm.ds = ds;
+    prm.y = y;
+    prm.sub = nullptr;
+    prm.T = T;
+    prm.O = O;
+    prm.K = K;
+    const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM));
+    mmq_q4K_sb_kernel<<<grid, q4s::NTHREADS, q4s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
+    return launch_status();
+}
+
 template <int FMT, int MODE>
 int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int32_t *sub, int T, int O, int K,
            mmq_stream_t stream)
@@ -1044,8 +1475,14 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
 }  // namespace
 }  // namespace mmq
 
-extern "C" int mmq_gemm_q4K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O, int K,
+extern "C" int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K,
                             mmq_stream_t stream)
+{
+    return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, stream);
+}
+
+extern "C" int mmq_gemm_q4K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O,
+                                     int K, mmq_stream_t stream)
 {
     return mmq::launch<mmq::kQ4K, mmq::kFold>(w, xh, ds, y, nullptr, T, O, K, stream);
 }

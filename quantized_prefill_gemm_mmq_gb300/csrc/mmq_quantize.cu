@@ -8,6 +8,12 @@
 // Both divisions are IEEE round-to-nearest (__fdiv_rn) so the result does
 // not depend on fast-math flags.
 //
+// Optional outputs: qs (int8 values), xh (the same values as f16, the integer
+// operand form) and xa (the dequantised activation f32(d16)*q as an exact
+// pair of f16 planes hi + lo: every such value is a multiple of 2^-24 with at
+// most 18 significant bits, so hi = f16(v) and lo = f16(v - hi) are both
+// exact and hi + lo == v).
+//
 // Layout: eight threads own one 32-block, four consecutive floats each
 // (one 16-byte load).  The block's amax and ssum are reduced across the
 // eight lanes with shuffles.  The kernel is a grid-stride loop over all
@@ -24,7 +30,7 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
     const float *__restrict__ x, int64_t ldx, int T, int K, int8_t *__restrict__ qs,
-    uint32_t *__restrict__ ds, uint16_t *__restrict__ xh)
+    uint32_t *__restrict__ ds, uint16_t *__restrict__ xh, uint16_t *__restrict__ xa)
 {
     const int nb = K >> 5;                                   // 32-blocks per token
     const int64_t nblocks = (int64_t)T * nb;
@@ -76,10 +82,27 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
             hv.y = *reinterpret_cast<const uint32_t *>(&h23);
             *reinterpret_cast<uint2 *>(xh + e) = hv;
         }
-        if (sub == 0) {
-            const uint16_t dh = __half_as_ushort(__float2half_rn(d32));
-            ds[blk] = (uint32_t)dh | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
+        const __half dh = __float2half_rn(d32);
+        if (xa) {
+            const float df = __half2float(dh);
+            const int qv[4] = {q0, q1, q2, q3};
+            uint16_t hi[4], lo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float v = df * (float)qv[i];              // exact in f32
+                const __half h = __float2half_rn(v);
+                hi[i] = __half_as_ushort(h);
+                lo[i] = __half_as_ushort(__float2half_rn(v - __half2float(h)));   // exact
+            }
+            uint2 hv, lv;
+            hv.x = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
+            hv.y = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
+            lv.x = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
+            lv.y = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
+            *reinterpret_cast<uint2 *>(xa + e) = hv;
+            *reinterpret_cast<uint2 *>(xa + (int64_t)T * K + e) = lv;
         }
+        if (sub == 0) ds[blk] = (uint32_t)__half_as_ushort(dh) | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
     }
 }
 
@@ -87,13 +110,14 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
 }  // namespace mmq
 
 extern "C" int mmq_quantize_q8_1(const float *x, int64_t ldx, int T, int K, int8_t *qs, uint32_t *ds,
-                                 uint16_t *xh, mmq_stream_t stream)
+                                 uint16_t *xh, uint16_t *xa, mmq_stream_t stream)
 {
     using namespace mmq;
     if (T < 0 || K < 32 || K > (1 << 20) || (K & 31) || ldx < K) return MMQ_ERR_SHAPE;
     if (T == 0) return MMQ_OK;
-    if (!x || !ds || (!qs && !xh)) return MMQ_ERR_NULL;
-    if (!aligned16(x) || (ldx & 3) || !aligned16(ds) || (qs && !aligned16(qs)) || (xh && !aligned16(xh)))
+    if (!x || !ds || (!qs && !xh && !xa)) return MMQ_ERR_NULL;
+    if (!aligned16(x) || (ldx & 3) || !aligned16(ds) || (qs && !aligned16(qs)) || (xh && !aligned16(xh)) ||
+        (xa && !aligned16(xa)))
         return MMQ_ERR_ALIGN;
     const int a = check_arch();
     if (a != MMQ_OK) return a;
@@ -105,6 +129,6 @@ extern "C" int mmq_quantize_q8_1(const float *x, int64_t ldx, int T, int K, int8
     const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 8;   // 8 resident blocks per SM
     if (grid > cap) grid = cap;
     quantize_q8_1_kernel<<<(unsigned)grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        x, ldx, T, K, qs, ds, xh);
+        x, ldx, T, K, qs, ds, xh, xa);
     return launch_status();
 }

@@ -34,13 +34,16 @@ def _need_cuda(*ts):
             raise ValueError("libmmq ops need CUDA tensors")
 
 
-def quantize_q8_1(x: torch.Tensor, want_qs: bool = True, want_xh: bool = True, out=None):
+def quantize_q8_1(x: torch.Tensor, want_qs: bool = True, want_xh: bool = True, want_xa: bool = True, out=None):
     """q8_1-quantise activations x [T][K] f32 (row stride may exceed K).
 
-    Returns (qs, ds, xh): qs int8 [T][K] or None; ds int32 [T][K/32] holding
-    the library's uint32 words (f16 d | int16 block sum); xh float16 [T][K]
-    holding the same integer values as qs, or None.  `out` may supply the
-    three buffers (any of qs / xh may be None).
+    Returns (qs, ds, xh, xa):
+      qs  int8 [T][K] values, or None;
+      ds  int32 [T][K/32] holding the uint32 words (f16 d | int16 block sum);
+      xh  float16 [T][K], the same integer values as f16 (per-sub-block operand), or None;
+      xa  float16 [2][T][K], the dequantised values f32(d)*q as exact hi + lo planes
+          (production operand), or None.
+    `out` may supply the four buffers (any of qs / xh / xa may be None).
     """
     _need_cuda(x)
     if x.dtype != torch.float32 or x.dim() != 2 or x.stride(1) != 1:
@@ -48,8 +51,9 @@ def quantize_q8_1(x: torch.Tensor, want_qs: bool = True, want_xh: bool = True, o
     T, K = x.shape
     dev = x.device
     if out is not None:
-        qs, ds, xh = out
-        for t, dt, shape in ((qs, torch.int8, (T, K)), (ds, torch.int32, (T, K // 32)), (xh, torch.float16, (T, K))):
+        qs, ds, xh, xa = out
+        for t, dt, shape in ((qs, torch.int8, (T, K)), (ds, torch.int32, (T, K // 32)),
+                             (xh, torch.float16, (T, K)), (xa, torch.float16, (2, T, K))):
             if t is not None and (t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous()):
                 raise ValueError("bad output buffer")
         if ds is None:
@@ -57,56 +61,78 @@ def quantize_q8_1(x: torch.Tensor, want_qs: bool = True, want_xh: bool = True, o
     else:
         qs = torch.empty((T, K), dtype=torch.int8, device=dev) if want_qs else None
         xh = torch.empty((T, K), dtype=torch.float16, device=dev) if want_xh else None
+        xa = torch.empty((2, T, K), dtype=torch.float16, device=dev) if want_xa else None
         ds = torch.empty((T, K // 32), dtype=torch.int32, device=dev)
-    _need_cuda(qs, ds, xh)
+    _need_cuda(qs, ds, xh, xa)
     with torch.cuda.device(dev):
-        st = load().mmq_quantize_q8_1(_ptr(x), x.stride(0), T, K, _ptr(qs), _ptr(ds), _ptr(xh), _stream(dev))
+        st = load().mmq_quantize_q8_1(_ptr(x), x.stride(0), T, K, _ptr(qs), _ptr(ds), _ptr(xh), _ptr(xa),
+                                      _stream(dev))
     _check("mmq_quantize_q8_1", st)
-    return qs, ds, xh
+    return qs, ds, xh, xa
 
 
-def _check_gemm_args(fmt: str, w: torch.Tensor, xh: torch.Tensor, O: int):
-    _need_cuda(w, xh)
+def _check_gemm_args(fmt: str, w: torch.Tensor, xv: torch.Tensor, O: int, planes: int):
+    _need_cuda(w, xv)
     if fmt not in BLOCK_BYTES:
         raise ValueError(f"unknown format {fmt!r}")
-    if xh.dtype != torch.float16 or xh.dim() != 2 or not xh.is_contiguous():
-        raise ValueError("xh must be a contiguous [T][K] float16 tensor (q8_1 values)")
-    T, K = xh.shape
+    if xv.dtype != torch.float16 or xv.dim() != (2 if planes == 1 else 3) or not xv.is_contiguous() or \
+            (planes == 2 and xv.shape[0] != 2):
+        raise ValueError("activation operand must be contiguous float16 [T][K] (xh) or [2][T][K] (xa)")
+    T, K = xv.shape[-2:]
     if w.dtype != torch.uint8 or not w.is_contiguous() or w.numel() != O * (K // 256) * BLOCK_BYTES[fmt]:
         raise ValueError("w must be contiguous uint8 holding O*(K/256) super-blocks")
-    if w.device != xh.device:
-        raise ValueError("w and xh must be on the same device")
+    if w.device != xv.device:
+        raise ValueError("w and the activations must be on the same device")
     return T, K
 
 
-def gemm(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
-         out: torch.Tensor | None = None) -> torch.Tensor:
-    """Y [T][O] f32 = q8_1(X) . W^T with W in `fmt` ("q4_K" or "q6_K")."""
-    T, K = _check_gemm_args(fmt, w, xh, O)
-    if ds.dtype != torch.int32 or tuple(ds.shape) != (T, K // 32) or not ds.is_contiguous():
-        raise ValueError("ds must be contiguous int32 [T][K/32]")
+def _out(out, T, O, dev):
     if out is None:
-        out = torch.empty((T, O), dtype=torch.float32, device=xh.device)
-    elif out.dtype != torch.float32 or tuple(out.shape) != (T, O) or not out.is_contiguous():
+        return torch.empty((T, O), dtype=torch.float32, device=dev)
+    if out.dtype != torch.float32 or tuple(out.shape) != (T, O) or not out.is_contiguous():
         raise ValueError("out must be contiguous float32 [T][O]")
-    fn = load().mmq_gemm_q4K if fmt == "q4_K" else load().mmq_gemm_q6K
-    with torch.cuda.device(xh.device):
-        st = fn(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
-    _check(f"mmq_gemm_{fmt.replace('_', '')}", st)
     return out
 
 
-def gemm_q4K(w, xh, ds, O, out=None):
-    return gemm("q4_K", w, xh, ds, O, out)
+def _check_ds(ds, T, K):
+    if ds.dtype != torch.int32 or tuple(ds.shape) != (T, K // 32) or not ds.is_contiguous():
+        raise ValueError("ds must be contiguous int32 [T][K/32]")
 
 
-def gemm_q6K(w, xh, ds, O, out=None):
-    return gemm("q6_K", w, xh, ds, O, out)
+def gemm(fmt: str, w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int,
+         out: torch.Tensor | None = None) -> torch.Tensor:
+    """Production GEMM: Y [T][O] f32 from W (`fmt`) and the xa/ds activation planes.
+
+    q6_K is served by its per-sub-block kernel, which reads the integer plane;
+    pass that as `xh=` through gemm_subblock, or call mmq_forward.
+    """
+    if fmt == "q6_K":
+        raise ValueError("q6_K takes the integer operand: use gemm_subblock('q6_K', w, xh, ds, O)")
+    T, K = _check_gemm_args(fmt, w, xa, O, planes=2)
+    _check_ds(ds, T, K)
+    out = _out(out, T, O, xa.device)
+    with torch.cuda.device(xa.device):
+        st = load().mmq_gemm_q4K(_ptr(w), _ptr(xa), _ptr(ds), _ptr(out), T, O, K, _stream(xa.device))
+    _check("mmq_gemm_q4K", st)
+    return out
+
+
+def gemm_subblock(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    """Per-sub-block GEMM (exact integer sub-block dots + f32 fold) from the xh/ds planes."""
+    T, K = _check_gemm_args(fmt, w, xh, O, planes=1)
+    _check_ds(ds, T, K)
+    out = _out(out, T, O, xh.device)
+    fn = load().mmq_gemm_q4K_subblock if fmt == "q4_K" else load().mmq_gemm_q6K
+    with torch.cuda.device(xh.device):
+        st = fn(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
+    _check(f"gemm_subblock({fmt})", st)
+    return out
 
 
 def debug_subdots(fmt: str, w: torch.Tensor, xh: torch.Tensor, O: int) -> torch.Tensor:
     """Per-sub-block integer dots: int32 [T][O][K/32] (q4_K) or [T][O][K/16] (q6_K)."""
-    T, K = _check_gemm_args(fmt, w, xh, O)
+    T, K = _check_gemm_args(fmt, w, xh, O, planes=1)
     nsub = K // 32 if fmt == "q4_K" else K // 16
     out = torch.empty((T, O, nsub), dtype=torch.int32, device=xh.device)
     fn = load().mmq_debug_subdots_q4K if fmt == "q4_K" else load().mmq_debug_subdots_q6K
@@ -126,7 +152,20 @@ def check_status(device: torch.device | None = None):
         raise MMQError(f"kernel (id {detail[1]}, site {detail[2]}, block {detail[3]})", st)
 
 
+def tensor_peak_tmacs(kind: str = "int8", device: torch.device | None = None) -> float:
+    """Measured warp-level tensor throughput (TMAC/s) of the device: 'int8' or 'f16'."""
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    v = ctypes.c_double(0.0)
+    with torch.cuda.device(dev):
+        st = load().mmq_probe_tensor_peak(0 if kind == "int8" else 1, ctypes.byref(v), _stream(dev))
+    _check("mmq_probe_tensor_peak", st)
+    return v.value
+
+
 def mmq_forward(fmt: str, w: torch.Tensor, x: torch.Tensor, O: int) -> torch.Tensor:
     """Quantise x [T][K] to q8_1 and run the GEMM: the whole hot path."""
-    _, ds, xh = quantize_q8_1(x, want_qs=False, want_xh=True)
-    return gemm(fmt, w, xh, ds, O)
+    if fmt == "q4_K":
+        _, ds, _, xa = quantize_q8_1(x, want_qs=False, want_xh=False, want_xa=True)
+        return gemm(fmt, w, xa, ds, O)
+    _, ds, xh, _ = quantize_q8_1(x, want_qs=False, want_xh=True, want_xa=False)
+    return gemm_subblock(fmt, w, xh, ds, O)

@@ -16,7 +16,7 @@ needs_lib = pytest.mark.skipif(not HAVE_LIB, reason="libmmq.so not built (run __
 
 def test_header_declares_the_boundary():
     names = _lib.header_functions()
-    for required in ("mmq_quantize_q8_1", "mmq_gemm_q4K", "mmq_gemm_q6K", "mmq_check_status",
+    for required in ("mmq_quantize_q8_1", "mmq_gemm_q4K", "mmq_gemm_q4K_subblock", "mmq_gemm_q6K", "mmq_check_status",
                      "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
@@ -34,7 +34,7 @@ def test_library_exports_every_header_symbol():
 @needs_lib
 def test_library_loads_and_reports():
     lib = _lib.load()
-    assert lib.mmq_version() == 1
+    assert lib.mmq_version() == 2
     assert lib.mmq_status_str(0) == b"ok"
     for code in range(-8, 0):
         assert lib.mmq_status_str(code) not in (b"", b"unknown status")
@@ -49,19 +49,19 @@ def test_argument_errors_without_gpu():
     odd = ctypes.c_void_p(base + 4)
     null = ctypes.c_void_p(0)
     # shapes
-    assert lib.mmq_quantize_q8_1(p, 64, 1, 48, p, p, p, null) == -1           # K % 32
-    assert lib.mmq_quantize_q8_1(p, 16, 1, 32, p, p, p, null) == -1           # ldx < K
+    assert lib.mmq_quantize_q8_1(p, 64, 1, 48, p, p, p, p, null) == -1           # K % 32
+    assert lib.mmq_quantize_q8_1(p, 16, 1, 32, p, p, p, p, null) == -1           # ldx < K
     assert lib.mmq_gemm_q4K(p, p, p, p, 1, 1, 300, null) == -1               # K % 256
     assert lib.mmq_gemm_q6K(p, p, p, p, 1, 0, 256, null) == -1               # O < 1
     assert lib.mmq_gemm_q4K(p, p, p, p, -1, 1, 256, null) == -1              # T < 0
     # T == 0 is a no-op
     assert lib.mmq_gemm_q4K(p, p, p, p, 0, 1, 256, null) == 0
-    assert lib.mmq_quantize_q8_1(p, 32, 0, 32, p, p, p, null) == 0
+    assert lib.mmq_quantize_q8_1(p, 32, 0, 32, p, p, p, p, null) == 0
     # nulls and alignment
     assert lib.mmq_gemm_q4K(null, p, p, p, 1, 1, 256, null) == -6
-    assert lib.mmq_quantize_q8_1(p, 32, 1, 32, null, p, null, null) == -6   # neither qs nor xh
+    assert lib.mmq_quantize_q8_1(p, 32, 1, 32, null, p, null, null, null) == -6   # no value plane
     assert lib.mmq_gemm_q4K(odd, p, p, p, 1, 1, 256, null) == -2
-    assert lib.mmq_quantize_q8_1(p, 34, 1, 32, p, p, p, null) == -2          # ldx * 4 not 16-aligned
+    assert lib.mmq_quantize_q8_1(p, 34, 1, 32, p, p, p, p, null) == -2          # ldx * 4 not 16-aligned
 
 
 @needs_lib
@@ -72,5 +72,6 @@ def test_valid_call_without_gpu_fails_loudly():
     lib = _lib.load()
     buf = ctypes.create_string_buffer(1 << 16)
     p = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
-    assert lib.mmq_quantize_q8_1(p, 32, 1, 32, p, p, p, ctypes.c_void_p(0)) == -3   # no sm_103 device
+    assert lib.mmq_quantize_q8_1(p, 32, 1, 32, p, p, p, p, ctypes.c_void_p(0)) == -3   # no sm_103 device
     assert lib.mmq_gemm_q4K(p, p, p, p, 1, 1, 256, ctypes.c_void_p(0)) == -3
+    assert lib.mmq_gemm_q4K_subblock(p, p, p, p, 1, 1, 256, ctypes.c_void_p(0)) == -3

@@ -34,8 +34,8 @@ def _dev(a):
 
 
 def _gpu_quant(ops, x):
-    qs, ds, xh = ops.quantize_q8_1(_dev(x))
-    return qs, ds, xh
+    qs, ds, xh, xa = ops.quantize_q8_1(_dev(x))
+    return qs, ds, xh, xa
 
 
 def _to_np_ds(ds):
@@ -54,11 +54,14 @@ def _rel_err(y, ref):
 def test_quantize_bit_exact(ops, orc, T, K, seed, outl):
     x = synth.make_x(T, K, seed, outl)
     qs_r, ds_r = orc.quantize_q8_1(x)
-    qs, ds, xh = _gpu_quant(ops, x)
+    qs, ds, xh, xa = _gpu_quant(ops, x)
     ops.check_status()
     assert np.array_equal(qs.cpu().numpy(), qs_r)
     assert np.array_equal(_to_np_ds(ds), ds_r)
     assert np.array_equal(xh.cpu().numpy().astype(np.float32), qs_r.astype(np.float32))
+    # xa: hi + lo reproduces the dequantised value f32(d16)*q exactly
+    xa_np = xa.cpu().numpy().astype(np.float64)
+    assert np.array_equal(xa_np[0] + xa_np[1], orc.dequant_q8_1(qs_r, ds_r))
 
 
 def test_quantize_special_blocks(ops, orc):
@@ -69,15 +72,17 @@ def test_quantize_special_blocks(ops, orc):
     x[2, 64] = -1e-30
     x[3, :] = np.linspace(-1000, 1000, 128, dtype=np.float32)
     qs_r, ds_r = orc.quantize_q8_1(x)
-    qs, ds, xh = _gpu_quant(ops, x)
+    qs, ds, xh, xa = _gpu_quant(ops, x)
     assert np.array_equal(qs.cpu().numpy(), qs_r)
     assert np.array_equal(_to_np_ds(ds), ds_r)
+    xa_np = xa.cpu().numpy().astype(np.float64)
+    assert np.array_equal(xa_np[0] + xa_np[1], orc.dequant_q8_1(qs_r, ds_r))
 
 
 def test_quantize_strided_rows(ops, orc):
     xfull = synth.make_x(50, 1024 + 64, 3)
     xt = _dev(xfull)[:, :1024]
-    qs, ds, xh = ops.quantize_q8_1(xt)
+    qs, ds, xh, xa = ops.quantize_q8_1(xt)
     qs_r, ds_r = orc.quantize_q8_1(xfull[:, :1024])
     assert np.array_equal(qs.cpu().numpy(), qs_r)
     assert np.array_equal(_to_np_ds(ds), ds_r)
@@ -91,7 +96,7 @@ def test_subdots_bit_exact(ops, orc, fmt, T, O, K):
     w = synth.make_weights(fmt, O, K, seed=T + O + K)
     x = synth.make_x(T, K, seed=O)
     qs_r, _ = orc.quantize_q8_1(x)
-    _, _, xh = _gpu_quant(ops, x)
+    _, _, xh, _ = _gpu_quant(ops, x)
     got = ops.debug_subdots(fmt, _dev(w), xh, O)
     ops.check_status()
     ref = orc.subdots(fmt, w, qs_r, O)
@@ -109,49 +114,57 @@ def test_subdots_extremes(ops, orc):
     x[2, ::2] *= -1
     x[3, :] = 127.0 * ((np.arange(K) % 3) - 1)
     qs_r, _ = orc.quantize_q8_1(x)
-    _, _, xh = _gpu_quant(ops, x)
+    _, _, xh, _ = _gpu_quant(ops, x)
     assert np.array_equal(ops.debug_subdots("q4_K", _dev(w4), xh, O).cpu().numpy(), orc.subdots("q4_K", w4, qs_r, O))
     assert np.array_equal(ops.debug_subdots("q6_K", _dev(w6), xh, O).cpu().numpy(), orc.subdots("q6_K", w6, qs_r, O))
 
 
 # -------------------------------------------------------------- GEMM ----
 
-def _run_gemm(ops, fmt, w, x, O):
-    qs, ds, xh = _gpu_quant(ops, x)
-    y = ops.gemm(fmt, _dev(w), xh, ds, O)
+def _run_gemm(ops, fmt, w, x, O, kernel="production"):
+    qs, ds, xh, xa = _gpu_quant(ops, x)
+    if kernel == "production" and fmt == "q4_K":
+        y = ops.gemm(fmt, _dev(w), xa, ds, O)
+    else:
+        y = ops.gemm_subblock(fmt, _dev(w), xh, ds, O)
     ops.check_status()
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("fmt", ["q4_K", "q6_K"])
+KERNELS = [("q4_K", "production"), ("q4_K", "subblock"), ("q6_K", "subblock")]
+
+
+@pytest.mark.parametrize("fmt,kernel", KERNELS)
 @pytest.mark.parametrize("T,O,K", [(64, 256, 512), (1, 1, 256), (130, 300, 768), (129, 129, 1280),
                                    (256, 512, 2048)])
-def test_gemm_full_small(ops, orc, fmt, T, O, K):
+def test_gemm_full_small(ops, orc, fmt, kernel, T, O, K):
     w = synth.make_weights(fmt, O, K, seed=7 * T + O)
     x = synth.make_x(T, K, seed=K + T, outliers=T > 1)
     qs_r, ds_r = orc.quantize_q8_1(x)
     ref = orc.gemm(fmt, w, qs_r, ds_r, O)
-    y = _run_gemm(ops, fmt, w, x, O)
+    y = _run_gemm(ops, fmt, w, x, O, kernel)
     assert y.shape == ref.shape
     assert _rel_err(y, ref) <= TOL
 
 
-def test_gemm_config0_tiny(ops, orc):
+@pytest.mark.parametrize("kernel", ["production", "subblock"])
+def test_gemm_config0_tiny(ops, orc, kernel):
     g = synth.config(0).gemms[0]
     w, x = g.weights(), g.x()
     qs_r, ds_r = orc.quantize_q8_1(x)
     ref = orc.gemm(g.fmt, w, qs_r, ds_r, g.O)
-    y = _run_gemm(ops, g.fmt, w, x, g.O)
+    y = _run_gemm(ops, g.fmt, w, x, g.O, kernel)
     assert _rel_err(y, ref) <= TOL
 
 
-def test_gemm_closed_form_superblock(ops):
+@pytest.mark.parametrize("kernel", ["production", "subblock"])
+def test_gemm_closed_form_superblock(ops, kernel):
     sc = [63, 1, 32, 17, 48, 5, 60, 33]
     m = [0, 63, 16, 47, 31, 62, 2, 40]
     q = np.array([(i % 32) % 16 for i in range(256)])
     w = pack_q4K_block(1.0, 1.0, sc, m, q)
     x = np.full((1, 256), 127.0, np.float32)
-    y = _run_gemm(ops, "q4_K", w, x, 1)
+    y = _run_gemm(ops, "q4_K", w, x, 1, kernel)
     assert y[0, 0] == 6833616.0
 
 
@@ -175,36 +188,44 @@ def test_gemm_full_size_sampled(ops, orc, cfg, T):
         x = xs[g.x_seed]
         w = g.weights()
         qs_r, ds_r = orc.quantize_q8_1(x)
-        qs, ds, xh = _gpu_quant(ops, x)
+        qs, ds, xh, xa = _gpu_quant(ops, x)
         assert np.array_equal(qs.cpu().numpy(), qs_r)
         assert np.array_equal(_to_np_ds(ds), ds_r)
-        y = ops.gemm(g.fmt, _dev(w), xh, ds, g.O)
+        wd = _dev(w)
+        outs = []
+        if g.fmt == "q4_K":
+            outs.append(("production", ops.gemm(g.fmt, wd, xa, ds, g.O)))
+        if g.fmt == "q6_K" or cfg in (1, 2):
+            outs.append(("subblock", ops.gemm_subblock(g.fmt, wd, xh, ds, g.O)))
         ops.check_status()
         ti, oi = _sample_points(rng, g.T, g.O)
         ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
-        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-        assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
-        assert torch.isfinite(y).all()
+        for kernel, y in outs:
+            got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
+            assert _rel_err(got, ref) <= TOL, (g.name, kernel, _rel_err(got, ref))
+            assert torch.isfinite(y).all()
 
 
 def test_gemm_repeatable(ops):
     g = synth.config(1).gemms[0]
     w = _dev(g.weights())
-    _, ds, xh = ops.quantize_q8_1(_dev(g.x()))
-    y1 = ops.gemm(g.fmt, w, xh, ds, g.O)
-    y2 = ops.gemm(g.fmt, w, xh, ds, g.O)
+    _, ds, xh, xa = ops.quantize_q8_1(_dev(g.x()))
+    y1 = ops.gemm(g.fmt, w, xa, ds, g.O)
+    y2 = ops.gemm(g.fmt, w, xa, ds, g.O)
+    z1 = ops.gemm_subblock(g.fmt, w, xh, ds, g.O)
+    z2 = ops.gemm_subblock(g.fmt, w, xh, ds, g.O)
     ops.check_status()
-    assert torch.equal(y1, y2)
+    assert torch.equal(y1, y2) and torch.equal(z1, z2)
 
 
 def test_gpu_argument_errors(ops):
     from quantized_prefill_gemm_mmq_gb300._lib import MMQError
     w = torch.zeros(144 * 2, dtype=torch.uint8, device="cuda")
-    xh = torch.zeros((4, 512), dtype=torch.float16, device="cuda")
+    xa = torch.zeros((2, 4, 512), dtype=torch.float16, device="cuda")
     ds = torch.zeros((4, 16), dtype=torch.int32, device="cuda")
     with pytest.raises(ValueError):
-        ops.gemm("q4_K", w, xh, ds, 2)        # wrong weight size for O=2, K=512 is 576 bytes
+        ops.gemm("q4_K", w, xa, ds, 2)        # wrong weight size for O=2, K=512 is 576 bytes
     w2 = torch.zeros(144 * 4 + 4, dtype=torch.uint8, device="cuda")[4:]
     with pytest.raises(MMQError) as e:
-        ops.gemm("q4_K", w2, xh, ds, 2)       # misaligned weight pointer
+        ops.gemm("q4_K", w2, xa, ds, 2)       # misaligned weight pointer
     assert e.value.status == -2
