@@ -79,6 +79,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware for up to hint_ns
+// until the phase completes (it is woken by the completion), so that waiting
+// warps do not take issue slots from the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+constexpr uint32_t kWaitSleepNs = 20000;      // longest single hardware sleep of a wait
+
 // Wait for the phase with the given parity to complete.  Gives up (and
 // returns false) when *abort is set by another role, or after kWaitLimitNs,
 // in which case it records MMQ_ERR_TIMEOUT and raises *abort itself.
@@ -88,9 +106,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *abort = 1u;

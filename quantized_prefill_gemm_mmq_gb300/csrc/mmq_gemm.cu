@@ -997,43 +997,68 @@ __global__ void __launch_bounds__(q4::NTHREADS, 1)
 //     D_sb[t][o] = sum_{k in sb} v[t][k] * sc_b(o)*q[o][k]
 // through two MMAs per 16-k step (hi plane, lo plane).  The epilogue then
 // needs one packed FMA per output per super-block, Y += d*D_sb (Y held in
-// registers), and the min term (split-tf32 tensor-core GEMM over the
-// sub-block index, as in the kernel above) accumulates in its own TMEM
-// columns across K and is added at the end.  The per-sub-block integer dots
-// are not formed here (see mmq_q4K_kernel / the sub-block diagnostics for
-// those); the result differs from them only in f32 summation order.
-// TMEM: [0,384) three rotating super-block accumulators, [384,512) min term.
-// Warps: 0 TMA producer, 1 MMA issuer, 2-5 unpack, 6-13 epilogue, 14-15 scale.
+// registers).  The min term rides in the same accumulator: the tensor core
+// also adds sum_j (dx_j*ssum_j) * (-(dmin*m_j)/d) (split-tf32 MMAs over the
+// sub-block index), so that d*D_sb carries both terms of the super-block.
+// For rows with d == 0 the weight operand is zero and the min operand is
+// divided by 1 instead.  The per-sub-block integer dots are not formed here
+// (see mmq_q4K_kernel / the sub-block diagnostics for those); the result
+// differs from them only in f32 rounding.
+//
+// Two issuing threads.  On sm_103a issuing a 128x128x16 MMA occupies the
+// issuing thread for most of the 64 cycles the MMA executes, and any
+// dependent shared-memory access of that thread (an mbarrier wait included)
+// waits behind its queued MMAs, so a single issuer that synchronises once
+// per stage leaves the tensor pipe idle for a good part of every stage.  Two
+// threads in warps on different SM sub-partitions therefore issue the 64-k
+// stages alternately (even stages / odd stages), each into accumulators of
+// its own, and the epilogue adds the two: while one synchronises, the other's
+// MMAs keep the pipe busy, and every accumulator still sees its MMAs in one
+// fixed order, so results are reproducible bit for bit.
+// Each stage has a single "full" barrier (TMA bytes of both activation
+// planes + the 128 unpack threads' arrivals) and a single "empty" barrier;
+// the unpack warps, which wait on "empty" anyway, take turns issuing the
+// stages' activation TMA (stage ks by unpack warp ks % 4).  The raw weight
+// super-blocks (128 rows x 144 bytes) arrive by TMA one super-block ahead;
+// the unpack and scale threads copy what they need to registers at the
+// start of a super-block and release the raw slot at once.
+// TMEM: [0,256) even-stage accumulators, [256,512) odd-stage accumulators,
+// two super-blocks each (rotating).
+// Warps: 1 and 14 MMA issuers (even / odd stages), 2-5 unpack (+ TMA), 6-13
+// epilogue, 0 and 15 scale.
 // =========================================================================
 namespace q4s {
 
 constexpr int NWARPS = 16;
 constexpr int NTHREADS = NWARPS * 32;
-constexpr int SCALE_WARP0 = 14;
-constexpr int STG = 3;                            // operand ring (A hi, A lo, B tiles)
-constexpr int RSTG = 2;                           // raw super-block ring
+constexpr int MMA_WARP_ODD = 14;
+constexpr int SCALE_WARP_B = 15;                  // scale warps: 0 and 15
+constexpr int STG = 3;                            // operand ring: A hi, A lo, B per 64-k stage
+constexpr int RSTG = 2;                           // raw weight super-block ring
 constexpr int SSTG = 2;                           // scale / min-operand ring
-constexpr int NACC = 3;                           // rotating super-block accumulators
-constexpr uint32_t TM_ACC = 0, TM_MIN = NACC * BN;
-static_assert(TM_MIN + BN <= 512, "TMEM budget");
+constexpr int NACC = 2;                           // rotating super-block accumulators per issuer
+constexpr uint32_t TM_EVEN = 0, TM_ODD = NACC * BN;
+static_assert(TM_ODD + NACC * BN <= 512, "TMEM budget");
 constexpr uint32_t A_STAGE = 2 * A_BYTES;         // hi and lo planes
+constexpr uint32_t STAGE_BYTES = A_STAGE + B_BYTES;
 constexpr uint32_t RAW_BYTES = BN * 144;
 constexpr uint32_t MIN_OP_BYTES = 128 * 64;
 constexpr uint32_t SDS_D = 2 * MIN_OP_BYTES;
 constexpr uint32_t SDS_BYTES = SDS_D + BN * 4;
-constexpr uint32_t oA = 0;
-constexpr uint32_t oB = oA + STG * A_STAGE;
-constexpr uint32_t oRaw = oB + STG * B_BYTES;
+constexpr uint32_t oStage = 0;
+constexpr uint32_t oRaw = oStage + STG * STAGE_BYTES;
 constexpr uint32_t oSds = oRaw + RSTG * RAW_BYTES;
 constexpr uint32_t oBar = oSds + SSTG * SDS_BYTES;
-// a_full, b_full, st_empty [STG]; r_full, r_empty [RSTG]; s_full, s_empty
-// [SSTG]; acc_full, acc_empty [NACC]; mma_done
-constexpr int kNumBars = 3 * STG + 2 * RSTG + 2 * SSTG + 2 * NACC + 1;
+// full, empty [STG]; s_full [SSTG]; acc_full, acc_empty [NACC] (shared by the
+// even and odd accumulators of a super-block); r_full, r_empty [RSTG];
+// done [2] (each issuer's stage completions); mma_done
+constexpr int kNumBars = 2 * STG + SSTG + 2 * NACC + 2 * RSTG + 2 + 1;
 constexpr uint32_t oMisc = oBar + kNumBars * 8;
 constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
 static_assert(kDynSmem <= 232448, "shared memory budget");
-static_assert(oB % 1024 == 0 && oRaw % 1024 == 0 && RAW_BYTES % 1024 == 0, "ring alignment");
+static_assert(STAGE_BYTES % 1024 == 0 && oRaw % 1024 == 0 && RAW_BYTES % 1024 == 0, "ring alignment");
 static_assert(oSds % 16 == 0 && SDS_BYTES % 16 == 0, "min operands must be 16-byte aligned");
+static_assert(NACC >= SSTG, "a scale slot is rewritten only after its accumulator was released");
 
 }  // namespace q4s
 
@@ -1056,38 +1081,36 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     const int nks = K / BK, nsb = K / 256;
 
     const uint32_t bar0 = sbase + oBar;
-    auto a_full = [&](int s) { return bar0 + 8u * s; };
-    auto b_full = [&](int s) { return bar0 + 8u * (STG + s); };
-    auto st_empty = [&](int s) { return bar0 + 8u * (2 * STG + s); };
-    auto r_full = [&](int s) { return bar0 + 8u * (3 * STG + s); };
-    auto r_empty = [&](int s) { return bar0 + 8u * (3 * STG + RSTG + s); };
-    auto s_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + s); };
-    auto s_empty = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + SSTG + s); };
-    auto acc_full = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + s); };
-    auto acc_empty = [&](int s) { return bar0 + 8u * (3 * STG + 2 * RSTG + 2 * SSTG + NACC + s); };
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STG + s); };
+    auto s_full = [&](int s) { return bar0 + 8u * (2 * STG + s); };
+    auto acc_full = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + s); };
+    auto acc_empty = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + NACC + s); };
+    auto r_full = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + s); };
+    auto r_empty = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + RSTG + s); };
+    auto done = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + 2 * RSTG + s); };
     const uint32_t mma_done = bar0 + 8u * (kNumBars - 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + oMisc);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + oMisc + 4);
+    auto stage_a = [&](int s) { return sbase + oStage + (uint32_t)s * STAGE_BYTES; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STG; ++s) {
-            mbar_init(a_full(s), 1);
-            mbar_init(b_full(s), 128);
-            mbar_init(st_empty(s), 1);
+            mbar_init(full(s), 1 + 128);                    // TMA issue (with its bytes) + unpack threads
+            mbar_init(empty(s), 1);                         // the commit of the stage's issuer
+        }
+        for (int s = 0; s < SSTG; ++s) mbar_init(s_full(s), 64);   // scale threads
+        for (int s = 0; s < NACC; ++s) {
+            mbar_init(acc_full(s), 2);                      // both issuers' commits
+            mbar_init(acc_empty(s), NUM_EPI_WARPS);         // after the epilogue has also read d
         }
         for (int s = 0; s < RSTG; ++s) {
             mbar_init(r_full(s), 1);
             mbar_init(r_empty(s), 128 + 64);                // unpack and scale threads
         }
-        for (int s = 0; s < SSTG; ++s) {
-            mbar_init(s_full(s), 64);                       // scale threads
-            mbar_init(s_empty(s), NUM_EPI_WARPS + 1);       // epilogue warps (d) + the MMA's commit
-        }
-        for (int s = 0; s < NACC; ++s) {
-            mbar_init(acc_full(s), 1);
-            mbar_init(acc_empty(s), NUM_EPI_WARPS);
-        }
-        mbar_init(mma_done, 1);
+        mbar_init(done(0), 1);
+        mbar_init(done(1), 1);
+        mbar_init(mma_done, 2);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -1100,115 +1123,108 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer --
+    if (warp == 1 || warp == MMA_WARP_ODD) {
+        // ----------------------------------------------------- MMA issuers --
         if (lane == 0) {
-            tma_prefetch(&tmA);
-            tma_prefetch(&tmW);
-        }
-        int n_a = 0, n_r = 0;
-        bool ok = true;
-        auto issue_raw = [&](int sb) -> bool {
-            const int rs = sb % RSTG;
-            if (!mbar_wait_warp(r_empty(rs), ((sb / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW)) return false;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(r_full(rs), RAW_BYTES);
-                tma_load_2d(sbase + oRaw + rs * RAW_BYTES, &tmW, r_full(rs), sb * 144, o0);
-            }
-            ++n_r;
-            return true;
-        };
-        ok = issue_raw(0);
-        for (int ks = 0; ks < nks && ok; ++ks) {
-            if ((ks & 3) == 0 && (ks >> 2) + 1 < nsb) {
-                ok = issue_raw((ks >> 2) + 1);
-                if (!ok) break;
-            }
-            const int s = ks % STG;
-            ok = mbar_wait_warp(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
-            if (!ok) break;
-            if (lane == 0) {
-                // the activation tensor is [2T][K]: hi plane rows 0..T-1, lo plane rows T..2T-1
-                mbar_arrive_expect_tx(a_full(s), A_STAGE);
-                tma_load_2d(sbase + oA + s * A_STAGE, &tmA, a_full(s), ks * BK, t0);
-                tma_load_2d(sbase + oA + s * A_STAGE + A_BYTES, &tmA, a_full(s), ks * BK, T + t0);
-            }
-            ++n_a;
-            __syncwarp();
-        }
-        if (!ok) {
-            for (int i = max(0, n_a - STG); i < n_a; ++i) wait_drain(a_full(i % STG), (i / STG) & 1);
-            for (int i = max(0, n_r - RSTG); i < n_r; ++i) wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer --
-        if (lane == 0) {
+            const int me = warp == 1 ? 0 : 1;   // stages with ks % 2 == me
             bool ok = true;
-            for (int ks = 0; ks < nks && ok; ++ks) {
+            for (int ks = me; ks < nks && ok; ks += 2) {
                 const int s = ks % STG;
-                const uint32_t par = (ks / STG) & 1;
                 const int sb = ks >> 2, p4 = ks & 3, slot = sb % NACC;
-                ok = mbar_wait(a_full(s), par, abort_flag, kKid, SITE_M_A) &&
-                     mbar_wait(b_full(s), par, abort_flag, kKid, SITE_M_B) &&
-                     (p4 != 0 || mbar_wait(acc_empty(slot), ((sb / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC));
+                // Throttle: this issuer's previous stage has completed.  At most two stages
+                // are then queued in the tensor pipe (the other issuer's, executing, and this
+                // one), and the rest of the ring is free for loading.
+                const int n_mine = ks >> 1;   // stages this issuer has issued so far
+                ok = (n_mine == 0 || mbar_wait(done(me), (n_mine - 1) & 1, abort_flag, kKid, SITE_M_A)) &&
+                     mbar_wait(full(s), (ks / STG) & 1, abort_flag, kKid, SITE_M_A) &&
+                     (p4 > 1 || mbar_wait(acc_empty(slot), ((sb / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a_hi = sbase + oA + s * A_STAGE, a_lo = a_hi + A_BYTES;
-                const uint32_t b_base = sbase + oB + s * B_BYTES;
-                const uint32_t d_acc = tmem_base + TM_ACC + slot * BN;
+                const uint32_t a_hi = stage_a(s);
+                const uint64_t dh = sdesc_k_sw128(a_hi), dl = sdesc_k_sw128(a_hi + A_BYTES),
+                               db = sdesc_k_sw128(a_hi + A_STAGE);
+                const uint32_t d_acc = tmem_base + (me ? TM_ODD : TM_EVEN) + slot * BN;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint32_t koff = (uint32_t)kk * 32u;
-                    const uint64_t bd = sdesc_k_sw128(b_base + koff);
-                    umma_f16(d_acc, sdesc_k_sw128(a_hi + koff), bd, kIdesc, (p4 == 0 && kk == 0) ? 0u : 1u);
-                    umma_f16(d_acc, sdesc_k_sw128(a_lo + koff), bd, kIdesc, 1u);
+                    // +32 bytes along K within the 128-byte swizzled rows = +2 in the address field
+                    umma_f16(d_acc, dh + 2 * kk, db + 2 * kk, kIdesc, (p4 <= 1 && kk == 0) ? 0u : 1u);
+                    umma_f16(d_acc, dl + 2 * kk, db + 2 * kk, kIdesc, 1u);
                 }
-                umma_commit(st_empty(s));
                 if (p4 == 3) {
-                    // min term of this super-block, accumulated across K
+                    // min term of this super-block, into the odd accumulator
                     const int ss = sb % SSTG;
                     ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
-                    const uint32_t dmn = tmem_base + TM_MIN;
-                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32,
-                              sb > 0 ? 1u : 0u);
-                    umma_tf32(dmn, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
-                    umma_tf32(dmn, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
-                    umma_commit(acc_full(slot));
-                    umma_commit(s_empty(ss));
+                    umma_tf32(d_acc, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(d_acc, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(d_acc, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
                 }
+                if (p4 >= 2) umma_commit(acc_full(slot));   // this issuer's last stage of the super-block
+                umma_commit(empty(s));
+                umma_commit(done(me));
             }
             umma_commit(mma_done);
             if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
         }
         __syncwarp();
-    } else if (warp < EPI_WARP0) {
+    } else if (warp >= UNPACK_WARP0 && warp < EPI_WARP0) {
         // ------------------------------------------------------ unpack warps --
-        const int r = threadIdx.x - UNPACK_WARP0 * 32;   // weight row of the B tile
+        // Thread = one weight row (rows past O arrive zero-filled).  At the
+        // start of a super-block it copies the row's 144 raw bytes to
+        // registers; per 64-k stage it writes the row's 64 values sc*q as f16
+        // into the swizzled B tile (zeros when the row's d is zero).  Thread 0
+        // also issues the raw tile one super-block ahead.
+        const int r = threadIdx.x - UNPACK_WARP0 * 32;
+        const bool tma_lane = (r & 31) == 0;
         bool ok = true;
+        int last_a = -1;   // last activation stage this thread issued
+        if (r == 0) {
+            tma_prefetch(&tmA);
+            tma_prefetch(&tmW);
+            mbar_arrive_expect_tx(r_full(0), RAW_BYTES);
+            tma_load_2d(sbase + oRaw, &tmW, r_full(0), 0, o0);
+        }
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int rs = sb % RSTG;
             ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW);
             if (!ok) break;
-            const uint8_t *raw = smem + oRaw + rs * RAW_BYTES + r * 144;
-            const uint4 hd = *reinterpret_cast<const uint4 *>(raw);
+            uint4 cur[9];
+            const uint4 *raw = reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + r * 144);
+#pragma unroll
+            for (int i = 0; i < 9; ++i) cur[i] = raw[i];
+            mbar_arrive(r_empty(rs));
+            if (r == 0 && sb + 1 < nsb) {
+                const int rn = (sb + 1) % RSTG;
+                ok = mbar_wait(r_empty(rn), (((sb + 1) / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
+                if (ok) {
+                    mbar_arrive_expect_tx(r_full(rn), RAW_BYTES);
+                    tma_load_2d(sbase + oRaw + rn * RAW_BYTES, &tmW, r_full(rn), (sb + 1) * 144, o0);
+                }
+            }
 #pragma unroll
             for (int p4 = 0; p4 < 4; ++p4) {
                 const int ks = sb * 4 + p4, s = ks % STG;
                 int sc_lo, sc_hi, unused;
-                q4::q4K_scale_min(hd.y, hd.z, hd.w, 2 * p4, sc_lo, unused);
-                q4::q4K_scale_min(hd.y, hd.z, hd.w, 2 * p4 + 1, sc_hi, unused);
-                const float slo = (float)sc_lo, shi = (float)sc_hi;
+                q4::q4K_scale_min(cur[0].y, cur[0].z, cur[0].w, 2 * p4, sc_lo, unused);
+                q4::q4K_scale_min(cur[0].y, cur[0].z, cur[0].w, 2 * p4 + 1, sc_hi, unused);
+                const bool d_zero = (cur[0].x & 0x7FFFu) == 0u;
+                const float slo = d_zero ? 0.0f : (float)sc_lo, shi = d_zero ? 0.0f : (float)sc_hi;
                 const __half2 mlo = __float2half2_rn(slo), alo = __float2half2_rn(-1024.0f * slo);
                 const __half2 mhi = __float2half2_rn(shi * 0.0625f), ahi = __float2half2_rn(-64.0f * shi);
-                const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4);
-                const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4 + 16);
-                ok = mbar_wait(st_empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
+                const uint4 w0 = cur[1 + 2 * p4], w1 = cur[2 + 2 * p4];
+                ok = mbar_wait(empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
                 if (!ok) break;
+                if (tma_lane && (r >> 5) == (ks & 3)) {
+                    // the activation tensor is [2T][K]: hi plane rows 0..T-1, lo plane rows T..2T-1
+                    mbar_arrive_expect_tx(full(s), A_STAGE);
+                    tma_load_2d(stage_a(s), &tmA, full(s), ks * BK, t0);
+                    tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(s), ks * BK, T + t0);
+                    last_a = ks;
+                }
                 const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                uint8_t *brow = smem + oB + s * B_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+                uint8_t *brow = smem + oStage + s * STAGE_BYTES + A_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint32_t wa = wv[2 * (c & 3)], wb = wv[2 * (c & 3) + 1];
@@ -1222,14 +1238,16 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                     *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = v;
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(b_full(s));
+                mbar_arrive(full(s));
             }
-            if (ok) mbar_arrive(r_empty(rs));
         }
-    } else if (warp < SCALE_WARP0) {
+        if (!ok && last_a >= 0)
+            for (int i = max(0, last_a - STG + 1); i <= last_a; ++i)
+                if ((i & 3) == (r >> 5)) wait_drain(full(i % STG), (i / STG) & 1);
+    } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
         // --------------------------------------------------------- epilogue --
-        // Thread = one token (TMEM lane) x 64 weight rows; Y += d*D_sb per
-        // super-block in registers, plus the min term at the end.
+        // Thread = one token (TMEM lane) x 64 weight rows; Y += d*(D_even +
+        // D_odd) per super-block in registers.
         const int ew = warp - EPI_WARP0;
         const int quarter = warp & 3;
         const int c0 = (ew >> 2) * 64;
@@ -1248,67 +1266,58 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const float *dv = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + SDS_D) + c0;
+            const uint32_t col = tmem_base + lane_off + slot * BN + c0;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t rv[32];
-                tmem_ld32(tmem_base + lane_off + TM_ACC + (uint32_t)(slot * BN + c0 + hh * 32), rv);
-                tmem_ld_wait(rv);
-                if (hh == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acc_empty(slot));
-                }
+            for (int q = 0; q < 4; ++q) {
+                uint32_t ra[16], rb[16];
+                tmem_ld16(col + TM_EVEN + q * 16, ra);
+                tmem_ld16(col + TM_ODD + q * 16, rb);
+                tmem_ld_wait2(ra, rb);
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(dv + hh * 32 + i);
-                    const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(rv[i]), __uint_as_float(rv[i + 1])),
-                                                 make_float2(d4.x, d4.y),
-                                                 make_float2(yv[hh * 32 + i], yv[hh * 32 + i + 1]));
-                    const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(rv[i + 2]), __uint_as_float(rv[i + 3])),
-                                                 make_float2(d4.z, d4.w),
-                                                 make_float2(yv[hh * 32 + i + 2], yv[hh * 32 + i + 3]));
-                    yv[hh * 32 + i] = y0.x;
-                    yv[hh * 32 + i + 1] = y0.y;
-                    yv[hh * 32 + i + 2] = y1.x;
-                    yv[hh * 32 + i + 3] = y1.y;
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(dv + q * 16 + i);
+                    const float2 s0 = __fadd2_rn(make_float2(__uint_as_float(ra[i]), __uint_as_float(ra[i + 1])),
+                                                 make_float2(__uint_as_float(rb[i]), __uint_as_float(rb[i + 1])));
+                    const float2 s1 = __fadd2_rn(make_float2(__uint_as_float(ra[i + 2]), __uint_as_float(ra[i + 3])),
+                                                 make_float2(__uint_as_float(rb[i + 2]), __uint_as_float(rb[i + 3])));
+                    const int e = q * 16 + i;
+                    const float2 y0 = __ffma2_rn(s0, make_float2(d4.x, d4.y), make_float2(yv[e], yv[e + 1]));
+                    const float2 y1 = __ffma2_rn(s1, make_float2(d4.z, d4.w), make_float2(yv[e + 2], yv[e + 3]));
+                    yv[e] = y0.x;
+                    yv[e + 1] = y0.y;
+                    yv[e + 2] = y1.x;
+                    yv[e + 3] = y1.y;
                 }
             }
+            // both accumulators and this super-block's d have been read
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty(ss));
+            if (lane == 0) mbar_arrive(acc_empty(slot));
         }
-        if (ok) {
-            // every min-term MMA was issued before the last accumulator's commit
-            float *yrow = p.y + (size_t)(tok_ok ? t : 0) * O + o0 + c0;
-            const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
+        if (ok && tok_ok) {
+            float *yrow = p.y + (size_t)t * O + o0 + c0;
+            if ((O & 3) == 0 && o0 + c0 + 64 <= O) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t mv[32];
-                tmem_ld32(tmem_base + lane_off + TM_MIN + c0 + hh * 32, mv);
-                tmem_ld_wait(mv);
-                if (tok_ok) {
-                    if (vec) {
+                for (int i = 0; i < 64; i += 4)
+                    *reinterpret_cast<float4 *>(yrow + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+            } else {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(yrow + hh * 32 + i) =
-                                make_float4(yv[hh * 32 + i] + __uint_as_float(mv[i]),
-                                            yv[hh * 32 + i + 1] + __uint_as_float(mv[i + 1]),
-                                            yv[hh * 32 + i + 2] + __uint_as_float(mv[i + 2]),
-                                            yv[hh * 32 + i + 3] + __uint_as_float(mv[i + 3]));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (o0 + c0 + hh * 32 + i < O) yrow[hh * 32 + i] = yv[hh * 32 + i] + __uint_as_float(mv[i]);
-                    }
-                }
+                for (int i = 0; i < 64; ++i)
+                    if (o0 + c0 + i < O) yrow[i] = yv[i];
             }
         }
-    } else {
+    } else if (warp == 0 || warp == SCALE_WARP_B) {
         // ------------------------------------------------------- scale warps --
-        // Per super-block, for weight rows r and r+64: d and the min-term
-        // operand row (-(dmin*m_j) split hi/lo); for tokens r and r+64: the
-        // min-term operand row (dx_j*ssum_j split hi/lo).  The q8_1 scale words
-        // are fetched one super-block ahead.
-        const int sr = threadIdx.x - SCALE_WARP0 * 32;   // 0..63
+        // Per super-block, for weight rows r and r + 64: the multiplier d (1
+        // where d == 0) and the min-term operand row (-(dmin*m_j)/d, split
+        // hi/lo); for tokens r and r + 64: the min-term operand row
+        // (dx_j*ssum_j split hi/lo).  Slot sb % SSTG is rewritten once
+        // super-block sb - SSTG's accumulators have been released: its
+        // min-term MMAs completed before they were handed to the epilogue,
+        // and the epilogue releases them after reading d.  The weight headers
+        // come from the raw tile, the q8_1 scale words are fetched one
+        // super-block ahead.
+        const int sr = (warp == 0 ? 0 : 32) + lane;   // 0..63
         uint4 dsn[2][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -1322,24 +1331,35 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         }
         bool ok = true;
         for (int sb = 0; sb < nsb && ok; ++sb) {
-            const int rs = sb % RSTG, ss = sb % SSTG;
-            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW) &&
-                 mbar_wait(s_empty(ss), ((sb / SSTG) & 1) ^ 1, abort_flag, kKid, SITE_U_SDS);
+            const int ss = sb % SSTG, rs = sb % RSTG;
+            ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW);
             if (!ok) break;
+            uint4 hdn[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                hdn[h] = *reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + (sr + 64 * h) * 144);
+            mbar_arrive(r_empty(rs));
+            if (sb >= SSTG) {
+                const int prev = sb - SSTG;
+                ok = mbar_wait(acc_empty(prev % NACC), (prev / NACC) & 1, abort_flag, kKid, SITE_U_SDS);
+                if (!ok) break;
+            }
             uint8_t *slot = smem + oSds + ss * SDS_BYTES;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int r = sr + 64 * h;
-                const uint4 hd = *reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + r * 144);
+                const uint4 hd = hdn[h];
                 const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
                 const float dmin = __half2float(__ushort_as_half((unsigned short)(hd.x >> 16)));
-                reinterpret_cast<float *>(slot + SDS_D)[r] = d;
+                const float mult = d != 0.0f ? d : 1.0f;
+                const float rmult = __frcp_rn(mult);
+                reinterpret_cast<float *>(slot + SDS_D)[r] = mult;
                 float bh[8], bl[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     int sc, mm;
                     q4::q4K_scale_min(hd.y, hd.z, hd.w, j, sc, mm);
-                    const float v = -(dmin * (float)mm);
+                    const float v = -(dmin * (float)mm) * rmult;   // dmin*m exact: 11 x 6 bits
                     bh[j] = to_tf32(v);
                     bl[j] = to_tf32(v - bh[j]);
                 }
@@ -1350,13 +1370,13 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float dx = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
-                    const float v = dx * (float)(int)(int16_t)(w[j] >> 16);
+                    const float v = dx * (float)(int)(int16_t)(w[j] >> 16);   // exact: 11-bit x 12-bit
                     ah[j] = to_tf32(v);
                     al[j] = to_tf32(v - ah[j]);
                 }
                 q4::put_min_row(slot, r, ah, al);
                 const int t = t0 + r;
-                if (t < T && sb + 1 < nsb) {
+                if (sb + 1 < nsb && t < T) {
                     const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + (sb + 1) * 8);
                     dsn[h][0] = __ldg(dp);
                     dsn[h][1] = __ldg(dp + 1);
@@ -1364,7 +1384,6 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(s_full(ss));
-            mbar_arrive(r_empty(rs));
         }
     }
 
@@ -1399,8 +1418,8 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(mmq_q4K_sb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)q4s::kDynSmem) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(mmq_q4K_sb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)q4s::kDynSmem) != cudaSuccess)
             return launch_status();
         attr_done[dev] = true;
     }
