@@ -1060,6 +1060,16 @@ static_assert(STAGE_BYTES % 1024 == 0 && oRaw % 1024 == 0 && RAW_BYTES % 1024 ==
 static_assert(oSds % 16 == 0 && SDS_BYTES % 16 == 0, "min operands must be 16-byte aligned");
 static_assert(NACC >= SSTG, "a scale slot is rewritten only after its accumulator was released");
 
+// Two f16 values sc*q from the two bytes of x selected by sel (x holds the
+// quants already masked: q in the low nibble, or 16q in the high nibble):
+// the bytes become the low halves of 1024 + b, then one packed FMA with
+// (m, a) = (sc, -1024 sc) or (sc/16, -64 sc).  Every step is exact.
+__device__ __forceinline__ uint32_t magic2(uint32_t x, uint32_t sel, __half2 m, __half2 a)
+{
+    const uint32_t h = __byte_perm(x, 0x64646464u, sel);
+    return q4::h2bits(__hfma2(*reinterpret_cast<const __half2 *>(&h), m, a));
+}
+
 }  // namespace q4s
 
 __global__ void __launch_bounds__(q4s::NTHREADS, 1)
@@ -1213,7 +1223,19 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 const float slo = d_zero ? 0.0f : (float)sc_lo, shi = d_zero ? 0.0f : (float)sc_hi;
                 const __half2 mlo = __float2half2_rn(slo), alo = __float2half2_rn(-1024.0f * slo);
                 const __half2 mhi = __float2half2_rn(shi * 0.0625f), ahi = __float2half2_rn(-64.0f * shi);
-                const uint4 w0 = cur[1 + 2 * p4], w1 = cur[2 + 2 * p4];
+                // convert before waiting for the slot: only the stores need it
+                uint4 vv[8];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 q = cur[1 + 2 * p4 + (c >> 1)];
+                    const uint32_t w_a = (c & 1) ? q.z : q.x, w_b = (c & 1) ? q.w : q.y;
+                    const uint32_t la = w_a & 0x0F0F0F0Fu, lb = w_b & 0x0F0F0F0Fu;
+                    const uint32_t ha = w_a & 0xF0F0F0F0u, hb = w_b & 0xF0F0F0F0u;
+                    vv[c] = make_uint4(q4s::magic2(la, 0x4140u, mlo, alo), q4s::magic2(la, 0x4342u, mlo, alo),
+                                       q4s::magic2(lb, 0x4140u, mlo, alo), q4s::magic2(lb, 0x4342u, mlo, alo));
+                    vv[c + 4] = make_uint4(q4s::magic2(ha, 0x4140u, mhi, ahi), q4s::magic2(ha, 0x4342u, mhi, ahi),
+                                           q4s::magic2(hb, 0x4140u, mhi, ahi), q4s::magic2(hb, 0x4342u, mhi, ahi));
+                }
                 ok = mbar_wait(empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
                 if (!ok) break;
                 if (tma_lane && (r >> 5) == (ks & 3)) {
@@ -1223,20 +1245,9 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                     tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(s), ks * BK, T + t0);
                     last_a = ks;
                 }
-                const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
                 uint8_t *brow = smem + oStage + s * STAGE_BYTES + A_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t wa = wv[2 * (c & 3)], wb = wv[2 * (c & 3) + 1];
-                    const uint32_t mask = c < 4 ? 0x000F000Fu : 0x00F000F0u;
-                    const __half2 m2 = c < 4 ? mlo : mhi, a2 = c < 4 ? alo : ahi;
-                    uint4 v;
-                    v.x = q4::nib2(wa, 0x4140u, mask, m2, a2);
-                    v.y = q4::nib2(wa, 0x4342u, mask, m2, a2);
-                    v.z = q4::nib2(wb, 0x4140u, mask, m2, a2);
-                    v.w = q4::nib2(wb, 0x4342u, mask, m2, a2);
-                    *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = v;
-                }
+                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = vv[c];
                 fence_proxy_async_smem();
                 mbar_arrive(full(s));
             }
