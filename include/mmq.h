@@ -121,6 +121,26 @@ int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *ds,
                  float *y, int T, int O, int K, mmq_stream_t stream);
 
 /*
+ * Split-K form of mmq_gemm_q4K for outputs with few 128 x 128 tiles (small T):
+ * the super-blocks of each row are divided among up to `ksplit` CTAs per
+ * output tile (ceil(K/256 / ksplit) each).  Every CTA writes its partial sums
+ * to `part` [splits][T][O] f32; the last CTA of a tile to finish (counted in
+ * counters[tile], tile = (t/128) * ceil(O/128) + o/128) adds the splits in
+ * split order and writes y, so the result is the same on every call.  The
+ * sum is the same mathematical Y as mmq_gemm_q4K's; only the f32 summation
+ * order differs.
+ * part, counters: caller-owned device scratch; mmq_splitk_sizes gives their
+ * sizes.  counters (int32, 4-byte aligned) must be all zero before the first
+ * call and are left all zero by every completed call.  Two calls that use
+ * the same part/counters at the same time (different streams) race.
+ * ksplit == 1 is mmq_gemm_q4K (part and counters unused, may be NULL).
+ * Limits as mmq_gemm_q4K; ksplit >= 1; part 16-byte aligned.
+ */
+int mmq_splitk_sizes(int T, int O, int K, int ksplit, int64_t *part_floats, int64_t *counters);
+int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint32_t *ds, float *y,
+                        int T, int O, int K, int ksplit, float *part, int *counters, mmq_stream_t stream);
+
+/*
  * The same q4_K GEMM in the pages' per-sub-block form: the tensor core forms
  * every 32-weight sub-block's exact integer dot (times its 6-bit scale) in
  * its own TMEM accumulator and the f32 fold dx_b*C'_b runs per sub-block

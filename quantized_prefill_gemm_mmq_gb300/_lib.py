@@ -25,6 +25,8 @@ SIGNATURES = {
     "mmq_quantize_q8_1": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P]),
     "mmq_gemm_q4K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q4K_subblock": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_splitk_sizes": (_I, [_I, _I, _I, _I, _P, _P]),
+    "mmq_gemm_q4K_splitk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "mmq_gemm_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q4K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q6K": (_I, [_P, _P, _P, _I, _I, _I, _P]),

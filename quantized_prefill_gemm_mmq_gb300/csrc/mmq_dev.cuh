@@ -95,7 +95,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return done != 0;
 }
 
-constexpr uint32_t kWaitSleepNs = 20000;      // longest single hardware sleep of a wait
+constexpr uint32_t kWaitSleepNs = 20000;     // longest single hardware sleep of a wait
 
 // Wait for the phase with the given parity to complete.  Gives up (and
 // returns false) when *abort is set by another role, or after kWaitLimitNs,
@@ -125,6 +125,12 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, kernel_id, site);
     return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// barrier among `count` threads (whole warps) on hardware barrier `id` (1..15)
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // -------------------------------------------------------------------- TMA --

@@ -32,6 +32,7 @@
 //     thread drains its tensor-core work and TMEM is freed.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "mmq_dev.cuh"
@@ -102,6 +103,13 @@ struct Params {
     float *y;             // [T][O]
     int32_t *sub;         // [T][O][K/kKSub] (subdots mode)
     int T, O, K;
+    // split-K (production q4_K kernel): blockIdx.z handles super-blocks
+    // [z*sb_per_split, min(nsb, (z+1)*sb_per_split)); with part != nullptr the
+    // partial sums go to part[z][T][O] and the last CTA of each output tile
+    // (counted in cnt[tile]) adds them in z order and writes y.
+    int sb_per_split;
+    float *part;
+    int *cnt;
 };
 
 // wait sites recorded with a timeout
@@ -1088,7 +1096,11 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int o0 = blockIdx.x * BN, t0 = blockIdx.y * BM;
     const int T = p.T, K = p.K, O = p.O;
-    const int nks = K / BK, nsb = K / 256;
+    // this CTA's super-blocks: [sb_base, sb_base + nsb) of the K/256 in a row
+    const int nsb_row = K / 256;
+    const int sb_base = blockIdx.z * p.sb_per_split;
+    const int nsb = min(nsb_row - sb_base, p.sb_per_split);
+    const int nks = nsb * 4;
 
     const uint32_t bar0 = sbase + oBar;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -1194,7 +1206,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             tma_prefetch(&tmA);
             tma_prefetch(&tmW);
             mbar_arrive_expect_tx(r_full(0), RAW_BYTES);
-            tma_load_2d(sbase + oRaw, &tmW, r_full(0), 0, o0);
+            tma_load_2d(sbase + oRaw, &tmW, r_full(0), sb_base * 144, o0);
         }
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int rs = sb % RSTG;
@@ -1210,7 +1222,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 ok = mbar_wait(r_empty(rn), (((sb + 1) / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
                 if (ok) {
                     mbar_arrive_expect_tx(r_full(rn), RAW_BYTES);
-                    tma_load_2d(sbase + oRaw + rn * RAW_BYTES, &tmW, r_full(rn), (sb + 1) * 144, o0);
+                    tma_load_2d(sbase + oRaw + rn * RAW_BYTES, &tmW, r_full(rn), (sb_base + sb + 1) * 144, o0);
                 }
             }
 #pragma unroll
@@ -1241,8 +1253,8 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 if (tma_lane && (r >> 5) == (ks & 3)) {
                     // the activation tensor is [2T][K]: hi plane rows 0..T-1, lo plane rows T..2T-1
                     mbar_arrive_expect_tx(full(s), A_STAGE);
-                    tma_load_2d(stage_a(s), &tmA, full(s), ks * BK, t0);
-                    tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(s), ks * BK, T + t0);
+                    tma_load_2d(stage_a(s), &tmA, full(s), (sb_base * 4 + ks) * BK, t0);
+                    tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(s), (sb_base * 4 + ks) * BK, T + t0);
                     last_a = ks;
                 }
                 uint8_t *brow = smem + oStage + s * STAGE_BYTES + A_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
@@ -1305,16 +1317,66 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(slot));
         }
-        if (ok && tok_ok) {
-            float *yrow = p.y + (size_t)t * O + o0 + c0;
-            if ((O & 3) == 0 && o0 + c0 + 64 <= O) {
+        const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
+        auto store_row = [&](float *row) {
+            if (vec) {
 #pragma unroll
                 for (int i = 0; i < 64; i += 4)
-                    *reinterpret_cast<float4 *>(yrow + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+                    *reinterpret_cast<float4 *>(row + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 64; ++i)
-                    if (o0 + c0 + i < O) yrow[i] = yv[i];
+                    if (o0 + c0 + i < O) row[i] = yv[i];
+            }
+        };
+        if (p.part == nullptr || gridDim.z == 1) {
+            if (ok && tok_ok) store_row(p.y + (size_t)t * O + o0 + c0);
+        } else {
+            // split-K: publish this split's partial sums; the last CTA of the
+            // tile to arrive adds all splits in z order (deterministic)
+            if (ok && tok_ok) store_row(p.part + ((size_t)blockIdx.z * T + t) * O + o0 + c0);
+            __threadfence();
+            named_bar_sync(1, NUM_EPI_WARPS * 32);
+            uint32_t *last_flag = reinterpret_cast<uint32_t *>(smem + oMisc + 8);
+            if (warp == EPI_WARP0 && lane == 0) {
+                int *c = p.cnt + blockIdx.y * gridDim.x + blockIdx.x;
+                const int prev = atomicAdd(c, 1);
+                const bool last = prev == (int)gridDim.z - 1;
+                if (last) *c = 0;   // ready for the next launch on this stream
+                *last_flag = last ? 1u : 0u;
+            }
+            named_bar_sync(1, NUM_EPI_WARPS * 32);
+            if (*last_flag && ok && tok_ok) {
+                __threadfence();
+#pragma unroll
+                for (int i = 0; i < 64; i += 4) {
+                    float4 a4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    for (int z = 0; z < (int)gridDim.z; ++z) {
+                        float4 v;
+                        if (z == (int)blockIdx.z) {
+                            v = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+                        } else {
+                            const float *prow = p.part + ((size_t)z * T + t) * O + o0 + c0 + i;
+                            if (vec) {
+                                v = __ldcg(reinterpret_cast<const float4 *>(prow));
+                            } else {
+                                v.x = o0 + c0 + i < O ? __ldcg(prow) : 0.0f;
+                                v.y = o0 + c0 + i + 1 < O ? __ldcg(prow + 1) : 0.0f;
+                                v.z = o0 + c0 + i + 2 < O ? __ldcg(prow + 2) : 0.0f;
+                                v.w = o0 + c0 + i + 3 < O ? __ldcg(prow + 3) : 0.0f;
+                            }
+                        }
+                        a4.x += v.x;
+                        a4.y += v.y;
+                        a4.z += v.z;
+                        a4.w += v.w;
+                    }
+                    yv[i] = a4.x;
+                    yv[i + 1] = a4.y;
+                    yv[i + 2] = a4.z;
+                    yv[i + 3] = a4.w;
+                }
+                store_row(p.y + (size_t)t * O + o0 + c0);
             }
         }
     } else if (warp == 0 || warp == SCALE_WARP_B) {
@@ -1335,7 +1397,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             const int t = t0 + sr + 64 * h;
             dsn[h][0] = dsn[h][1] = make_uint4(0u, 0u, 0u, 0u);
             if (t < T) {
-                const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32));
+                const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + sb_base * 8);
                 dsn[h][0] = __ldg(dp);
                 dsn[h][1] = __ldg(dp + 1);
             }
@@ -1388,7 +1450,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 q4::put_min_row(slot, r, ah, al);
                 const int t = t0 + r;
                 if (sb + 1 < nsb && t < T) {
-                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + (sb + 1) * 8);
+                    const uint4 *dp = reinterpret_cast<const uint4 *>(p.ds + (size_t)t * (K / 32) + (sb_base + sb + 1) * 8);
                     dsn[h][0] = __ldg(dp);
                     dsn[h][1] = __ldg(dp + 1);
                 }
@@ -1407,21 +1469,29 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
 }
 
 // Production q4_K launch: activations as the [2T][K] f16 hi/lo planes.
-int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K,
-                  mmq_stream_t stream)
+// ksplit <= 1 or part == nullptr: one CTA per output tile covers all of K.
+int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K, int ksplit,
+                  float *part, int *cnt, mmq_stream_t stream)
 {
     if (T < 0 || O < 1 || K < 256 || K > (1 << 20) || (K & 255)) return MMQ_ERR_SHAPE;
     if (T == 0) return MMQ_OK;
     if (!w || !xa || !ds || !y) return MMQ_ERR_NULL;
     if (!aligned16(w) || !aligned16(xa) || !aligned16(ds) || !aligned16(y)) return MMQ_ERR_ALIGN;
+    const int nsb = K / 256;
+    int sbps = nsb, splits = 1;
+    if (part != nullptr && ksplit > 1) {
+        if (!cnt) return MMQ_ERR_NULL;
+        if (!aligned16(part) || ((uintptr_t)cnt & 3u)) return MMQ_ERR_ALIGN;
+        sbps = (nsb + min(ksplit, nsb) - 1) / min(ksplit, nsb);
+        splits = (nsb + sbps - 1) / sbps;
+    }
     int rc = check_arch();
     if (rc != MMQ_OK) return rc;
-    const long long nsb = K / 256;
     CUtensorMap tmA, tmW;
     rc = make_tmap_2d(&tmA, xa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, 2ull * (uint64_t)T, (uint64_t)K * 2, BK,
                       BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MMQ_OK) return rc;
-    rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)(nsb * 144), (uint64_t)O, (uint64_t)(nsb * 144),
+    rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)nsb * 144, (uint64_t)O, (uint64_t)nsb * 144,
                       144, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != MMQ_OK) return rc;
     static bool attr_done[64];
@@ -1442,7 +1512,10 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     prm.T = T;
     prm.O = O;
     prm.K = K;
-    const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM));
+    prm.sb_per_split = sbps;
+    prm.part = splits > 1 ? part : nullptr;
+    prm.cnt = splits > 1 ? cnt : nullptr;
+    const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM), (unsigned)splits);
     mmq_q4K_sb_kernel<<<grid, q4s::NTHREADS, q4s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
     return launch_status();
 }
@@ -1508,7 +1581,26 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
 extern "C" int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K,
                             mmq_stream_t stream)
 {
-    return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, stream);
+    return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, 1, nullptr, nullptr, stream);
+}
+
+extern "C" int mmq_splitk_sizes(int T, int O, int K, int ksplit, int64_t *part_floats, int64_t *counters)
+{
+    if (T < 1 || O < 1 || K < 256 || K > (1 << 20) || (K & 255) || ksplit < 1) return MMQ_ERR_SHAPE;
+    const int nsb = K / 256;
+    const int sbps = (nsb + std::min(ksplit, nsb) - 1) / std::min(ksplit, nsb);
+    const int splits = (nsb + sbps - 1) / sbps;
+    if (part_floats) *part_floats = splits > 1 ? (int64_t)splits * T * O : 0;
+    if (counters) *counters = (int64_t)((O + mmq::BN - 1) / mmq::BN) * ((T + mmq::BM - 1) / mmq::BM);
+    return MMQ_OK;
+}
+
+extern "C" int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O,
+                                   int K, int ksplit, float *part, int *counters, mmq_stream_t stream)
+{
+    if (ksplit < 1) return MMQ_ERR_SHAPE;
+    if (ksplit > 1 && (!part || !counters)) return MMQ_ERR_NULL;
+    return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, ksplit, part, counters, stream);
 }
 
 extern "C" int mmq_gemm_q4K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O,

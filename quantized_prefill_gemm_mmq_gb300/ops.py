@@ -117,6 +117,52 @@ def gemm(fmt: str, w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int,
     return out
 
 
+def splitk_sizes(T: int, O: int, K: int, ksplit: int) -> tuple[int, int]:
+    """(floats of partial-sum workspace, ints of tile counters) for a split-K q4_K GEMM."""
+    pf, nc = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check("mmq_splitk_sizes", load().mmq_splitk_sizes(T, O, K, ksplit, ctypes.byref(pf), ctypes.byref(nc)))
+    return pf.value, nc.value
+
+
+def choose_ksplit(T: int, O: int, K: int, sms: int = 148) -> int:
+    """Splits of K that bring the grid near one wave when the output has few tiles."""
+    tiles = -(-O // 128) * -(-T // 128)
+    return max(1, min(K // 256, sms // max(1, tiles)))
+
+
+class SplitKWorkspace:
+    """Caller-owned scratch of the split-K q4_K GEMM: partial sums and tile
+    counters (the counters start at zero and every call leaves them at zero).
+    Calls that share one workspace must be ordered (one stream)."""
+
+    def __init__(self, device, max_partial_floats: int, max_tiles: int):
+        self.part = torch.empty(max(1, max_partial_floats), dtype=torch.float32, device=device)
+        self.counters = torch.zeros(max(1, max_tiles), dtype=torch.int32, device=device)
+
+    def fits(self, partial_floats: int, tiles: int) -> bool:
+        return partial_floats <= self.part.numel() and tiles <= self.counters.numel()
+
+
+def gemm_splitk(w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int, ksplit: int | None = None,
+                workspace: SplitKWorkspace | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """q4_K production GEMM with K split over `ksplit` CTAs per output tile (default:
+    choose_ksplit); partial sums are added in a fixed order, so results repeat bit
+    for bit.  Without `workspace` one is allocated for this call."""
+    T, K = _check_gemm_args("q4_K", w, xa, O, planes=2)
+    _check_ds(ds, T, K)
+    out = _out(out, T, O, xa.device)
+    if ksplit is None:
+        ksplit = choose_ksplit(T, O, K)
+    pf, nc = splitk_sizes(T, O, K, ksplit)
+    if workspace is None or not workspace.fits(pf, nc):
+        workspace = SplitKWorkspace(xa.device, pf, nc)
+    with torch.cuda.device(xa.device):
+        st = load().mmq_gemm_q4K_splitk(_ptr(w), _ptr(xa), _ptr(ds), _ptr(out), T, O, K, ksplit,
+                                        _ptr(workspace.part), _ptr(workspace.counters), _stream(xa.device))
+    _check("mmq_gemm_q4K_splitk", st)
+    return out
+
+
 def gemm_subblock(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
                   out: torch.Tensor | None = None) -> torch.Tensor:
     """Per-sub-block GEMM (exact integer sub-block dots + f32 fold) from the xh/ds planes."""

@@ -17,7 +17,8 @@ needs_lib = pytest.mark.skipif(not HAVE_LIB, reason="libmmq.so not built (run __
 def test_header_declares_the_boundary():
     names = _lib.header_functions()
     for required in ("mmq_quantize_q8_1", "mmq_gemm_q4K", "mmq_gemm_q4K_subblock", "mmq_gemm_q6K", "mmq_check_status",
-                     "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K"):
+                     "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K",
+                     "mmq_gemm_q4K_splitk", "mmq_splitk_sizes"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -34,7 +35,7 @@ def test_library_exports_every_header_symbol():
 @needs_lib
 def test_library_loads_and_reports():
     lib = _lib.load()
-    assert lib.mmq_version() == 2
+    assert lib.mmq_version() == 3
     assert lib.mmq_status_str(0) == b"ok"
     for code in range(-8, 0):
         assert lib.mmq_status_str(code) not in (b"", b"unknown status")
@@ -62,6 +63,32 @@ def test_argument_errors_without_gpu():
     assert lib.mmq_quantize_q8_1(p, 32, 1, 32, null, p, null, null, null) == -6   # no value plane
     assert lib.mmq_gemm_q4K(odd, p, p, p, 1, 1, 256, null) == -2
     assert lib.mmq_quantize_q8_1(p, 34, 1, 32, p, p, p, p, null) == -2          # ldx * 4 not 16-aligned
+    # split-K: workspace required when splitting, ksplit >= 1
+    assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, null, p, null) == -6
+    assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, p, null, null) == -6
+    assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 0, p, p, null) == -1
+    assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, odd, p, null) == -2
+
+
+@needs_lib
+def test_splitk_sizes():
+    lib = _lib.load()
+    pf, nc = ctypes.c_int64(), ctypes.c_int64()
+    # K = 4096: 16 super-blocks; ksplit 4 -> 4 splits of 4
+    assert lib.mmq_splitk_sizes(16, 4096, 4096, 4, ctypes.byref(pf), ctypes.byref(nc)) == 0
+    assert (pf.value, nc.value) == (4 * 16 * 4096, 32)
+    # K = 11008: 43 super-blocks; ksplit 4 -> 11 per split -> 4 splits
+    assert lib.mmq_splitk_sizes(200, 300, 11008, 4, ctypes.byref(pf), ctypes.byref(nc)) == 0
+    assert (pf.value, nc.value) == (4 * 200 * 300, 3 * 2)
+    # ksplit 5 on 16 super-blocks -> 4 per split -> 4 splits; ksplit 100 -> one per split
+    assert lib.mmq_splitk_sizes(1, 128, 4096, 5, ctypes.byref(pf), ctypes.byref(nc)) == 0
+    assert pf.value == 4 * 1 * 128
+    assert lib.mmq_splitk_sizes(1, 128, 4096, 100, ctypes.byref(pf), ctypes.byref(nc)) == 0
+    assert pf.value == 16 * 1 * 128
+    # no split: no partial workspace
+    assert lib.mmq_splitk_sizes(1, 128, 256, 4, ctypes.byref(pf), ctypes.byref(nc)) == 0
+    assert pf.value == 0
+    assert lib.mmq_splitk_sizes(1, 128, 4096, 0, ctypes.byref(pf), ctypes.byref(nc)) == -1
 
 
 @needs_lib

@@ -206,6 +206,40 @@ def test_gemm_full_size_sampled(ops, orc, cfg, T):
             assert torch.isfinite(y).all()
 
 
+@pytest.mark.parametrize("T,O,K,ksplit", [(16, 256, 1024, 4), (1, 129, 2816, 3), (130, 300, 1280, 2),
+                                          (64, 512, 4096, 16), (200, 128, 768, 7)])
+def test_gemm_splitk_small(ops, orc, T, O, K, ksplit):
+    w = synth.make_weights("q4_K", O, K, seed=3 * T + O)
+    x = synth.make_x(T, K, seed=K + T + 1, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q4_K", w, qs_r, ds_r, O)
+    _, ds, _, xa = _gpu_quant(ops, x)
+    ws = ops.SplitKWorkspace(xa.device, *ops.splitk_sizes(T, O, K, ksplit))
+    y1 = ops.gemm_splitk(_dev(w), xa, ds, O, ksplit=ksplit, workspace=ws)
+    y2 = ops.gemm_splitk(_dev(w), xa, ds, O, ksplit=ksplit, workspace=ws)
+    ops.check_status()
+    assert _rel_err(y1.cpu().numpy(), ref) <= TOL
+    assert torch.equal(y1, y2)                       # fixed summation order
+    assert int(ws.counters.abs().sum()) == 0         # counters left at zero
+
+
+@pytest.mark.parametrize("cfg,T", [(4, 16), (4, 64), (4, 256)])
+def test_gemm_splitk_full_size_sampled(ops, orc, cfg, T):
+    wl = synth.config(cfg, T)
+    rng = np.random.default_rng(cfg * 777 + T)
+    for g in wl.gemms:
+        x = g.x()
+        qs_r, ds_r = orc.quantize_q8_1(x)
+        _, ds, _, xa = _gpu_quant(ops, x)
+        w = g.weights()
+        y = ops.gemm_splitk(_dev(w), xa, ds, g.O)
+        ops.check_status()
+        ti, oi = _sample_points(rng, g.T, g.O)
+        ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
+        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
+        assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
+
+
 def test_gemm_repeatable(ops):
     g = synth.config(1).gemms[0]
     w = _dev(g.weights())
