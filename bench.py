@@ -50,6 +50,7 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-small-t", action="store_true", help="skip the small-T (split-K) side measurement")
     return ap.parse_args()
 
 
@@ -124,7 +125,7 @@ class ClockSampler:
 
 def traffic_bytes(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None if the kernel source changed since those counters were taken."""
+    None if the kernel's source region changed since those counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -135,10 +136,67 @@ def traffic_bytes(kernel: str):
     if not rec:
         return None
     src = os.path.join(ROOT, "quantized_prefill_gemm_mmq_gb300", "csrc", rec["source"])
-    with open(src, "rb") as fh:
-        if hashlib.sha256(fh.read()).hexdigest() != rec["source_sha256"]:
-            return None
+    with open(src, encoding="utf-8") as fh:
+        text = fh.read()
+    try:
+        a = text.index(rec["region_begin"])
+        b = text.index(rec["region_end"], a)
+    except ValueError:
+        return None
+    if hashlib.sha256(text[a:b].encode()).hexdigest() != rec["region_sha256"]:
+        return None
     return rec["dram_bytes_per_launch"]
+
+
+def graph_time_us(fn, n=20, reps=5):
+    """Device time per call of fn, replayed from a CUDA graph of n calls (best of reps)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(n):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e3 / n)
+    return best
+
+
+def small_t_lines(dev, hbm_gbs):
+    """Side measurement of the small-T tier (config 4 shapes at T = 16 and 64):
+    the one-CTA-per-tile GEMM against the split-K GEMM, device time per launch."""
+    import torch
+    from quantized_prefill_gemm_mmq_gb300 import ops, synth
+    out = []
+    for T in (16, 64):
+        for g in synth.config(4, T).gemms:
+            w = torch.from_numpy(g.weights()).to(dev)
+            x = torch.from_numpy(g.x()).to(dev)
+            _, ds, _, xa = ops.quantize_q8_1(x, want_qs=False, want_xh=False)
+            y = torch.empty((g.T, g.O), dtype=torch.float32, device=dev)
+            ks = ops.choose_ksplit(g.T, g.O, g.K)
+            ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
+            us_plain = graph_time_us(lambda: ops.gemm("q4_K", w, xa, ds, g.O, out=y))
+            us_split = graph_time_us(lambda: ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws, out=y))
+            nbytes = w.numel() + g.T * g.K * 4 + g.T * g.K // 8 + g.T * g.O * 4   # W + xa + ds + Y
+            out.append({"T": g.T, "K": g.K, "O": g.O, "ksplit": ks, "plain_us": us_plain, "splitk_us": us_split,
+                        "splitk_tmacs": g.macs / (us_split * 1e-6) / 1e12,
+                        "splitk_gbs": nbytes / (us_split * 1e-6) / 1e9,
+                        "splitk_hbm_frac": nbytes / (us_split * 1e-6) / 1e9 / hbm_gbs})
+    ops.check_status(dev)
+    return out
 
 
 def workload_desc(T, layers):
@@ -400,14 +458,15 @@ def mmq_arm(args):
     ms_step = elapsed_ms / args.steps
     value = step_macs * args.steps * world / (elapsed_ms * 1e-3) / 1e12
     achieved = 2.0 * sq_macs / (sq_ms * 1e-3) / 1e12 if sq_ms > 0 else None
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # the q4_K launches are timed inside a long step: the sustained bf16 figure applies
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
         "frac": achieved / peak if achieved else None,
         "traffic": traffic_bytes("mmq_q4K_sb_kernel"),
         "kernel": "mmq_q4K_sb_kernel (q4_K GEMM), launches of shape T=512 K=4096 O=4096",
         "algorithmic_bytes_per_launch": 4096 * 4096 * 9 // 16 + 512 * 4096 * 4 + 512 * 4096 // 8 + 512 * 4096 * 4,
-        "peak_source": f"{peak_src} bf16 dense burst; f16 runs at the bf16 rate",
+        "peak_source": f"{peak_src} bf16 dense, sustained (timed inside the step); f16 runs at the bf16 rate",
         "timing": kernel_timing,
         "avg_launch_us": 1e3 * sq_ms / max(1, n_sq),
         "all_q4K_launches_tflops": 2.0 * all_macs / (all_ms * 1e-3) / 1e12 if all_ms > 0 else None,
@@ -419,6 +478,13 @@ def mmq_arm(args):
         cpu = {"value": macs / secs / 1e12, "unit": "TMAC/s", "cores": 1, "kind": "oracle",
                "sample": f"q8_1 quantisation of the 4 layer inputs and the first {rows} output rows of each of the "
                          f"7 GEMMs of one layer ({macs} MACs, {secs:.1f} s, one thread)"}
+    small_t = None
+    if not args.no_small_t and world == 1:
+        small_t = {"kernel": "mmq_q4K_sb_kernel, one CTA per 128x128 tile vs split-K (mmq_gemm_q4K_splitk)",
+                   "timing": "CUDA-graph replay of 20 launches, device events, best of 5",
+                   "bytes": "weights + xa (4 B/elem) + ds + y",
+                   "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                   "lines": small_t_lines(dev, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))}
     line = {
         "metric": METRIC,
         "value": value,
@@ -450,6 +516,7 @@ def mmq_arm(args):
         "e2e": e2e,
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
+        "small_t": small_t,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

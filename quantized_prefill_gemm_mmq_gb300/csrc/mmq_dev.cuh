@@ -105,10 +105,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    for (;;) {
+    for (uint32_t polls = 1;; ++polls) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        // both the clock and a minimum number of polls must say so: a jump of
+        // the global timer alone never ends a wait
+        if (polls > 4096u && globaltimer() - t0 > kWaitLimitNs) {
             *abort = 1u;
             record_error(kStatusTimeout, kernel_id, site);
             return false;
