@@ -78,7 +78,8 @@ enum {
     MMQ_ERR_TIMEOUT = -5,   /* (mmq_check_status) a kernel pipeline wait timed out */
     MMQ_ERR_NULL = -6,      /* a required pointer is NULL                          */
     MMQ_ERR_DRIVER = -7,    /* the driver could not build a TMA tensor map         */
-    MMQ_ERR_CUDA = -8       /* (mmq_check_status) a CUDA error is pending          */
+    MMQ_ERR_CUDA = -8,      /* (mmq_check_status) a CUDA error is pending          */
+    MMQ_ERR_SCRATCH = -9    /* the call needs more than the library's static scratch */
 };
 
 /* Library ABI version; bumped on any signature or format change. */
@@ -139,6 +140,28 @@ int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *ds,
 int mmq_splitk_sizes(int T, int O, int K, int ksplit, int64_t *part_floats, int64_t *counters);
 int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint32_t *ds, float *y,
                         int T, int O, int K, int ksplit, float *part, int *counters, mmq_stream_t stream);
+
+/*
+ * mmq_gemm_q4K_splitk without caller scratch: this entry point allocates
+ * nothing.  The partial sums and tile counters live in the library's own
+ * statically allocated device arrays, 4 Mi f32 (16 MiB) of partial sums and
+ * 8192 tile counters per device.  (The pages have no counterpart: their
+ * kernel never splits K.)
+ *   - The scratch address is obtained once per device, with that device
+ *     current, on the first call for that device.  Make that first call
+ *     before any stream capture.
+ *   - Calls whose mmq_splitk_sizes exceed that scratch return
+ *     MMQ_ERR_SCRATCH and launch nothing.
+ *   - What must start at zero: the tile counters.  They are zero when the
+ *     library is loaded, and every call that launched leaves them at zero
+ *     when its kernel ends (a kernel that timed out included).
+ *   - The scratch is shared by every call on the device: calls that may
+ *     overlap in time (different streams, no ordering between them) race
+ *     and give wrong results.  Order them on one stream.
+ * Arguments, limits and result as mmq_gemm_q4K_splitk.
+ */
+int mmq_gemm_q4K_splitk_static(const void *w, const uint16_t *xa, const uint32_t *ds, float *y,
+                               int T, int O, int K, int ksplit, mmq_stream_t stream);
 
 /*
  * The same q4_K GEMM in the pages' per-sub-block form: the tensor core forms

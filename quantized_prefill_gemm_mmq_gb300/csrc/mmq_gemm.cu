@@ -1603,6 +1603,37 @@ extern "C" int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint
     return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, ksplit, part, counters, stream);
 }
 
+// Scratch of mmq_gemm_q4K_splitk_static: partial sums and tile counters in
+// the library's own device memory (zero-initialised at module load; every
+// completed launch leaves the counters at zero).
+constexpr int64_t kStaticPartFloats = (int64_t)1 << 22;   // 16 MiB of f32 partial sums
+constexpr int64_t kStaticCounters = 8192;                 // output tiles
+static __device__ __align__(256) float g_splitk_part[kStaticPartFloats];
+static __device__ __align__(256) int g_splitk_cnt[kStaticCounters];
+
+extern "C" int mmq_gemm_q4K_splitk_static(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T,
+                                          int O, int K, int ksplit, mmq_stream_t stream)
+{
+    if (T == 0) return mmq_gemm_q4K_splitk(w, xa, ds, y, T, O, K, 1, nullptr, nullptr, stream);
+    int64_t part_floats = 0, tiles = 0;
+    const int rc = mmq_splitk_sizes(T, O, K, ksplit, &part_floats, &tiles);
+    if (rc != MMQ_OK) return rc;
+    if (part_floats > kStaticPartFloats || tiles > kStaticCounters) return MMQ_ERR_SCRATCH;
+    static float *part[64];
+    static int *cnt[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (!part[dev] || !cnt[dev]) {
+        void *a = nullptr, *b = nullptr;
+        if (cudaGetSymbolAddress(&a, g_splitk_part) != cudaSuccess ||
+            cudaGetSymbolAddress(&b, g_splitk_cnt) != cudaSuccess)
+            return mmq::launch_status();
+        part[dev] = static_cast<float *>(a);
+        cnt[dev] = static_cast<int *>(b);
+    }
+    return mmq_gemm_q4K_splitk(w, xa, ds, y, T, O, K, ksplit, part[dev], cnt[dev], stream);
+}
+
 extern "C" int mmq_gemm_q4K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O,
                                      int K, mmq_stream_t stream)
 {

@@ -103,6 +103,7 @@ extern "C" const char *mmq_status_str(int status)
     case MMQ_ERR_NULL: return "required pointer is NULL";
     case MMQ_ERR_DRIVER: return "driver could not encode a TMA tensor map";
     case MMQ_ERR_CUDA: return "CUDA error pending on the stream";
+    case MMQ_ERR_SCRATCH: return "split-K scratch needed exceeds the library's static scratch (4 Mi f32 partial sums, 8192 tiles)";
     default: return "unknown status";
     }
 }

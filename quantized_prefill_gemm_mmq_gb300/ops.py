@@ -163,6 +163,22 @@ def gemm_splitk(w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int, ksp
     return out
 
 
+def gemm_splitk_static(w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int, ksplit: int | None = None,
+                       out: torch.Tensor | None = None) -> torch.Tensor:
+    """gemm_splitk with the library's static scratch (no workspace anywhere);
+    calls on one device must not overlap in time."""
+    T, K = _check_gemm_args("q4_K", w, xa, O, planes=2)
+    _check_ds(ds, T, K)
+    out = _out(out, T, O, xa.device)
+    if ksplit is None:
+        ksplit = choose_ksplit(T, O, K)
+    with torch.cuda.device(xa.device):
+        st = load().mmq_gemm_q4K_splitk_static(_ptr(w), _ptr(xa), _ptr(ds), _ptr(out), T, O, K, ksplit,
+                                               _stream(xa.device))
+    _check("mmq_gemm_q4K_splitk_static", st)
+    return out
+
+
 def gemm_subblock(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
                   out: torch.Tensor | None = None) -> torch.Tensor:
     """Per-sub-block GEMM (exact integer sub-block dots + f32 fold) from the xh/ds planes."""

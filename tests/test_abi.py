@@ -18,7 +18,7 @@ def test_header_declares_the_boundary():
     names = _lib.header_functions()
     for required in ("mmq_quantize_q8_1", "mmq_gemm_q4K", "mmq_gemm_q4K_subblock", "mmq_gemm_q6K", "mmq_check_status",
                      "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K",
-                     "mmq_gemm_q4K_splitk", "mmq_splitk_sizes"):
+                     "mmq_gemm_q4K_splitk", "mmq_splitk_sizes", "mmq_gemm_q4K_splitk_static"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -37,7 +37,7 @@ def test_library_loads_and_reports():
     lib = _lib.load()
     assert lib.mmq_version() == 3
     assert lib.mmq_status_str(0) == b"ok"
-    for code in range(-8, 0):
+    for code in range(-9, 0):
         assert lib.mmq_status_str(code) not in (b"", b"unknown status")
 
 
@@ -68,6 +68,9 @@ def test_argument_errors_without_gpu():
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, p, null, null) == -6
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 0, p, p, null) == -1
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, odd, p, null) == -2
+    # static-scratch variant: oversize requests are refused before anything else
+    assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 4096, 4096, 4096, 4, null) == -9
+    assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 16, 256, 1024, 0, null) == -1
 
 
 @needs_lib
