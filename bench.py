@@ -123,10 +123,25 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
+def kernel_source_digest(rec):
+    """sha256 over the kernel's source region and the headers it is built from."""
+    import hashlib
+    csrc = os.path.join(ROOT, "quantized_prefill_gemm_mmq_gb300", "csrc")
+    h = hashlib.sha256()
+    with open(os.path.join(csrc, rec["source"]), encoding="utf-8") as fh:
+        text = fh.read()
+    a = text.index(rec["region_begin"])
+    b = text.index(rec["region_end"], a)
+    h.update(text[a:b].encode())
+    for name in rec.get("headers", []):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def traffic_bytes(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None if the kernel's source region changed since those counters were taken."""
-    import hashlib
+    None if the kernel's source changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
@@ -135,15 +150,10 @@ def traffic_bytes(kernel: str):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, "quantized_prefill_gemm_mmq_gb300", "csrc", rec["source"])
-    with open(src, encoding="utf-8") as fh:
-        text = fh.read()
     try:
-        a = text.index(rec["region_begin"])
-        b = text.index(rec["region_end"], a)
-    except ValueError:
-        return None
-    if hashlib.sha256(text[a:b].encode()).hexdigest() != rec["region_sha256"]:
+        if kernel_source_digest(rec) != rec["sha256"]:
+            return None
+    except (OSError, ValueError, KeyError):
         return None
     return rec["dram_bytes_per_launch"]
 
