@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small-t", action="store_true", help="skip the small-T (split-K) side measurement")
+    ap.add_argument("--small-t-launches", type=int, default=0, metavar="T",
+                    help="only launch the split-K GEMM of the config-4 shapes at T tokens three times each "
+                         "(eager; for profiling) and exit")
     return ap.parse_args()
 
 
@@ -275,11 +278,31 @@ def reference_arm(args):
 
 # ------------------------------------------------------------- GPU arm ---
 
+def small_t_launches(T):
+    """Three eager launches of the split-K GEMM per config-4 shape at T tokens."""
+    import torch
+    from quantized_prefill_gemm_mmq_gb300 import ops, synth
+    dev = torch.device("cuda", 0)
+    for g in synth.config(4, T).gemms:
+        w = torch.from_numpy(g.weights()).to(dev)
+        _, ds, _, xa = ops.quantize_q8_1(torch.from_numpy(g.x()).to(dev), want_qs=False, want_xh=False)
+        ks = ops.choose_ksplit(g.T, g.O, g.K)
+        ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
+        for _ in range(3):
+            ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws)
+    ops.check_status(dev)
+    print(json.dumps({"small_t_launches": T, "status": "ok"}))
+
+
 def mmq_arm(args):
     import torch
     import torch.distributed as dist
 
     from quantized_prefill_gemm_mmq_gb300 import ops
+
+    if args.small_t_launches:
+        small_t_launches(args.small_t_launches)
+        return
 
     rank, world, local = dist_env()
     if world > 1:
@@ -292,14 +315,12 @@ def mmq_arm(args):
     w_layer = {n: torch.from_numpy(w).to(dev) for n, w in host_w.items()}
     layers = [w_layer] + [{n: t.clone() for n, t in w_layer.items()} for _ in range(args.layers - 1)]
     x_dev = {s: torch.from_numpy(x).to(dev) for s, x in xs.items()}
-    # q8_1 planes per input: the q4_K GEMM reads xa (exact hi/lo dequantised
-    # values), the q6_K GEMM reads xh (integer values); each input gets only
-    # the planes its consumers need
-    fmts_of = {s: {g.fmt for g in wl.gemms if g.x_seed == s} for s in xs}
+    # q8_1 planes per input: both production GEMMs read xa (the exact hi/lo
+    # dequantised values) and ds
     qbuf = {s: (None,
                 torch.empty((x.shape[0], x.shape[1] // 32), dtype=torch.int32, device=dev),
-                torch.empty(x.shape, dtype=torch.float16, device=dev) if "q6_K" in fmts_of[s] else None,
-                torch.empty((2,) + x.shape, dtype=torch.float16, device=dev) if "q4_K" in fmts_of[s] else None)
+                None,
+                torch.empty((2,) + x.shape, dtype=torch.float16, device=dev))
             for s, x in xs.items()}
     ybuf = {g.name: torch.empty((g.T, g.O), dtype=torch.float32, device=dev) for g in wl.gemms}
     layer_macs = wl.macs
@@ -309,11 +330,8 @@ def mmq_arm(args):
     ext_events = None   # per-launch events of the q4_K GEMMs, recorded inside the graph
 
     def run_gemm(g, lw):
-        _, ds, xh, xa = qbuf[g.x_seed]
-        if g.fmt == "q4_K":
-            ops.gemm(g.fmt, lw[g.name], xa, ds, g.O, out=ybuf[g.name])
-        else:
-            ops.gemm_subblock(g.fmt, lw[g.name], xh, ds, g.O, out=ybuf[g.name])
+        _, ds, _, xa = qbuf[g.x_seed]
+        ops.gemm(g.fmt, lw[g.name], xa, ds, g.O, out=ybuf[g.name])
 
     def step(record=None):
         for li, lw in enumerate(layers):

@@ -174,14 +174,32 @@ int mmq_gemm_q4K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds,
                           float *y, int T, int O, int K, mmq_stream_t stream);
 
 /*
- * q6_K x q8_1 GEMM ("43 . r40", 5: 16-weight sub-blocks, two k16 halves
- * per 32-block):  y[t][o] = sum over 16-weight halves u of
- * dx_(u/2)*(d*sc_u)*C16_u,  C16_u the exact integer dot of (q-32) with the
- * int8 activations.  w: O*(K/256)*210 bytes; xh, ds and the other
- * arguments as for mmq_gemm_q4K_subblock.
+ * q6_K x q8_1 GEMM ("43 . r40", 5: w = d*sc_u*(q-32) on 16-weight
+ * sub-blocks u):  y[t][o] = sum_k dequant(W)[o][k]*dequant(X)[t][k], i.e.
+ * the pages' per-16 fold sum_u dx_(u/2)*(d*sc_u)*C16_u with C16_u the exact
+ * integer dot of (q-32) with the int8 activations; accumulation in f32
+ * (rounding order unspecified).
+ * Production form: the tensor core accumulates each 256-weight super-block
+ * from the exact activation planes xa (hi + lo) and the weight values
+ * sc*(q-32) as exact f16 hi + lo planes (three MMAs per 16-k step; the
+ * dropped lo*lo product is below 2^-22 of each product); d is applied per
+ * super-block.
+ * w: O*(K/256)*210 bytes.  xa: as written by mmq_quantize_q8_1.  ds: not
+ * read (q6_K has no min term; may be NULL).  y: f32 [T][O], overwritten.
+ * T >= 0, O >= 1, 256 <= K <= 2^20, K % 256 == 0.
  */
-int mmq_gemm_q6K(const void *w, const uint16_t *xh, const uint32_t *ds,
+int mmq_gemm_q6K(const void *w, const uint16_t *xa, const uint32_t *ds,
                  float *y, int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * The same q6_K GEMM in the pages' per-sub-block form: the tensor core forms
+ * every 16-weight half's exact integer dot C16_u = sum (q-32)*a (operand xh,
+ * the int8 values as f16) in its own TMEM accumulator and the f32 fold
+ * dx*(d*sc_u)*C16_u runs per 16-weight half.  Same limits and result (up to
+ * f32 summation order) as mmq_gemm_q6K.
+ */
+int mmq_gemm_q6K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds,
+                          float *y, int T, int O, int K, mmq_stream_t stream);
 
 /*
  * Diagnostic: the per-sub-block exact integer dots the GEMMs fold, through

@@ -278,6 +278,18 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t addr)
            | ((uint64_t)2 << 61);                   // layout: 128-byte swizzle
 }
 
+// As sdesc_k_sw128 for the 64-byte swizzle layout: rows of 64 bytes (32 f16),
+// 8-row groups 512 bytes apart, group base 512-byte aligned; `addr` may be
+// offset by 32 bytes inside a row group for the second 16-value K slice.
+__device__ __forceinline__ uint64_t sdesc_k_sw64(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4)      // start address >> 4
+           | ((uint64_t)1 << 16)                    // leading byte offset (unused for swizzled K-major)
+           | ((uint64_t)(512 >> 4) << 32)           // stride byte offset: 8 rows x 64 B
+           | ((uint64_t)1 << 46)                    // descriptor version (tcgen05)
+           | ((uint64_t)4 << 61);                   // layout: 64-byte swizzle
+}
+
 // 32 TMEM lanes x 32 consecutive 32-bit columns: register i of lane l holds
 // column (taddr.col + i) of lane (taddr.lane + l).  Values are valid only
 // after tmem_ld_wait() on the same registers.

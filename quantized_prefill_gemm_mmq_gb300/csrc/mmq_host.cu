@@ -89,7 +89,7 @@ int make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, 
 
 }  // namespace mmq
 
-extern "C" int mmq_version(void) { return 3; }
+extern "C" int mmq_version(void) { return 4; }
 
 extern "C" const char *mmq_status_str(int status)
 {

@@ -101,19 +101,15 @@ def _check_ds(ds, T, K):
 
 def gemm(fmt: str, w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int,
          out: torch.Tensor | None = None) -> torch.Tensor:
-    """Production GEMM: Y [T][O] f32 from W (`fmt`) and the xa/ds activation planes.
-
-    q6_K is served by its per-sub-block kernel, which reads the integer plane;
-    pass that as `xh=` through gemm_subblock, or call mmq_forward.
-    """
-    if fmt == "q6_K":
-        raise ValueError("q6_K takes the integer operand: use gemm_subblock('q6_K', w, xh, ds, O)")
+    """Production GEMM: Y [T][O] f32 from W (`fmt`) and the xa/ds activation planes
+    (q6_K does not read ds)."""
     T, K = _check_gemm_args(fmt, w, xa, O, planes=2)
     _check_ds(ds, T, K)
     out = _out(out, T, O, xa.device)
+    fn = load().mmq_gemm_q4K if fmt == "q4_K" else load().mmq_gemm_q6K
     with torch.cuda.device(xa.device):
-        st = load().mmq_gemm_q4K(_ptr(w), _ptr(xa), _ptr(ds), _ptr(out), T, O, K, _stream(xa.device))
-    _check("mmq_gemm_q4K", st)
+        st = fn(_ptr(w), _ptr(xa), _ptr(ds), _ptr(out), T, O, K, _stream(xa.device))
+    _check(f"gemm({fmt})", st)
     return out
 
 
@@ -185,7 +181,7 @@ def gemm_subblock(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor,
     T, K = _check_gemm_args(fmt, w, xh, O, planes=1)
     _check_ds(ds, T, K)
     out = _out(out, T, O, xh.device)
-    fn = load().mmq_gemm_q4K_subblock if fmt == "q4_K" else load().mmq_gemm_q6K
+    fn = load().mmq_gemm_q4K_subblock if fmt == "q4_K" else load().mmq_gemm_q6K_subblock
     with torch.cuda.device(xh.device):
         st = fn(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
     _check(f"gemm_subblock({fmt})", st)
@@ -225,9 +221,6 @@ def tensor_peak_tmacs(kind: str = "int8", device: torch.device | None = None) ->
 
 
 def mmq_forward(fmt: str, w: torch.Tensor, x: torch.Tensor, O: int) -> torch.Tensor:
-    """Quantise x [T][K] to q8_1 and run the GEMM: the whole hot path."""
-    if fmt == "q4_K":
-        _, ds, _, xa = quantize_q8_1(x, want_qs=False, want_xh=False, want_xa=True)
-        return gemm(fmt, w, xa, ds, O)
-    _, ds, xh, _ = quantize_q8_1(x, want_qs=False, want_xh=True, want_xa=False)
-    return gemm_subblock(fmt, w, xh, ds, O)
+    """Quantise x [T][K] to q8_1 and run the production GEMM: the whole hot path."""
+    _, ds, _, xa = quantize_q8_1(x, want_qs=False, want_xh=False, want_xa=True)
+    return gemm(fmt, w, xa, ds, O)

@@ -123,7 +123,7 @@ def test_subdots_extremes(ops, orc):
 
 def _run_gemm(ops, fmt, w, x, O, kernel="production"):
     qs, ds, xh, xa = _gpu_quant(ops, x)
-    if kernel == "production" and fmt == "q4_K":
+    if kernel == "production":
         y = ops.gemm(fmt, _dev(w), xa, ds, O)
     else:
         y = ops.gemm_subblock(fmt, _dev(w), xh, ds, O)
@@ -131,7 +131,7 @@ def _run_gemm(ops, fmt, w, x, O, kernel="production"):
     return y.cpu().numpy()
 
 
-KERNELS = [("q4_K", "production"), ("q4_K", "subblock"), ("q6_K", "subblock")]
+KERNELS = [("q4_K", "production"), ("q4_K", "subblock"), ("q6_K", "production"), ("q6_K", "subblock")]
 
 
 @pytest.mark.parametrize("fmt,kernel", KERNELS)
@@ -193,8 +193,7 @@ def test_gemm_full_size_sampled(ops, orc, cfg, T):
         assert np.array_equal(_to_np_ds(ds), ds_r)
         wd = _dev(w)
         outs = []
-        if g.fmt == "q4_K":
-            outs.append(("production", ops.gemm(g.fmt, wd, xa, ds, g.O)))
+        outs.append(("production", ops.gemm(g.fmt, wd, xa, ds, g.O)))
         if g.fmt == "q6_K" or cfg in (1, 2):
             outs.append(("subblock", ops.gemm_subblock(g.fmt, wd, xh, ds, g.O)))
         ops.check_status()
@@ -240,16 +239,38 @@ def test_gemm_splitk_full_size_sampled(ops, orc, cfg, T):
         assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
 
 
+@pytest.mark.parametrize("kernel", ["production", "subblock"])
+@pytest.mark.parametrize("T,O,K", [(64, 256, 512), (130, 300, 768), (512, 128, 4096)])
+def test_gemm_q6K_full_range_scales(ops, orc, kernel, T, O, K):
+    # int8 sub-block scales over the whole -128..127 range (as real q6_K data
+    # has), so that sc*(q-32) reaches +-4096 and needs the weight lo plane
+    w = synth.make_weights("q6_K", O, K, seed=11 * T + O).reshape(O, K // 256, 210).copy()
+    rng = np.random.default_rng(T + O + K)
+    w[:, :, 192:208] = rng.integers(-128, 128, size=(O, K // 256, 16), dtype=np.int64).astype(np.int8).view(np.uint8)
+    w[:, 0, 192] = np.uint8(0x80)                 # -128 in every row
+    w = w.reshape(-1)
+    x = synth.make_x(T, K, seed=K - T, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q6_K", w, qs_r, ds_r, O)
+    y = _run_gemm(ops, "q6_K", w, x, O, kernel)
+    assert _rel_err(y, ref) <= TOL
+
+
 def test_gemm_repeatable(ops):
     g = synth.config(1).gemms[0]
     w = _dev(g.weights())
     _, ds, xh, xa = ops.quantize_q8_1(_dev(g.x()))
     y1 = ops.gemm(g.fmt, w, xa, ds, g.O)
     y2 = ops.gemm(g.fmt, w, xa, ds, g.O)
+    g6 = synth.config(3).gemms[0]
+    w6 = _dev(g6.weights())
+    _, ds6, _, xa6 = ops.quantize_q8_1(_dev(g6.x()))
+    v1 = ops.gemm(g6.fmt, w6, xa6, ds6, g6.O)
+    v2 = ops.gemm(g6.fmt, w6, xa6, ds6, g6.O)
     z1 = ops.gemm_subblock(g.fmt, w, xh, ds, g.O)
     z2 = ops.gemm_subblock(g.fmt, w, xh, ds, g.O)
     ops.check_status()
-    assert torch.equal(y1, y2) and torch.equal(z1, z2)
+    assert torch.equal(y1, y2) and torch.equal(z1, z2) and torch.equal(v1, v2)
 
 
 def test_gpu_argument_errors(ops):
