@@ -142,6 +142,19 @@ int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint32_t *ds, f
                         int T, int O, int K, int ksplit, float *part, int *counters, mmq_stream_t stream);
 
 /*
+ * q4_K GEMM for few tokens (1 <= T <= 16), where the GEMM is bound by
+ * streaming W from HBM: the pages' per-sub-block form ("31 . r28", 2.3) on
+ * the int8 warp MMA (mma.sync m16n8k32 s8: one instruction per 32-weight
+ * sub-block, the nibbles used as int8 operands), the exact integer dots C_b
+ * folded in f32 per sub-block.  qs: the int8 q8_1 values [T][K] and ds the
+ * scale words, both as written by mmq_quantize_q8_1.  Result as
+ * mmq_gemm_q4K up to f32 summation order; deterministic.
+ * T <= 16 (MMQ_ERR_SHAPE above), other limits as mmq_gemm_q4K.
+ */
+int mmq_gemm_q4K_small(const void *w, const int8_t *qs, const uint32_t *ds, float *y,
+                       int T, int O, int K, mmq_stream_t stream);
+
+/*
  * mmq_gemm_q4K_splitk without caller scratch: this entry point allocates
  * nothing.  The partial sums and tile counters live in the library's own
  * statically allocated device arrays, 4 Mi f32 (16 MiB) of partial sums and

@@ -1965,6 +1965,230 @@ int launch_q6K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     return launch_status();
 }
 
+// =========================================================================
+// Small-T q4_K GEMM (T <= 16): the pages' per-sub-block form on the int8
+// warp MMA.
+//
+// With few tokens the GEMM is bound by streaming the weights from HBM, and
+// the cost that matters is how many instructions turn a weight byte into a
+// tensor-core operand.  mma.sync m16n8k32 (s8 x s8 -> s32) takes exactly one
+// q4_K sub-block (32 k) per instruction, the unsigned nibbles are int8
+// operands after one AND per four weights, and the int8 activations qs are
+// used as they are.  Every MMA gives the exact integer dots C_b of one
+// sub-block for 16 tokens x 8 weight rows; the f32 fold
+//     y += dx_b*(d*sc_b)*C_b + (dx_b*ssum_b)*(-(dmin*m_b))
+// follows per sub-block ("31 . r28", 2.3).
+// CTA = 8 warps on the same 16 weight rows (two MMAs per activation
+// fragment); warp w takes the w-th eighth of the super-blocks, and the eight
+// partial sums are added in warp order through shared memory
+// (deterministic).  Each warp stages the next super-block's activation rows
+// and scale words in shared memory with cp.async and loads the weights from
+// global memory one super-block ahead.
+// =========================================================================
+namespace smt {
+
+constexpr int NWARPS = 8;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int ROWS = 16;         // weight rows per CTA: two MMA N tiles
+constexpr int MAXT = 16;         // tokens: one MMA M tile
+constexpr int A_ROW = 256 + 16;  // staged activation row (bytes): 256 k + pad (conflict-free fragment reads)
+constexpr int D_ROW = 48;        // staged scale-word row: 8 words + pad
+constexpr int BUF = MAXT * A_ROW + MAXT * D_ROW;   // one super-block of one warp
+static_assert(BUF % 16 == 0, "cp.async destinations are 16-byte aligned");
+
+__device__ __forceinline__ void mma_s8(int (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 16-byte asynchronous copy; with src_bytes = 0 nothing is read and the
+// destination is zero-filled
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+}  // namespace smt
+
+__global__ void __launch_bounds__(smt::NTHREADS, 2)
+    mmq_q4K_small_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ qs, const uint32_t *__restrict__ ds,
+                         float *__restrict__ y, int T, int O, int K)
+{
+    using namespace smt;
+    extern __shared__ __align__(16) uint8_t sm[];
+    float *part = reinterpret_cast<float *>(sm + NWARPS * 2 * BUF);   // [NWARPS][MAXT][ROWS]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;   // MMA group and thread in group
+    const int o0 = blockIdx.x * ROWS;
+    const int nsb = K / 256;
+    const int per = (nsb + NWARPS - 1) / NWARPS;
+    const int sb0 = min(nsb, warp * per), sb1 = min(nsb, sb0 + per);
+    uint8_t *wbuf = sm + warp * 2 * BUF;
+    const uint32_t wbuf_s = smem_u32(wbuf);
+
+    // B rows of this thread: o0 + g (tile 0) and o0 + 8 + g (tile 1); C columns:
+    // rows o0 + 8 n + 2 tig + {0, 1} of tile n
+    const uint8_t *wb[2], *wc[2][2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        wb[n] = w + (size_t)min(o0 + 8 * n + g, O - 1) * nsb * 144;
+        wc[n][0] = w + (size_t)min(o0 + 8 * n + 2 * tig, O - 1) * nsb * 144;
+        wc[n][1] = w + (size_t)min(o0 + 8 * n + 2 * tig + 1, O - 1) * nsb * 144;
+    }
+    // stage super-block sb's activations (16 rows x 256 B) and scale words (16 x 32 B) into buffer b
+    auto stage = [&](int sb, int b) {
+        const uint32_t base = wbuf_s + b * BUF;
+// token rows >= T are zero-filled (their outputs are never stored)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = lane + 32 * i, row = c >> 4, ch = c & 15;
+            const int t = min(row, T - 1);
+            cp_async16(base + row * A_ROW + ch * 16, qs + (size_t)t * K + sb * 256 + ch * 16, row < T ? 16u : 0u);
+        }
+        {
+            const int row = lane >> 1, ch = lane & 1;
+            const int t = min(row, T - 1);
+            cp_async16(base + MAXT * A_ROW + row * D_ROW + ch * 16, ds + (size_t)t * (K / 32) + sb * 8 + ch * 4,
+                       row < T ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    uint4 nq[2][2], nh[2][2];
+    auto load_w = [&](int sb) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const uint8_t *b = wb[n] + (size_t)sb * 144 + 16;
+            nq[n][0] = make_uint4(__ldg(reinterpret_cast<const uint32_t *>(b + 4 * tig)),
+                                  __ldg(reinterpret_cast<const uint32_t *>(b + 16 + 4 * tig)),
+                                  __ldg(reinterpret_cast<const uint32_t *>(b + 32 + 4 * tig)),
+                                  __ldg(reinterpret_cast<const uint32_t *>(b + 48 + 4 * tig)));
+            nq[n][1] = make_uint4(__ldg(reinterpret_cast<const uint32_t *>(b + 64 + 4 * tig)),
+                                  __ldg(reinterpret_cast<const uint32_t *>(b + 80 + 4 * tig)),
+                                  __ldg(reinterpret_cast<const uint32_t *>(b + 96 + 4 * tig)),
+                                  __ldg(reinterpret_cast<const uint32_t *>(b + 112 + 4 * tig)));
+            nh[n][0] = __ldg(reinterpret_cast<const uint4 *>(wc[n][0] + (size_t)sb * 144));
+            nh[n][1] = __ldg(reinterpret_cast<const uint4 *>(wc[n][1] + (size_t)sb * 144));
+        }
+    };
+    float acc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[n][i] = 0.0f;
+    if (sb0 < sb1) {
+        stage(sb0, 0);
+        load_w(sb0);
+    }
+    for (int sb = sb0; sb < sb1; ++sb) {
+        const int b = (sb - sb0) & 1;
+        uint4 q[2][2], h[2][2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                q[n][e] = nq[n][e];
+                h[n][e] = nh[n][e];
+            }
+        if (sb + 1 < sb1) {
+            stage(sb + 1, b ^ 1);
+            load_w(sb + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncwarp();
+        const uint8_t *abuf = wbuf + b * BUF;
+        const uint32_t *dbuf = reinterpret_cast<const uint32_t *>(abuf + MAXT * A_ROW);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t a[4];
+            a[0] = *reinterpret_cast<const uint32_t *>(abuf + g * A_ROW + 32 * j + 4 * tig);
+            a[1] = *reinterpret_cast<const uint32_t *>(abuf + (g + 8) * A_ROW + 32 * j + 4 * tig);
+            a[2] = *reinterpret_cast<const uint32_t *>(abuf + g * A_ROW + 32 * j + 16 + 4 * tig);
+            a[3] = *reinterpret_cast<const uint32_t *>(abuf + (g + 8) * A_ROW + 32 * j + 16 + 4 * tig);
+            const uint32_t da = dbuf[g * (D_ROW / 4) + j], db = dbuf[(g + 8) * (D_ROW / 4) + j];
+            const float dxa = __half2float(__ushort_as_half((unsigned short)(da & 0xFFFFu)));
+            const float dxb = __half2float(__ushort_as_half((unsigned short)(db & 0xFFFFu)));
+            const float sma = dxa * (float)(int)(int16_t)(da >> 16), smb = dxb * (float)(int)(int16_t)(db >> 16);
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                // sub-block j: low (j even) or high (j odd) nibbles of bytes 32 (j/2) ..
+                const uint32_t wl = (j & 2) ? (j & 4 ? q[n][1].z : q[n][0].z) : (j & 4 ? q[n][1].x : q[n][0].x);
+                const uint32_t wh = (j & 2) ? (j & 4 ? q[n][1].w : q[n][0].w) : (j & 4 ? q[n][1].y : q[n][0].y);
+                const uint32_t b0 = ((j & 1) ? (wl >> 4) : wl) & 0x0F0F0F0Fu;
+                const uint32_t b1 = ((j & 1) ? (wh >> 4) : wh) & 0x0F0F0F0Fu;
+                int c[4] = {0, 0, 0, 0};
+                mma_s8(c, a, b0, b1);
+                int sc0, m0, sc1, m1;
+                q4::q4K_scale_min(h[n][0].y, h[n][0].z, h[n][0].w, j, sc0, m0);
+                q4::q4K_scale_min(h[n][1].y, h[n][1].z, h[n][1].w, j, sc1, m1);
+                const float d0 = __half2float(__ushort_as_half((unsigned short)(h[n][0].x & 0xFFFFu)));
+                const float d1 = __half2float(__ushort_as_half((unsigned short)(h[n][1].x & 0xFFFFu)));
+                const float dm0 = __half2float(__ushort_as_half((unsigned short)(h[n][0].x >> 16)));
+                const float dm1 = __half2float(__ushort_as_half((unsigned short)(h[n][1].x >> 16)));
+                const float dsv0 = d0 * (float)sc0, dsv1 = d1 * (float)sc1;
+                const float dmv0 = -(dm0 * (float)m0), dmv1 = -(dm1 * (float)m1);
+                // c0, c1: token g, rows 2 tig, 2 tig + 1 of tile n; c2, c3: token g + 8
+                acc[n][0] += (dxa * dsv0) * (float)c[0] + sma * dmv0;
+                acc[n][1] += (dxa * dsv1) * (float)c[1] + sma * dmv1;
+                acc[n][2] += (dxb * dsv0) * (float)c[2] + smb * dmv0;
+                acc[n][3] += (dxb * dsv1) * (float)c[3] + smb * dmv1;
+            }
+        }
+        __syncwarp();   // the buffer is restaged two super-blocks later
+    }
+    // partial sums of this warp's super-blocks -> shared memory; warp order fixed
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        part[(warp * MAXT + g) * ROWS + 8 * n + 2 * tig] = acc[n][0];
+        part[(warp * MAXT + g) * ROWS + 8 * n + 2 * tig + 1] = acc[n][1];
+        part[(warp * MAXT + g + 8) * ROWS + 8 * n + 2 * tig] = acc[n][2];
+        part[(warp * MAXT + g + 8) * ROWS + 8 * n + 2 * tig + 1] = acc[n][3];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < MAXT * ROWS; i += NTHREADS) {
+        const int t = i / ROWS, n = i % ROWS;
+        if (t < T && o0 + n < O) {
+            float s = 0.0f;
+#pragma unroll
+            for (int v = 0; v < NWARPS; ++v) s += part[(v * MAXT + t) * ROWS + n];
+            y[(size_t)t * O + o0 + n] = s;
+        }
+    }
+}
+
+int launch_q4K_small(const void *w, const int8_t *qs, const uint32_t *ds, float *y, int T, int O, int K,
+                     mmq_stream_t stream)
+{
+    if (T < 0 || T > smt::MAXT || O < 1 || K < 256 || K > (1 << 20) || (K & 255)) return MMQ_ERR_SHAPE;
+    if (T == 0) return MMQ_OK;
+    if (!w || !qs || !ds || !y) return MMQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(qs) || !aligned16(ds) || !aligned16(y)) return MMQ_ERR_ALIGN;
+    int rc = check_arch();
+    if (rc != MMQ_OK) return rc;
+    constexpr int kSmem = smt::NWARPS * 2 * smt::BUF + smt::NWARPS * smt::MAXT * smt::ROWS * 4;
+    static bool attr_done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(mmq_q4K_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+            cudaSuccess)
+            return launch_status();
+        attr_done[dev] = true;
+    }
+    const dim3 grid((unsigned)((O + smt::ROWS - 1) / smt::ROWS));
+    mmq_q4K_small_kernel<<<grid, smt::NTHREADS, kSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(w), qs, ds, y, T, O, K);
+    return launch_status();
+}
+
 template <int FMT, int MODE>
 int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int32_t *sub, int T, int O, int K,
            mmq_stream_t stream)
@@ -2027,6 +2251,12 @@ extern "C" int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *d
                             mmq_stream_t stream)
 {
     return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, 1, nullptr, nullptr, stream);
+}
+
+extern "C" int mmq_gemm_q4K_small(const void *w, const int8_t *qs, const uint32_t *ds, float *y, int T, int O, int K,
+                                  mmq_stream_t stream)
+{
+    return mmq::launch_q4K_small(w, qs, ds, y, T, O, K, stream);
 }
 
 extern "C" int mmq_splitk_sizes(int T, int O, int K, int ksplit, int64_t *part_floats, int64_t *counters)

@@ -113,6 +113,26 @@ def gemm(fmt: str, w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int,
     return out
 
 
+SMALL_T_MAX = 16
+
+
+def gemm_small(w: torch.Tensor, qs: torch.Tensor, ds: torch.Tensor, O: int,
+               out: torch.Tensor | None = None) -> torch.Tensor:
+    """q4_K GEMM for T <= 16 tokens from the int8 q8_1 values qs [T][K] and ds."""
+    _need_cuda(w, qs)
+    if qs.dtype != torch.int8 or qs.dim() != 2 or not qs.is_contiguous():
+        raise ValueError("qs must be contiguous int8 [T][K]")
+    T, K = qs.shape
+    if w.dtype != torch.uint8 or not w.is_contiguous() or w.numel() != O * (K // 256) * BLOCK_BYTES["q4_K"]:
+        raise ValueError("w must be contiguous uint8 holding O*(K/256) q4_K super-blocks")
+    _check_ds(ds, T, K)
+    out = _out(out, T, O, qs.device)
+    with torch.cuda.device(qs.device):
+        st = load().mmq_gemm_q4K_small(_ptr(w), _ptr(qs), _ptr(ds), _ptr(out), T, O, K, _stream(qs.device))
+    _check("mmq_gemm_q4K_small", st)
+    return out
+
+
 def splitk_sizes(T: int, O: int, K: int, ksplit: int) -> tuple[int, int]:
     """(floats of partial-sum workspace, ints of tile counters) for a split-K q4_K GEMM."""
     pf, nc = ctypes.c_int64(0), ctypes.c_int64(0)
