@@ -142,17 +142,33 @@ int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint32_t *ds, f
                         int T, int O, int K, int ksplit, float *part, int *counters, mmq_stream_t stream);
 
 /*
- * q4_K GEMM for few tokens (1 <= T <= 16), where the GEMM is bound by
- * streaming W from HBM: the pages' per-sub-block form ("31 . r28", 2.3) on
- * the int8 warp MMA (mma.sync m16n8k32 s8: one instruction per 32-weight
- * sub-block, the nibbles used as int8 operands), the exact integer dots C_b
- * folded in f32 per sub-block.  qs: the int8 q8_1 values [T][K] and ds the
- * scale words, both as written by mmq_quantize_q8_1.  Result as
- * mmq_gemm_q4K up to f32 summation order; deterministic.
+ * q4_K GEMM for few tokens (1 <= T <= 64), where the GEMM is bound by
+ * streaming W from HBM.  Same operands and result as mmq_gemm_q4K (xa, ds
+ * from mmq_quantize_q8_1; y [T][O] f32, overwritten), computed with the
+ * weight rows on the tensor core's 128-row side fed from tensor memory and
+ * the (at most 64) tokens on the other; the per-super-block fold of
+ * "31 . r28" (2.3), as in mmq_gemm_q4K.  Each 128-row tile is handled by a
+ * cluster of up to 8 CTAs that split its super-blocks and add their partial
+ * sums in a fixed order through distributed shared memory, so the result is
+ * the same on every call.  Allocates nothing; no scratch.
+ * T <= 64 (MMQ_ERR_SHAPE above), other limits as mmq_gemm_q4K.
+ */
+int mmq_gemm_q4K_small(const void *w, const uint16_t *xa, const uint32_t *ds, float *y,
+                       int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * q4_K GEMM for few tokens (1 <= T <= 16) on the int8 warp MMA: the pages'
+ * per-sub-block form ("31 . r28", 2.3) with mma.sync m16n8k32 s8 (one
+ * instruction per 32-weight sub-block, the nibbles used as int8 operands),
+ * the exact integer dots C_b folded in f32 per sub-block.  qs: the int8 q8_1
+ * values [T][K] and ds the scale words, both as written by
+ * mmq_quantize_q8_1.  Result as mmq_gemm_q4K up to f32 summation order;
+ * deterministic.  Allocates nothing.  Kept beside mmq_gemm_q4K_small as the
+ * per-sub-block integer form of the same product.
  * T <= 16 (MMQ_ERR_SHAPE above), other limits as mmq_gemm_q4K.
  */
-int mmq_gemm_q4K_small(const void *w, const int8_t *qs, const uint32_t *ds, float *y,
-                       int T, int O, int K, mmq_stream_t stream);
+int mmq_gemm_q4K_small_imma(const void *w, const int8_t *qs, const uint32_t *ds, float *y,
+                            int T, int O, int K, mmq_stream_t stream);
 
 /*
  * mmq_gemm_q4K_splitk without caller scratch: this entry point allocates

@@ -87,9 +87,25 @@ int make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, 
     return r == CUDA_SUCCESS ? MMQ_OK : MMQ_ERR_DRIVER;
 }
 
+int make_tmap_4d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, const uint64_t (&dims)[4],
+                 const uint64_t (&strides_bytes)[3], const uint32_t (&box)[4], CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return MMQ_ERR_DRIVER;
+    const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+    const cuuint64_t st[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+    const cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map, dtype, 4, const_cast<void *>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && std::getenv("MMQ_DEBUG"))
+        std::fprintf(stderr, "libmmq: cuTensorMapEncodeTiled(4d) failed: %d\n", (int)r);
+    return r == CUDA_SUCCESS ? MMQ_OK : MMQ_ERR_DRIVER;
+}
+
 }  // namespace mmq
 
-extern "C" int mmq_version(void) { return 4; }
+extern "C" int mmq_version(void) { return 5; }
 
 extern "C" const char *mmq_status_str(int status)
 {

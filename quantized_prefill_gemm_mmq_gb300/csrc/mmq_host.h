@@ -25,5 +25,9 @@ int launch_status();
 int make_tmap_2d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, uint64_t inner,
                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                  CUtensorMapSwizzle swizzle);
+// 4-D tiled map: dims innermost first, strides of dims 1..3 in bytes (each a
+// multiple of 16, in any order), box extents per dim
+int make_tmap_4d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, const uint64_t (&dims)[4],
+                 const uint64_t (&strides_bytes)[3], const uint32_t (&box)[4], CUtensorMapSwizzle swizzle);
 
 }  // namespace mmq

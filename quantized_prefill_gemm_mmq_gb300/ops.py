@@ -113,12 +113,26 @@ def gemm(fmt: str, w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int,
     return out
 
 
-SMALL_T_MAX = 16
+SMALL_T_MAX = 64          # mmq_gemm_q4K_small
+SMALL_IMMA_T_MAX = 16     # mmq_gemm_q4K_small_imma
 
 
-def gemm_small(w: torch.Tensor, qs: torch.Tensor, ds: torch.Tensor, O: int,
+def gemm_small(w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int,
                out: torch.Tensor | None = None) -> torch.Tensor:
-    """q4_K GEMM for T <= 16 tokens from the int8 q8_1 values qs [T][K] and ds."""
+    """q4_K GEMM for T <= 64 tokens (weight rows on the tensor core's 128-row
+    side, fed from tensor memory); same operands and result as gemm("q4_K")."""
+    T, K = _check_gemm_args("q4_K", w, xa, O, planes=2)
+    _check_ds(ds, T, K)
+    out = _out(out, T, O, xa.device)
+    with torch.cuda.device(xa.device):
+        st = load().mmq_gemm_q4K_small(_ptr(w), _ptr(xa), _ptr(ds), _ptr(out), T, O, K, _stream(xa.device))
+    _check("mmq_gemm_q4K_small", st)
+    return out
+
+
+def gemm_small_imma(w: torch.Tensor, qs: torch.Tensor, ds: torch.Tensor, O: int,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """q4_K GEMM for T <= 16 tokens on the int8 warp MMA from the int8 q8_1 values qs [T][K] and ds."""
     _need_cuda(w, qs)
     if qs.dtype != torch.int8 or qs.dim() != 2 or not qs.is_contiguous():
         raise ValueError("qs must be contiguous int8 [T][K]")
@@ -128,8 +142,8 @@ def gemm_small(w: torch.Tensor, qs: torch.Tensor, ds: torch.Tensor, O: int,
     _check_ds(ds, T, K)
     out = _out(out, T, O, qs.device)
     with torch.cuda.device(qs.device):
-        st = load().mmq_gemm_q4K_small(_ptr(w), _ptr(qs), _ptr(ds), _ptr(out), T, O, K, _stream(qs.device))
-    _check("mmq_gemm_q4K_small", st)
+        st = load().mmq_gemm_q4K_small_imma(_ptr(w), _ptr(qs), _ptr(ds), _ptr(out), T, O, K, _stream(qs.device))
+    _check("mmq_gemm_q4K_small_imma", st)
     return out
 
 

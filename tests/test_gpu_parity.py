@@ -222,35 +222,56 @@ def test_gemm_splitk_small(ops, orc, T, O, K, ksplit):
     assert int(ws.counters.abs().sum()) == 0         # counters left at zero
 
 
+@pytest.mark.parametrize("T,O,K", [(1, 1, 256), (16, 256, 1024), (5, 131, 2816), (17, 200, 768), (33, 512, 4096),
+                                   (64, 8, 11008), (40, 1000, 512), (3, 20000, 512), (64, 4096, 256),
+                                   (16, 384, 4352), (1, 2048, 11008)])
+def test_gemm_small_t(ops, orc, T, O, K):
+    """Weight-stationary small-T kernel: token tiles of 16, 32 and 64, clusters of
+    1 to 8 CTAs per row tile (O = 20000: one CTA per tile), ragged T and O."""
+    w = synth.make_weights("q4_K", O, K, seed=5 * T + O)
+    x = synth.make_x(T, K, seed=K + 2 * T, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q4_K", w, qs_r, ds_r, O)
+    _, ds, _, xa = _gpu_quant(ops, x)
+    y1 = ops.gemm_small(_dev(w), xa, ds, O)
+    y2 = ops.gemm_small(_dev(w), xa, ds, O)
+    ops.check_status()
+    assert _rel_err(y1.cpu().numpy(), ref) <= TOL
+    assert torch.equal(y1, y2)                       # fixed summation order
+
+
 @pytest.mark.parametrize("T,O,K", [(1, 1, 256), (16, 256, 1024), (5, 131, 2816), (13, 200, 768), (16, 512, 4096),
                                    (9, 8, 11008), (2, 1000, 512)])
-def test_gemm_small_t(ops, orc, T, O, K):
+def test_gemm_small_t_imma(ops, orc, T, O, K):
     w = synth.make_weights("q4_K", O, K, seed=5 * T + O)
     x = synth.make_x(T, K, seed=K + 2 * T, outliers=True)
     qs_r, ds_r = orc.quantize_q8_1(x)
     ref = orc.gemm("q4_K", w, qs_r, ds_r, O)
     qs, ds, _, _ = ops.quantize_q8_1(_dev(x), want_xh=False, want_xa=False)
-    y1 = ops.gemm_small(_dev(w), qs, ds, O)
-    y2 = ops.gemm_small(_dev(w), qs, ds, O)
+    y1 = ops.gemm_small_imma(_dev(w), qs, ds, O)
+    y2 = ops.gemm_small_imma(_dev(w), qs, ds, O)
     ops.check_status()
     assert _rel_err(y1.cpu().numpy(), ref) <= TOL
     assert torch.equal(y1, y2)
 
 
-@pytest.mark.parametrize("T", [16])
+@pytest.mark.parametrize("T", [16, 64])
 def test_gemm_small_t_full_size_sampled(ops, orc, T):
     wl = synth.config(4, T)
     rng = np.random.default_rng(4242 + T)
     for g in wl.gemms:
         x, w = g.x(), g.weights()
         qs_r, ds_r = orc.quantize_q8_1(x)
-        qs, ds, _, _ = ops.quantize_q8_1(_dev(x), want_xh=False, want_xa=False)
-        y = ops.gemm_small(_dev(w), qs, ds, g.O)
+        qs, ds, _, xa = ops.quantize_q8_1(_dev(x), want_xh=False)
+        outs = [("small", ops.gemm_small(_dev(w), xa, ds, g.O))]
+        if T <= ops.SMALL_IMMA_T_MAX:
+            outs.append(("small_imma", ops.gemm_small_imma(_dev(w), qs, ds, g.O)))
         ops.check_status()
         ti, oi = _sample_points(rng, g.T, g.O)
         ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
-        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-        assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
+        for kernel, y in outs:
+            got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
+            assert _rel_err(got, ref) <= TOL, (g.name, kernel, _rel_err(got, ref))
 
 
 def test_gemm_small_t_closed_form(ops):
@@ -259,9 +280,9 @@ def test_gemm_small_t_closed_form(ops):
     q = np.array([(i % 32) % 16 for i in range(256)])
     w = pack_q4K_block(1.0, 1.0, sc, m, q)
     x = np.full((1, 256), 127.0, np.float32)
-    qs, ds, _, _ = ops.quantize_q8_1(_dev(x), want_xh=False, want_xa=False)
-    y = ops.gemm_small(_dev(w), qs, ds, 1)
-    assert float(y[0, 0]) == 6833616.0
+    qs, ds, _, xa = ops.quantize_q8_1(_dev(x), want_xh=False)
+    assert float(ops.gemm_small(_dev(w), xa, ds, 1)[0, 0]) == 6833616.0
+    assert float(ops.gemm_small_imma(_dev(w), qs, ds, 1)[0, 0]) == 6833616.0
 
 
 @pytest.mark.parametrize("cfg,T", [(4, 16), (4, 64), (4, 256)])
