@@ -50,10 +50,10 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-small-t", action="store_true", help="skip the small-T (split-K) side measurement")
+    ap.add_argument("--no-small-t", action="store_true", help="skip the small-T side measurement")
     ap.add_argument("--small-t-launches", type=int, default=0, metavar="T",
-                    help="only launch the split-K GEMM of the config-4 shapes at T tokens three times each "
-                         "(eager; for profiling) and exit")
+                    help="only launch the small-T and the split-K GEMM of the config-4 shapes at T tokens three "
+                         "times each (eager; for profiling) and exit")
     return ap.parse_args()
 
 
@@ -161,19 +161,22 @@ def traffic_bytes(kernel: str):
     return rec["dram_bytes_per_launch"]
 
 
-def graph_time_us(fn, n=20, reps=5):
-    """Device time per call of fn, replayed from a CUDA graph of n calls (best of reps)."""
+def graph_time_us(fns, n=20, reps=5):
+    """Device time per call, replayed from a CUDA graph of n calls that cycles
+    through the callables `fns` (best of reps)."""
     import torch
+    if callable(fns):
+        fns = [fns]
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        fn()
+        fns[0]()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        for _ in range(n):
-            fn()
+        for i in range(n):
+            fns[i % len(fns)]()
     g.replay()
     torch.cuda.synchronize()
     best = float("inf")
@@ -188,26 +191,37 @@ def graph_time_us(fn, n=20, reps=5):
 
 
 def small_t_lines(dev, hbm_gbs):
-    """Side measurement of the small-T tier (config 4 shapes at T = 16 and 64):
-    the one-CTA-per-tile GEMM against the split-K GEMM, device time per launch."""
+    """Side measurement of the small-T tier (config 4 shapes at T = 16 and 64),
+    device time per launch with the weights streamed from HBM (the timed
+    launches cycle through copies of W larger than L2 together): the
+    weight-stationary small-T GEMM, the int8 warp-MMA form (T <= 16), the
+    split-K GEMM and the one-CTA-per-tile production GEMM."""
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     out = []
     for T in (16, 64):
         for g in synth.config(4, T).gemms:
-            w = torch.from_numpy(g.weights()).to(dev)
+            w0 = torch.from_numpy(g.weights()).to(dev)
+            copies = [w0] + [w0.clone() for _ in range(int(320e6 // w0.numel()))]
+            n = 2 * len(copies)
             x = torch.from_numpy(g.x()).to(dev)
-            _, ds, _, xa = ops.quantize_q8_1(x, want_qs=False, want_xh=False)
+            qs, ds, _, xa = ops.quantize_q8_1(x, want_xh=False)
             y = torch.empty((g.T, g.O), dtype=torch.float32, device=dev)
             ks = ops.choose_ksplit(g.T, g.O, g.K)
             ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
-            us_plain = graph_time_us(lambda: ops.gemm("q4_K", w, xa, ds, g.O, out=y))
-            us_split = graph_time_us(lambda: ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws, out=y))
-            nbytes = w.numel() + g.T * g.K * 4 + g.T * g.K // 8 + g.T * g.O * 4   # W + xa + ds + Y
-            out.append({"T": g.T, "K": g.K, "O": g.O, "ksplit": ks, "plain_us": us_plain, "splitk_us": us_split,
-                        "splitk_tmacs": g.macs / (us_split * 1e-6) / 1e12,
-                        "splitk_gbs": nbytes / (us_split * 1e-6) / 1e9,
-                        "splitk_hbm_frac": nbytes / (us_split * 1e-6) / 1e9 / hbm_gbs})
+            us_small = graph_time_us([lambda w=w: ops.gemm_small(w, xa, ds, g.O, out=y) for w in copies], n=n)
+            us_imma = (graph_time_us([lambda w=w: ops.gemm_small_imma(w, qs, ds, g.O, out=y) for w in copies], n=n)
+                       if g.T <= ops.SMALL_IMMA_T_MAX else None)
+            us_split = graph_time_us([lambda w=w: ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws, out=y)
+                                      for w in copies], n=n)
+            us_plain = graph_time_us([lambda w=w: ops.gemm("q4_K", w, xa, ds, g.O, out=y) for w in copies], n=n)
+            nbytes = w0.numel() + g.T * g.K * 4 + g.T * g.K // 8 + g.T * g.O * 4   # W + xa + ds + Y
+            out.append({"T": g.T, "K": g.K, "O": g.O, "small_us": us_small, "small_imma_us": us_imma,
+                        "splitk_us": us_split, "ksplit": ks, "plain_us": us_plain,
+                        "small_tmacs": g.macs / (us_small * 1e-6) / 1e12,
+                        "small_gbs": nbytes / (us_small * 1e-6) / 1e9,
+                        "small_hbm_frac": nbytes / (us_small * 1e-6) / 1e9 / hbm_gbs})
+            del copies
     ops.check_status(dev)
     return out
 
@@ -279,7 +293,8 @@ def reference_arm(args):
 # ------------------------------------------------------------- GPU arm ---
 
 def small_t_launches(T):
-    """Three eager launches of the split-K GEMM per config-4 shape at T tokens."""
+    """Three eager launches each of the small-T GEMM and of the split-K GEMM
+    per config-4 shape at T tokens."""
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     dev = torch.device("cuda", 0)
@@ -288,6 +303,8 @@ def small_t_launches(T):
         _, ds, _, xa = ops.quantize_q8_1(torch.from_numpy(g.x()).to(dev), want_qs=False, want_xh=False)
         ks = ops.choose_ksplit(g.T, g.O, g.K)
         ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
+        for _ in range(3):
+            ops.gemm_small(w, xa, ds, g.O)
         for _ in range(3):
             ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws)
     ops.check_status(dev)
@@ -508,8 +525,10 @@ def mmq_arm(args):
                          f"7 GEMMs of one layer ({macs} MACs, {secs:.1f} s, one thread)"}
     small_t = None
     if not args.no_small_t and world == 1:
-        small_t = {"kernel": "mmq_q4K_sb_kernel, one CTA per 128x128 tile vs split-K (mmq_gemm_q4K_splitk)",
-                   "timing": "CUDA-graph replay of 20 launches, device events, best of 5",
+        small_t = {"kernel": "mmq_q4K_wt_kernel (mmq_gemm_q4K_small) vs mmq_q4K_small_kernel (int8 warp MMA), "
+                             "split-K (mmq_gemm_q4K_splitk) and one CTA per 128x128 tile (mmq_gemm_q4K)",
+                   "timing": "CUDA-graph replay cycling through >320 MB of weight copies (HBM-resident), device "
+                             "events, best of 5",
                    "bytes": "weights + xa (4 B/elem) + ds + y",
                    "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
                    "lines": small_t_lines(dev, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))}
