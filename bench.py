@@ -226,9 +226,39 @@ def small_t_lines(dev, hbm_gbs):
     return out
 
 
+class LaunchGroup:
+    """Projections run as one GEMM launch: members share the input and the
+    format, the weight rows are concatenated and the output columns too."""
+
+    def __init__(self, name, members):
+        g0 = members[0]
+        self.name, self.members = name, members
+        self.fmt, self.T, self.K, self.x_seed = g0.fmt, g0.T, g0.K, g0.x_seed
+        self.O = sum(m.O for m in members)
+        self.macs = sum(m.macs for m in members)
+
+
+def launch_groups(wl):
+    """gate and up read the same input: one GEMM over their concatenated rows
+    (at T = 512, 688 output tiles of 128 x 128 instead of 2 x 344, i.e. five
+    waves of 152 SMs instead of six; the same MACs and, tile for tile, the
+    same arithmetic).  Every other projection is its own launch."""
+    byname = {g.name: g for g in wl.gemms}
+    out = []
+    for g in wl.gemms:
+        if g.name == "up" and "gate" in byname:
+            continue
+        if g.name == "gate" and "up" in byname:
+            out.append(LaunchGroup("gate+up", [g, byname["up"]]))
+        else:
+            out.append(LaunchGroup(g.name, [g]))
+    return out
+
+
 def workload_desc(T, layers):
     return (f"LLaMA-7B decoder-stack projections, prefill T={T}, {layers} layers: per layer q/k/o q4_K 4096x4096, "
-            f"v q6_K 4096x4096, gate/up q4_K 4096->11008, down q4_K 11008->4096, 4 q8_1 quantisations")
+            f"v q6_K 4096x4096, gate/up q4_K 4096->11008 (one launch over the concatenated rows), down q4_K "
+            f"11008->4096, 4 q8_1 quantisations")
 
 
 def build_inputs(T):
@@ -312,6 +342,7 @@ def small_t_launches(T):
 
 
 def mmq_arm(args):
+    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -328,8 +359,11 @@ def mmq_arm(args):
     dev = torch.device("cuda", local)
 
     wl, xs = build_inputs(args.tokens)
+    groups = launch_groups(wl)
     host_w = {g.name: g.weights() for g in wl.gemms}
-    w_layer = {n: torch.from_numpy(w).to(dev) for n, w in host_w.items()}
+    # one device weight tensor per launch group (gate and up: their rows concatenated)
+    w_layer = {gr.name: torch.from_numpy(np.concatenate([host_w[m.name] for m in gr.members])).to(dev)
+               for gr in groups}
     layers = [w_layer] + [{n: t.clone() for n, t in w_layer.items()} for _ in range(args.layers - 1)]
     x_dev = {s: torch.from_numpy(x).to(dev) for s, x in xs.items()}
     # q8_1 planes per input: both production GEMMs read xa (the exact hi/lo
@@ -339,10 +373,11 @@ def mmq_arm(args):
                 None,
                 torch.empty((2,) + x.shape, dtype=torch.float16, device=dev))
             for s, x in xs.items()}
-    ybuf = {g.name: torch.empty((g.T, g.O), dtype=torch.float32, device=dev) for g in wl.gemms}
+    ybuf = {g.name: torch.empty((g.T, g.O), dtype=torch.float32, device=dev) for g in groups}
     layer_macs = wl.macs
+    assert layer_macs == sum(g.macs for g in groups)
     step_macs = layer_macs * args.layers
-    launches_per_step = args.layers * (len(xs) + len(wl.gemms))
+    launches_per_step = args.layers * (len(xs) + len(groups))
 
     ext_events = None   # per-launch events of the q4_K GEMMs, recorded inside the graph
 
@@ -354,7 +389,7 @@ def mmq_arm(args):
         for li, lw in enumerate(layers):
             for s, x in x_dev.items():
                 ops.quantize_q8_1(x, out=qbuf[s])
-            for gi, g in enumerate(wl.gemms):
+            for gi, g in enumerate(groups):
                 ev = record[li][gi] if record is not None else None
                 if ev is not None:
                     ev[0].record()
@@ -374,7 +409,7 @@ def mmq_arm(args):
         try:
             ext_events = [[(torch.cuda.Event(enable_timing=True, external=True),
                             torch.cuda.Event(enable_timing=True, external=True)) if g.fmt == "q4_K" else None
-                           for g in wl.gemms] for _ in layers]
+                           for g in groups] for _ in layers]
         except TypeError:
             ext_events = None
         graph = torch.cuda.CUDAGraph()
@@ -428,7 +463,7 @@ def mmq_arm(args):
 
     if ext_events is not None:
         for li in range(len(layers)):
-            for gi, g in enumerate(wl.gemms):
+            for gi, g in enumerate(groups):
                 ev = ext_events[li][gi]
                 if ev is not None:
                     ms = ev[0].elapsed_time(ev[1])
@@ -442,7 +477,7 @@ def mmq_arm(args):
     if sq_ms <= 0.0:
         pairs = []
         for lw in layers:
-            for g in wl.gemms:
+            for g in groups:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(cur)
                 run_gemm(g, lw)

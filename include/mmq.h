@@ -262,6 +262,16 @@ int mmq_probe_tensor_peak(int kind, double *tmacs, mmq_stream_t stream);
  */
 int mmq_check_status(mmq_stream_t stream, int *detail);
 
+/*
+ * More detail on the last failure that mmq_check_status reported (no
+ * counterpart on the pages; a diagnostic of the library's own bounded waits): info
+ * receives 4 ints: the time the failed wait had waited (microseconds), its
+ * poll count, the phase parity it waited for and the waited barrier's
+ * shared-memory address.  All zero if no failure was reported yet.  Returns
+ * MMQ_OK, or MMQ_ERR_NULL for a NULL `info`.
+ */
+int mmq_last_failure_info(int *info);
+
 #ifdef __cplusplus
 }
 #endif

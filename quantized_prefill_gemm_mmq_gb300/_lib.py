@@ -35,6 +35,7 @@ SIGNATURES = {
     "mmq_debug_subdots_q4K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q6K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_check_status": (_I, [_P, _P]),
+    "mmq_last_failure_info": (_I, [_P]),
     "mmq_probe_tensor_peak": (_I, [_I, _P, _P]),
 }
 

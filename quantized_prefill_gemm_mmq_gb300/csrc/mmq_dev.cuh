@@ -13,9 +13,11 @@ namespace mmq {
 
 // ------------------------------------------------------------ status word --
 // g_status[0] = first error code, [1] = kernel id, [2] = wait site,
-// [3] = linear block index.  One copy per translation unit (internal
-// linkage); the GEMM translation unit owns the one mmq_check_status reads.
-static __device__ int g_status[4];
+// [3] = linear block index, [4] = time waited (us), [5] = polls,
+// [6] = phase parity waited for, [7] = the barrier's shared-memory address.
+// One copy per translation unit (internal linkage); the GEMM translation
+// unit owns the one mmq_check_status reads.
+static __device__ int g_status[8];
 
 constexpr int kStatusTimeout = -5;            // == MMQ_ERR_TIMEOUT
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
@@ -27,12 +29,17 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
-__device__ __forceinline__ void record_error(int code, int kernel_id, int site)
+__device__ __forceinline__ void record_error(int code, int kernel_id, int site, int waited_us = 0, int polls = 0,
+                                             int parity = 0, int bar = 0)
 {
     if (atomicCAS(&g_status[0], 0, code) == 0) {
         g_status[1] = kernel_id;
         g_status[2] = site;
         g_status[3] = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+        g_status[4] = waited_us;
+        g_status[5] = polls;
+        g_status[6] = parity;
+        g_status[7] = bar;
     }
 }
 
@@ -97,22 +104,31 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 constexpr uint32_t kWaitSleepNs = 20000;     // longest single hardware sleep of a wait
 
+constexpr uint64_t kPollCreditNs = 1000000;    // most waiting time one poll may add (1 ms)
+
 // Wait for the phase with the given parity to complete.  Gives up (and
-// returns false) when *abort is set by another role, or after kWaitLimitNs,
-// in which case it records MMQ_ERR_TIMEOUT and raises *abort itself.
+// returns false) when *abort is set by another role, or after kWaitLimitNs
+// of waiting, in which case it records MMQ_ERR_TIMEOUT and raises *abort
+// itself.  The time waited is the sum of the global timer's steps between
+// polls, each counted only if positive and at most kPollCreditNs, so that an
+// adjustment of the global timer (backwards or a jump forwards) cannot end a
+// wait on its own.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t *abort,
                                           int kernel_id, int site)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    uint64_t prev = globaltimer(), waited = 0;
     for (uint32_t polls = 1;; ++polls) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (*abort) return false;
-        // both the clock and a minimum number of polls must say so: a jump of
-        // the global timer alone never ends a wait
-        if (polls > 4096u && globaltimer() - t0 > kWaitLimitNs) {
+        const uint64_t now = globaltimer();
+        const int64_t step = (int64_t)(now - prev);
+        prev = now;
+        if (step > 0) waited += (uint64_t)step < kPollCreditNs ? (uint64_t)step : kPollCreditNs;
+        if (waited > kWaitLimitNs) {
             *abort = 1u;
-            record_error(kStatusTimeout, kernel_id, site);
+            record_error(kStatusTimeout, kernel_id, site, (int)(waited / 1000u),
+                         (int)(polls < 0x7FFFFFFFu ? polls : 0x7FFFFFFFu), (int)parity, (int)bar);
             return false;
         }
     }

@@ -118,11 +118,18 @@ enum { SITE_P_RAW = 1, SITE_P_STAGE, SITE_M_A, SITE_M_B, SITE_M_ACC, SITE_U_RAW,
 
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity)
 {
-    // used only on the way out: waits for work already in flight, which
-    // completes on its own; bounded all the same
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    // used on the way out: waits for work already in flight, which completes
+    // on its own; bounded all the same, with the time waited counted as in
+    // mbar_wait (positive global-timer steps of at most kPollCreditNs each),
+    // so that a timer adjustment cannot end the drain early
+    uint64_t prev = globaltimer(), waited = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        const uint64_t now = globaltimer();
+        const int64_t step = (int64_t)(now - prev);
+        prev = now;
+        if (step > 0) waited += (uint64_t)step < kPollCreditNs ? (uint64_t)step : kPollCreditNs;
+        if (waited > kWaitLimitNs) return false;
+    }
     return true;
 }
 
@@ -2891,6 +2898,9 @@ extern "C" int mmq_debug_subdots_q6K(const void *w, const uint16_t *xh, int32_t 
     return mmq::launch<mmq::kQ6K, mmq::kSubdots>(w, xh, nullptr, nullptr, out, T, O, K, stream);
 }
 
+// extra detail of the last failure reported by mmq_check_status (host side)
+static int g_last_failure[4];
+
 extern "C" int mmq_check_status(mmq_stream_t stream, int *detail)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
@@ -2898,16 +2908,24 @@ extern "C" int mmq_check_status(mmq_stream_t stream, int *detail)
         if (detail) detail[0] = detail[1] = detail[2] = detail[3] = 0;
         return MMQ_ERR_CUDA;
     }
-    int h[4] = {0, 0, 0, 0};
+    int h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (cudaMemcpyFromSymbol(h, mmq::g_status, sizeof(h)) != cudaSuccess) {
         cudaGetLastError();
         return MMQ_ERR_CUDA;
     }
     if (h[0] != 0) {
-        const int zero[4] = {0, 0, 0, 0};
+        const int zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         cudaMemcpyToSymbol(mmq::g_status, zero, sizeof(zero));
+        for (int i = 0; i < 4; ++i) g_last_failure[i] = h[4 + i];
     }
     if (detail)
         for (int i = 0; i < 4; ++i) detail[i] = h[i];
     return h[0];
+}
+
+extern "C" int mmq_last_failure_info(int *info)
+{
+    if (!info) return MMQ_ERR_NULL;
+    for (int i = 0; i < 4; ++i) info[i] = g_last_failure[i];
+    return MMQ_OK;
 }

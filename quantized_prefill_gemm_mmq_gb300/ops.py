@@ -241,7 +241,10 @@ def check_status(device: torch.device | None = None):
     with torch.cuda.device(dev):
         st = load().mmq_check_status(_stream(dev), detail)
     if st != 0:
-        raise MMQError(f"kernel (id {detail[1]}, site {detail[2]}, block {detail[3]})", st)
+        info = (ctypes.c_int * 4)()
+        load().mmq_last_failure_info(info)
+        raise MMQError(f"kernel (id {detail[1]}, site {detail[2]}, block {detail[3]}; waited {info[0]} us over "
+                       f"{info[1]} polls for parity {info[2]} of the barrier at shared address {info[3]})", st)
 
 
 def tensor_peak_tmacs(kind: str = "int8", device: torch.device | None = None) -> float:

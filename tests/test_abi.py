@@ -19,7 +19,8 @@ def test_header_declares_the_boundary():
     for required in ("mmq_quantize_q8_1", "mmq_gemm_q4K", "mmq_gemm_q4K_subblock", "mmq_gemm_q6K", "mmq_check_status",
                      "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K",
                      "mmq_gemm_q4K_splitk", "mmq_splitk_sizes", "mmq_gemm_q4K_splitk_static",
-                     "mmq_gemm_q6K_subblock", "mmq_gemm_q4K_small", "mmq_gemm_q4K_small_imma"):
+                     "mmq_gemm_q6K_subblock", "mmq_gemm_q4K_small", "mmq_gemm_q4K_small_imma",
+                     "mmq_last_failure_info"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -36,7 +37,7 @@ def test_library_exports_every_header_symbol():
 @needs_lib
 def test_library_loads_and_reports():
     lib = _lib.load()
-    assert lib.mmq_version() == 5
+    assert lib.mmq_version() == 6
     assert lib.mmq_status_str(0) == b"ok"
     for code in range(-9, 0):
         assert lib.mmq_status_str(code) not in (b"", b"unknown status")
@@ -64,6 +65,9 @@ def test_argument_errors_without_gpu():
     assert lib.mmq_gemm_q4K_small(p, p, null, p, 64, 8, 256, null) == -6
     assert lib.mmq_gemm_q4K_small(p, odd, p, p, 64, 8, 256, null) == -2
     assert lib.mmq_gemm_q4K_small(p, p, p, p, 0, 8, 256, null) == 0          # T == 0 no-op
+    assert lib.mmq_last_failure_info(null) == -6
+    info = (ctypes.c_int * 4)(7, 7, 7, 7)
+    assert lib.mmq_last_failure_info(info) == 0 and list(info) == [0, 0, 0, 0]   # nothing reported yet
     assert lib.mmq_gemm_q4K(p, p, p, p, -1, 1, 256, null) == -1              # T < 0
     # T == 0 is a no-op
     assert lib.mmq_gemm_q4K(p, p, p, p, 0, 1, 256, null) == 0

@@ -347,3 +347,22 @@ def test_gpu_argument_errors(ops):
     with pytest.raises(MMQError) as e:
         ops.gemm("q4_K", w2, xa, ds, 2)       # misaligned weight pointer
     assert e.value.status == -2
+
+
+def test_gemm_concatenated_rows_equal_separate(ops):
+    """One GEMM over the concatenated rows of two weight matrices that share an
+    input gives, column block for column block, exactly the two GEMMs' outputs
+    (each 128 x 128 output tile depends only on its own weight rows); the
+    benchmark's gate/up projections run this way."""
+    T, K = 512, 4096
+    O1, O2 = 11008, 11008
+    w1 = synth.make_weights("q4_K", O1, K, seed=71)
+    w2 = synth.make_weights("q4_K", O2, K, seed=72)
+    x = synth.make_x(T, K, seed=73, outliers=True)
+    _, ds, _, xa = ops.quantize_q8_1(_dev(x), want_qs=False, want_xh=False)
+    y1 = ops.gemm("q4_K", _dev(w1), xa, ds, O1)
+    y2 = ops.gemm("q4_K", _dev(w2), xa, ds, O2)
+    y12 = ops.gemm("q4_K", _dev(np.concatenate([w1, w2])), xa, ds, O1 + O2)
+    ops.check_status()
+    assert torch.equal(y12[:, :O1], y1)
+    assert torch.equal(y12[:, O1:], y2)
