@@ -241,7 +241,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 
-// generic-proxy shared-memory writes -> visible to the tensor core's reads
+// Orders this thread's generic-proxy shared-memory accesses with the async
+// proxy (TMA, bulk copies, the tensor core): needed after writes the tensor
+// core will read, and also after reads of a buffer that a TMA or bulk copy
+// refills once it is released -- an mbarrier release alone did not order
+// those reads before the copy's write (measured: a one-slot raw-weight ring
+// released without it gave results that changed from run to run).
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -1209,11 +1209,13 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         const bool tma_lane = (r & 31) == 0;
         bool ok = true;
         int last_a = -1;   // last activation stage this thread issued
+        int n_raw = 0;     // raw super-blocks requested (thread 0), for the drain on abort
         if (r == 0) {
             tma_prefetch(&tmA);
             tma_prefetch(&tmW);
             mbar_arrive_expect_tx(r_full(0), RAW_BYTES);
             tma_load_2d(sbase + oRaw, &tmW, r_full(0), sb_base * 144, o0);
+            n_raw = 1;
         }
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int rs = sb % RSTG;
@@ -1223,6 +1225,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             const uint4 *raw = reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + r * 144);
 #pragma unroll
             for (int i = 0; i < 9; ++i) cur[i] = raw[i];
+            fence_proxy_async_smem();   // these reads before the next TMA write into the slot
             mbar_arrive(r_empty(rs));
             if (r == 0 && sb + 1 < nsb) {
                 const int rn = (sb + 1) % RSTG;
@@ -1230,6 +1233,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 if (ok) {
                     mbar_arrive_expect_tx(r_full(rn), RAW_BYTES);
                     tma_load_2d(sbase + oRaw + rn * RAW_BYTES, &tmW, r_full(rn), (sb_base + sb + 1) * 144, o0);
+                    n_raw = sb + 2;
                 }
             }
 #pragma unroll
@@ -1274,6 +1278,8 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         if (!ok && last_a >= 0)
             for (int i = max(0, last_a - STG + 1); i <= last_a; ++i)
                 if ((i & 3) == (r >> 5)) wait_drain(full(i % STG), (i / STG) & 1);
+        if (!ok && r == 0)
+            for (int i = max(0, n_raw - RSTG); i < n_raw; ++i) wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
         // --------------------------------------------------------- epilogue --
         // Thread = one token (TMEM lane) x 64 weight rows; Y += d*(D_even +
@@ -1418,6 +1424,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
                 hdn[h] = *reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + (sr + 64 * h) * 144);
+            fence_proxy_async_smem();   // these reads before the next TMA write into the slot
             mbar_arrive(r_empty(rs));
             if (sb >= SSTG) {
                 const int prev = sb - SSTG;
@@ -1820,7 +1827,10 @@ __global__ void __launch_bounds__(q6s::NTHREADS, 1)
                 uint32_t ql[16], qh[8];
                 row_words<16>(row, lead + 64 * h, ql);
                 row_words<8>(row, lead + 128 + 32 * h, qh);
-                if (h == 1) mbar_arrive(r_empty(rs));
+                if (h == 1) {
+                    fence_proxy_async_smem();   // these reads before the next bulk copy into the slot
+                    mbar_arrive(r_empty(rs));
+                }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const int jb = 4 * h + g, ks = sb * SPS + jb, s = ks % STG;
@@ -2493,6 +2503,7 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
             const uint4 *raw = reinterpret_cast<const uint4 *>(smem + C::oRaw + rs * RAW_BYTES + r * 144);
 #pragma unroll
             for (int k = 0; k < 9; ++k) cur[k] = raw[k];
+            fence_proxy_async_smem();   // these reads before the next TMA write into the slot
             __syncwarp();
             if (lane == 0) mbar_arrive(raw_empty(rs));
             const bool d_zero = (cur[0].x & 0x7FFFu) == 0u;
