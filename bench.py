@@ -191,7 +191,7 @@ def graph_time_us(fns, n=20, reps=5):
 
 
 def small_t_lines(dev, hbm_gbs):
-    """Side measurement of the small-T tier (config 4 shapes at T = 16 and 64),
+    """Side measurement of the small-T tier (config 4 shapes at T = 1, 16 and 64),
     device time per launch with the weights streamed from HBM (the timed
     launches cycle through copies of W larger than L2 together): the
     weight-stationary small-T GEMM, the int8 warp-MMA form (T <= 16), the
@@ -199,7 +199,7 @@ def small_t_lines(dev, hbm_gbs):
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     out = []
-    for T in (16, 64):
+    for T in (1, 16, 64):
         for g in synth.config(4, T).gemms:
             w0 = torch.from_numpy(g.weights()).to(dev)
             copies = [w0] + [w0.clone() for _ in range(int(320e6 // w0.numel()))]
