@@ -366,3 +366,55 @@ def test_gemm_concatenated_rows_equal_separate(ops):
     ops.check_status()
     assert torch.equal(y12[:, :O1], y1)
     assert torch.equal(y12[:, O1:], y2)
+
+
+def _sampled_check(orc, fmt, w, x, O, ys, n=24, seed=0):
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    rng = np.random.default_rng(seed)
+    T = x.shape[0]
+    ti = rng.integers(0, T, n).astype(np.int32)
+    oi = rng.integers(0, O, n).astype(np.int32)
+    ti[0], oi[0] = T - 1, O - 1                      # the last row and column
+    ref = orc.gemm_points(fmt, w, qs_r, ds_r, O, ti, oi)
+    for name, y in ys:
+        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
+        assert _rel_err(got, ref) <= TOL, (name, _rel_err(got, ref))
+        assert torch.isfinite(y).all(), name
+
+
+def test_gemm_max_k(ops, orc):
+    """K at the library's limit (2^20: 4096 super-blocks per row): long
+    accumulation in every q4_K and q6_K GEMM form, sampled against the oracle."""
+    T, O, K = 4, 128, 1 << 20
+    x = synth.make_x(T, K, seed=91, outliers=True)
+    qs, ds, xh, xa = _gpu_quant(ops, x)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    assert np.array_equal(qs.cpu().numpy(), qs_r)
+    assert np.array_equal(ds.cpu().numpy().view(np.uint32), ds_r)
+    w4 = synth.make_weights("q4_K", O, K, seed=92)
+    wd = _dev(w4)
+    ys = [("production", ops.gemm("q4_K", wd, xa, ds, O)),
+          ("splitk", ops.gemm_splitk(wd, xa, ds, O, ksplit=8)),
+          ("small", ops.gemm_small(wd, xa, ds, O)),
+          ("small_imma", ops.gemm_small_imma(wd, qs, ds, O))]
+    ops.check_status()
+    _sampled_check(orc, "q4_K", w4, x, O, ys, seed=1)
+    w6 = synth.make_weights("q6_K", O, K, seed=93)
+    y6 = ops.gemm("q6_K", _dev(w6), xa, ds, O)
+    ops.check_status()
+    _sampled_check(orc, "q6_K", w6, x, O, [("q6_K production", y6)], seed=2)
+
+
+def test_gemm_large_o(ops, orc):
+    """2^18 output rows (2048 row tiles, 37.7 MB of q4_K weights at K = 256):
+    tile indexing and 64-bit offsets, sampled against the oracle."""
+    T, O, K = 3, 1 << 18, 256
+    x = synth.make_x(T, K, seed=94, outliers=True)
+    qs, ds, _, xa = _gpu_quant(ops, x)
+    w = synth.make_weights("q4_K", O, K, seed=95)
+    wd = _dev(w)
+    ys = [("production", ops.gemm("q4_K", wd, xa, ds, O)),
+          ("small", ops.gemm_small(wd, xa, ds, O)),
+          ("small_imma", ops.gemm_small_imma(wd, qs, ds, O))]
+    ops.check_status()
+    _sampled_check(orc, "q4_K", w, x, O, ys, seed=3)
