@@ -1033,7 +1033,14 @@ __global__ void __launch_bounds__(q4::NTHREADS, 1)
 // Each stage has a single "full" barrier (TMA bytes of both activation
 // planes + the 128 unpack threads' arrivals) and a single "empty" barrier;
 // the unpack warps, which wait on "empty" anyway, take turns issuing the
-// stages' activation TMA (stage ks by unpack warp ks % 4).  The raw weight
+// stages' activation TMA (stage ks by unpack warp ks % 4).  Stage ks uses
+// operand slot ks % STG but barriers ks % (2 STG): a parity wait can only
+// tell apart phases one apart, so every waiter must see each phase of the
+// barriers it waits on.  With one barrier per slot and an odd ring, stages
+// ks and ks + STG belong to different issuers, and an issuer waiting for
+// stage ks + 2 STG while stage ks + STG was still filling would pass at once
+// on the parity of the phase before it.  With 2 STG barriers all stages on
+// one barrier belong to one issuer.  The raw weight
 // super-blocks (128 rows x 144 bytes) arrive by TMA one super-block ahead;
 // the unpack and scale threads copy what they need to registers at the
 // start of a super-block and release the raw slot at once.
@@ -1060,14 +1067,15 @@ constexpr uint32_t RAW_BYTES = BN * 144;
 constexpr uint32_t MIN_OP_BYTES = 128 * 64;
 constexpr uint32_t SDS_D = 2 * MIN_OP_BYTES;
 constexpr uint32_t SDS_BYTES = SDS_D + BN * 4;
+constexpr int SBAR = 2 * STG;                     // full / empty barriers: stage ks uses ks % SBAR
 constexpr uint32_t oStage = 0;
 constexpr uint32_t oRaw = oStage + STG * STAGE_BYTES;
 constexpr uint32_t oSds = oRaw + RSTG * RAW_BYTES;
 constexpr uint32_t oBar = oSds + SSTG * SDS_BYTES;
-// full, empty [STG]; s_full [SSTG]; acc_full, acc_empty [NACC] (shared by the
+// full, empty [SBAR]; s_full [SSTG]; acc_full, acc_empty [NACC] (shared by the
 // even and odd accumulators of a super-block); r_full, r_empty [RSTG];
 // done [2] (each issuer's stage completions); mma_done
-constexpr int kNumBars = 2 * STG + SSTG + 2 * NACC + 2 * RSTG + 2 + 1;
+constexpr int kNumBars = 2 * SBAR + SSTG + 2 * NACC + 2 * RSTG + 2 + 1;
 constexpr uint32_t oMisc = oBar + kNumBars * 8;
 constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
 static_assert(kDynSmem <= 232448, "shared memory budget");
@@ -1110,23 +1118,23 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     const int nks = nsb * 4;
 
     const uint32_t bar0 = sbase + oBar;
-    auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (STG + s); };
-    auto s_full = [&](int s) { return bar0 + 8u * (2 * STG + s); };
-    auto acc_full = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + s); };
-    auto acc_empty = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + NACC + s); };
-    auto r_full = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + s); };
-    auto r_empty = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + RSTG + s); };
-    auto done = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + 2 * RSTG + s); };
+    auto full = [&](int b) { return bar0 + 8u * b; };
+    auto empty = [&](int b) { return bar0 + 8u * (SBAR + b); };
+    auto s_full = [&](int s) { return bar0 + 8u * (2 * SBAR + s); };
+    auto acc_full = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + s); };
+    auto acc_empty = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + NACC + s); };
+    auto r_full = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + 2 * NACC + s); };
+    auto r_empty = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + 2 * NACC + RSTG + s); };
+    auto done = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + 2 * NACC + 2 * RSTG + s); };
     const uint32_t mma_done = bar0 + 8u * (kNumBars - 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + oMisc);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + oMisc + 4);
     auto stage_a = [&](int s) { return sbase + oStage + (uint32_t)s * STAGE_BYTES; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STG; ++s) {
-            mbar_init(full(s), 1 + 128);                    // TMA issue (with its bytes) + unpack threads
-            mbar_init(empty(s), 1);                         // the commit of the stage's issuer
+        for (int b = 0; b < SBAR; ++b) {
+            mbar_init(full(b), 1 + 128);                    // TMA issue (with its bytes) + unpack threads
+            mbar_init(empty(b), 1);                         // the commit of the stage's issuer
         }
         for (int s = 0; s < SSTG; ++s) mbar_init(s_full(s), 64);   // scale threads
         for (int s = 0; s < NACC; ++s) {
@@ -1158,14 +1166,14 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             const int me = warp == 1 ? 0 : 1;   // stages with ks % 2 == me
             bool ok = true;
             for (int ks = me; ks < nks && ok; ks += 2) {
-                const int s = ks % STG;
+                const int s = ks % STG, fb = ks % SBAR;
                 const int sb = ks >> 2, p4 = ks & 3, slot = sb % NACC;
                 // Throttle: this issuer's previous stage has completed.  At most two stages
                 // are then queued in the tensor pipe (the other issuer's, executing, and this
                 // one), and the rest of the ring is free for loading.
                 const int n_mine = ks >> 1;   // stages this issuer has issued so far
                 ok = (n_mine == 0 || mbar_wait(done(me), (n_mine - 1) & 1, abort_flag, kKid, SITE_M_A)) &&
-                     mbar_wait(full(s), (ks / STG) & 1, abort_flag, kKid, SITE_M_A) &&
+                     mbar_wait(full(fb), (ks / SBAR) & 1, abort_flag, kKid, SITE_M_A) &&
                      (p4 > 1 || mbar_wait(acc_empty(slot), ((sb / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC));
                 if (!ok) break;
                 tc_fence_after();
@@ -1191,7 +1199,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                     umma_tf32(d_acc, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
                 }
                 if (p4 >= 2) umma_commit(acc_full(slot));   // this issuer's last stage of the super-block
-                umma_commit(empty(s));
+                umma_commit(empty(fb));
                 umma_commit(done(me));
             }
             umma_commit(mma_done);
@@ -1238,7 +1246,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             }
 #pragma unroll
             for (int p4 = 0; p4 < 4; ++p4) {
-                const int ks = sb * 4 + p4, s = ks % STG;
+                const int ks = sb * 4 + p4, s = ks % STG, fb = ks % SBAR;
                 int sc_lo, sc_hi, unused;
                 q4::q4K_scale_min(cur[0].y, cur[0].z, cur[0].w, 2 * p4, sc_lo, unused);
                 q4::q4K_scale_min(cur[0].y, cur[0].z, cur[0].w, 2 * p4 + 1, sc_hi, unused);
@@ -1259,25 +1267,27 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                     vv[c + 4] = make_uint4(q4s::magic2(ha, 0x4140u, mhi, ahi), q4s::magic2(ha, 0x4342u, mhi, ahi),
                                            q4s::magic2(hb, 0x4140u, mhi, ahi), q4s::magic2(hb, 0x4342u, mhi, ahi));
                 }
-                ok = mbar_wait(empty(s), ((ks / STG) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
+                // slot s is free once stage ks - STG's MMAs have completed
+                ok = ks < STG ||
+                     mbar_wait(empty((ks - STG) % SBAR), ((ks - STG) / SBAR) & 1, abort_flag, kKid, SITE_U_STAGE);
                 if (!ok) break;
                 if (tma_lane && (r >> 5) == (ks & 3)) {
                     // the activation tensor is [2T][K]: hi plane rows 0..T-1, lo plane rows T..2T-1
-                    mbar_arrive_expect_tx(full(s), A_STAGE);
-                    tma_load_2d(stage_a(s), &tmA, full(s), (sb_base * 4 + ks) * BK, t0);
-                    tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(s), (sb_base * 4 + ks) * BK, T + t0);
+                    mbar_arrive_expect_tx(full(fb), A_STAGE);
+                    tma_load_2d(stage_a(s), &tmA, full(fb), (sb_base * 4 + ks) * BK, t0);
+                    tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(fb), (sb_base * 4 + ks) * BK, T + t0);
                     last_a = ks;
                 }
                 uint8_t *brow = smem + oStage + s * STAGE_BYTES + A_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = vv[c];
                 fence_proxy_async_smem();
-                mbar_arrive(full(s));
+                mbar_arrive(full(fb));
             }
         }
         if (!ok && last_a >= 0)
             for (int i = max(0, last_a - STG + 1); i <= last_a; ++i)
-                if ((i & 3) == (r >> 5)) wait_drain(full(i % STG), (i / STG) & 1);
+                if ((i & 3) == (r >> 5)) wait_drain(full(i % SBAR), (i / SBAR) & 1);
         if (!ok && r == 0)
             for (int i = max(0, n_raw - RSTG); i < n_raw; ++i) wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
@@ -2234,6 +2244,11 @@ int launch_q4K_small(const void *w, const int8_t *qs, const uint32_t *ds, float 
 // accumulators of its own); 3 builds the tokens' min-term operand from the
 // q8_1 scale words; 4-7 and 8-11 unpack (even / odd units, thread = weight
 // row); 12-15 epilogue (thread = weight row).
+// The rings that alternating agents wait on (raw weights, activation
+// chunks, TMEM A buffers) have twice as many full / empty barriers as slots:
+// unit i uses slot i % S and barriers i % 2S, so every barrier is waited on
+// by one agent through consecutive phases (a parity wait cannot tell apart
+// phases two apart); the other rings are even-sized and waited on in order.
 // =========================================================================
 struct WtParams {
     const uint8_t *w;   // [O][nsb] q4_K blocks
@@ -2261,6 +2276,7 @@ struct Cfg {
     static constexpr int CSTG = N == 16 ? 16 : (N == 32 ? 10 : 8);  // activation chunk ring (64 k each)
     static constexpr int DSTG = 4;                                  // scale-word / min-operand ring
     static constexpr int RSTG = N == 64 ? 3 : 4;                    // raw weight ring
+    static constexpr int RB = 2 * RSTG, CB = 2 * CSTG, AB = 2 * ABUF;   // barriers of the rings above
     static constexpr uint32_t PLANE = N * 128;                      // 64 k x N rows of one plane
     static constexpr uint32_t CH_BYTES = 2 * PLANE;                 // hi rows then lo rows
     static constexpr uint32_t DS_BYTES = N * 32;                    // [N][8] q8_1 scale words
@@ -2273,9 +2289,10 @@ struct Cfg {
     static constexpr uint32_t oRaw = oDsr + DSTG * D_SLOT;
     static constexpr uint32_t oAmin = oRaw + RSTG * RAW_BYTES;
     static constexpr uint32_t oBar = oAmin + ABUF * AMIN_BYTES;
-    // raw_full, raw_empty [RSTG]; c_full, c_empty [CSTG]; d_full, d_empty, bmin_full [DSTG];
-    // a_full, a_empty [ABUF]; acc_full, acc_empty [NACC]; done [2]
-    static constexpr int kNumBars = 2 * RSTG + 2 * CSTG + 3 * DSTG + 2 * ABUF + 2 * NACC + 2;
+    // raw_full, raw_empty [RB]; c_full, c_empty [CB]; d_full, d_empty, bmin_full [DSTG];
+    // a_full, a_empty [AB]; acc_full, acc_empty [NACC]; done [2]
+    static constexpr int kNumBars = 2 * RB + 2 * CB + 3 * DSTG + 2 * AB + 2 * NACC + 2;
+    static_assert(DSTG % 2 == 0 && NACC % 2 == 0, "rings with one barrier per slot must be even-sized");
     static constexpr uint32_t oMisc = oBar + kNumBars * 8;
     static constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
     static_assert(TM_ACC + NACC * NM <= 512, "TMEM budget");
@@ -2298,6 +2315,7 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
     constexpr uint32_t kIdesc = idesc_f16_f32(128, C::NM);
     constexpr uint32_t kIdescTf32 = idesc_tf32_f32(128, N);
     constexpr int RSTG = C::RSTG, CSTG = C::CSTG, DSTG = C::DSTG, ABUF = C::ABUF, NACC = C::NACC;
+    constexpr int RB = C::RB, CB = C::CB, AB = C::AB;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -2309,19 +2327,19 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
     const int n = max(0, min(nsb, sb0 + p.sb_per_split) - sb0);
 
     const uint32_t bar0 = sbase + C::oBar;
-    auto raw_full = [&](int s) { return bar0 + 8u * s; };
-    auto raw_empty = [&](int s) { return bar0 + 8u * (RSTG + s); };
-    auto c_full = [&](int s) { return bar0 + 8u * (2 * RSTG + s); };
-    auto c_empty = [&](int s) { return bar0 + 8u * (2 * RSTG + CSTG + s); };
-    constexpr int kD = 2 * RSTG + 2 * CSTG;
+    auto raw_full = [&](int b) { return bar0 + 8u * b; };
+    auto raw_empty = [&](int b) { return bar0 + 8u * (RB + b); };
+    auto c_full = [&](int b) { return bar0 + 8u * (2 * RB + b); };
+    auto c_empty = [&](int b) { return bar0 + 8u * (2 * RB + CB + b); };
+    constexpr int kD = 2 * RB + 2 * CB;
     auto d_full = [&](int s) { return bar0 + 8u * (kD + s); };
     auto d_empty = [&](int s) { return bar0 + 8u * (kD + DSTG + s); };
     auto bmin_full = [&](int s) { return bar0 + 8u * (kD + 2 * DSTG + s); };
     constexpr int kA = kD + 3 * DSTG;
     auto a_full = [&](int b) { return bar0 + 8u * (kA + b); };
-    auto a_empty = [&](int b) { return bar0 + 8u * (kA + ABUF + b); };
-    auto acc_full = [&](int a) { return bar0 + 8u * (kA + 2 * ABUF + a); };
-    auto acc_empty = [&](int a) { return bar0 + 8u * (kA + 2 * ABUF + NACC + a); };
+    auto a_empty = [&](int b) { return bar0 + 8u * (kA + AB + b); };
+    auto acc_full = [&](int a) { return bar0 + 8u * (kA + 2 * AB + a); };
+    auto acc_empty = [&](int a) { return bar0 + 8u * (kA + 2 * AB + NACC + a); };
     auto done = [&](int e) { return bar0 + 8u * (C::kNumBars - 2 + e); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::oMisc);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + C::oMisc + 4);
@@ -2329,9 +2347,9 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
     // the producer's copies: raw weights and q8_1 scale words of unit i;
     // activation chunk j (64 k of unit j/4, hi and lo planes)
     auto issue_raw = [&](int i) {
-        const int rs = i % RSTG;
-        mbar_arrive_expect_tx(raw_full(rs), RAW_BYTES);
-        tma_load_2d(sbase + C::oRaw + rs * RAW_BYTES, &tmW, raw_full(rs), (sb0 + i) * 144, tile * 128);
+        const int rs = i % RSTG, rb = i % RB;
+        mbar_arrive_expect_tx(raw_full(rb), RAW_BYTES);
+        tma_load_2d(sbase + C::oRaw + rs * RAW_BYTES, &tmW, raw_full(rb), (sb0 + i) * 144, tile * 128);
     };
     auto issue_ds = [&](int i) {
         const int dsl = i % DSTG;
@@ -2341,29 +2359,29 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
     auto issue_chunk = [&](int j) {
         // a box of the activation planes viewed as [K/64 chunks][2 planes][T rows][64 k]:
         // lands as [hi rows 0..N-1, lo rows 0..N-1] (rows past T zero)
-        const int cs = j % CSTG;
-        mbar_arrive_expect_tx(c_full(cs), C::CH_BYTES);
-        tma_load_4d(sbase + C::oX + cs * C::CH_BYTES, &tmX, c_full(cs), 0, 0, 0, sb0 * 4 + j);
+        const int cs = j % CSTG, cb = j % CB;
+        mbar_arrive_expect_tx(c_full(cb), C::CH_BYTES);
+        tma_load_4d(sbase + C::oX + cs * C::CH_BYTES, &tmX, c_full(cb), 0, 0, 0, sb0 * 4 + j);
     };
 
     if (threadIdx.x == 0) {
         tma_prefetch(&tmX);
         tma_prefetch(&tmW);
         tma_prefetch(&tmD);
-        for (int s = 0; s < RSTG; ++s) {
-            mbar_init(raw_full(s), 1);
-            mbar_init(raw_empty(s), 4);       // the four unpack warps of one group
+        for (int b = 0; b < RB; ++b) {
+            mbar_init(raw_full(b), 1);
+            mbar_init(raw_empty(b), 4);       // the four unpack warps of one group
         }
-        for (int s = 0; s < CSTG; ++s) {
-            mbar_init(c_full(s), 1);
-            mbar_init(c_empty(s), 1);         // the issuer's commit
+        for (int b = 0; b < CB; ++b) {
+            mbar_init(c_full(b), 1);
+            mbar_init(c_empty(b), 1);         // the issuer's commit
         }
         for (int s = 0; s < DSTG; ++s) {
             mbar_init(d_full(s), 1);
             mbar_init(d_empty(s), 1);         // the issuer's commit (after the helper is done)
             mbar_init(bmin_full(s), 1);       // the helper warp
         }
-        for (int b = 0; b < ABUF; ++b) {
+        for (int b = 0; b < AB; ++b) {
             mbar_init(a_full(b), 4);
             mbar_init(a_empty(b), 1);
         }
@@ -2396,7 +2414,9 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
         int n_r = min(n, 1), n_d = min(n, 1), n_c = min(4 * n, 4);
         bool ok = true;
         for (int i = 1; i < n && ok; ++i) {
-            ok = mbar_wait_warp(raw_empty(i % RSTG), ((i / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
+            // a slot is free once the unit RSTG before (the chunk CSTG before) has released it
+            ok = i < RSTG ||
+                 mbar_wait_warp(raw_empty((i - RSTG) % RB), ((i - RSTG) / RB) & 1, abort_flag, kKid, SITE_P_RAW);
             if (!ok) break;
             if (lane == 0) issue_raw(i);
             ++n_r;
@@ -2405,7 +2425,8 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
             if (lane == 0) issue_ds(i);
             ++n_d;
             for (int j = 4 * i; j < 4 * i + 4 && ok; ++j) {
-                ok = mbar_wait_warp(c_empty(j % CSTG), ((j / CSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_STAGE);
+                ok = j < CSTG ||
+                     mbar_wait_warp(c_empty((j - CSTG) % CB), ((j - CSTG) / CB) & 1, abort_flag, kKid, SITE_P_STAGE);
                 if (!ok) break;
                 if (lane == 0) issue_chunk(j);
                 ++n_c;
@@ -2413,9 +2434,9 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
         }
         if (!ok && lane == 0) {
             // let copies already in flight land before the CTA exits
-            for (int i = max(0, n_r - RSTG); i < n_r; ++i) wait_drain(raw_full(i % RSTG), (i / RSTG) & 1);
+            for (int i = max(0, n_r - RSTG); i < n_r; ++i) wait_drain(raw_full(i % RB), (i / RB) & 1);
             for (int i = max(0, n_d - DSTG); i < n_d; ++i) wait_drain(d_full(i % DSTG), (i / DSTG) & 1);
-            for (int j = max(0, n_c - CSTG); j < n_c; ++j) wait_drain(c_full(j % CSTG), (j / CSTG) & 1);
+            for (int j = max(0, n_c - CSTG); j < n_c; ++j) wait_drain(c_full(j % CB), (j / CB) & 1);
         }
         __syncwarp();
     } else if (warp == 1 || warp == 2) {
@@ -2424,13 +2445,13 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
             const int e = warp - 1;
             bool ok = true;
             for (int i = e; i < n && ok; i += 2) {
-                const int buf = i % ABUF, dsl = i % DSTG, acc = i % NACC;
+                const int buf = i % ABUF, ab = i % AB, dsl = i % DSTG, acc = i % NACC;
                 // every wait of the unit before its first MMA: a wait of the issuing
                 // thread queues behind that thread's MMAs still in flight
-                ok = mbar_wait(a_full(buf), (i / ABUF) & 1, abort_flag, kKid, SITE_M_A) &&
+                ok = mbar_wait(a_full(ab), (i / AB) & 1, abort_flag, kKid, SITE_M_A) &&
                      mbar_wait(acc_empty(acc), ((i / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC);
                 for (int c = 0; c < 4 && ok; ++c)
-                    ok = mbar_wait(c_full((4 * i + c) % CSTG), ((4 * i + c) / CSTG) & 1, abort_flag, kKid, SITE_M_B);
+                    ok = mbar_wait(c_full((4 * i + c) % CB), ((4 * i + c) / CB) & 1, abort_flag, kKid, SITE_M_B);
                 ok = ok && mbar_wait(bmin_full(dsl), (i / DSTG) & 1, abort_flag, kKid, SITE_E_SDS);
                 if (!ok) break;
                 tc_fence_after();
@@ -2451,9 +2472,9 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
                 umma_tf32(d_acc, am, bm + (256 >> 4), kIdescTf32, 1u);
                 umma_tf32(d_acc, am + (256 >> 4), bm, kIdescTf32, 1u);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) umma_commit(c_empty((4 * i + c) % CSTG));
+                for (int c = 0; c < 4; ++c) umma_commit(c_empty((4 * i + c) % CB));
                 umma_commit(acc_full(acc));
-                umma_commit(a_empty(buf));
+                umma_commit(a_empty(ab));
                 umma_commit(d_empty(dsl));
             }
             umma_commit(done(e));
@@ -2497,7 +2518,7 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
         bool ok = true;
         for (int i = g; i < n && ok; i += 2) {
             const int rs = i % RSTG, buf = i % ABUF;
-            ok = mbar_wait_warp(raw_full(rs), (i / RSTG) & 1, abort_flag, kKid, SITE_U_RAW);
+            ok = mbar_wait_warp(raw_full(i % RB), (i / RB) & 1, abort_flag, kKid, SITE_U_RAW);
             if (!ok) break;
             uint4 cur[9];
             const uint4 *raw = reinterpret_cast<const uint4 *>(smem + C::oRaw + rs * RAW_BYTES + r * 144);
@@ -2505,7 +2526,7 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
             for (int k = 0; k < 9; ++k) cur[k] = raw[k];
             fence_proxy_async_smem();   // these reads before the next TMA write into the slot
             __syncwarp();
-            if (lane == 0) mbar_arrive(raw_empty(rs));
+            if (lane == 0) mbar_arrive(raw_empty(i % RB));
             const bool d_zero = (cur[0].x & 0x7FFFu) == 0u;
             const float d = __half2float(__ushort_as_half((unsigned short)(cur[0].x & 0xFFFFu)));
             const float dmin = __half2float(__ushort_as_half((unsigned short)(cur[0].x >> 16)));
@@ -2521,7 +2542,9 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
                 bh[j] = to_tf32(v);
                 bl[j] = to_tf32(v - bh[j]);
             }
-            ok = mbar_wait_warp(a_empty(buf), ((i / ABUF) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
+            // TMEM buffer buf is free once unit i - ABUF's MMAs have completed
+            ok = i < ABUF ||
+                 mbar_wait_warp(a_empty((i - ABUF) % AB), ((i - ABUF) / AB) & 1, abort_flag, kKid, SITE_U_STAGE);
             if (!ok) break;
             tc_fence_after();
             const uint32_t acol = tmem_base + lane_off + C::TM_A + buf * 128;
@@ -2553,7 +2576,7 @@ __global__ void __launch_bounds__(wts::NTHREADS, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(a_full(buf));
+            if (lane == 0) mbar_arrive(a_full(i % AB));
         }
     } else if (warp >= WT_EPI0) {
         // --------------------------------------------------------- epilogue --
