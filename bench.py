@@ -15,7 +15,9 @@ Headline `value` is TMAC/s over the step (all GEMM MACs / step time, the
 quantisations included in the time), measured on the device with CUDA
 events around K replays of a CUDA graph of the step.  `e2e` repeats the
 measurement through host buffers: each step copies its activations from
-pinned host memory and reads the seven outputs of the last layer back.
+pinned host memory and reads the last layer's GEMM outputs back, the copies
+on two copy streams overlapping the compute of the neighbouring steps
+(device inputs and outputs double-buffered).
 
 `--impl reference` times the CPU oracle (plain C, one thread) on a bounded
 sample of the same workload: full q8_1 quantisation of the four inputs and
@@ -380,20 +382,24 @@ def mmq_arm(args):
     launches_per_step = args.layers * (len(xs) + len(groups))
 
     ext_events = None   # per-launch events of the q4_K GEMMs, recorded inside the graph
+    # Events are recorded around the q4_K launches of every EV_STRIDE-th layer
+    # only: each event node in the graph adds a few microseconds between its
+    # neighbouring kernels, and the sampled layers are identical in shape.
+    EV_STRIDE = 8
 
-    def run_gemm(g, lw):
+    def run_gemm(g, lw, yb=None):
         _, ds, _, xa = qbuf[g.x_seed]
-        ops.gemm(g.fmt, lw[g.name], xa, ds, g.O, out=ybuf[g.name])
+        ops.gemm(g.fmt, lw[g.name], xa, ds, g.O, out=(yb if yb is not None else ybuf)[g.name])
 
-    def step(record=None):
+    def step(record=None, xd=None, yb=None):
         for li, lw in enumerate(layers):
-            for s, x in x_dev.items():
+            for s, x in (xd if xd is not None else x_dev).items():
                 ops.quantize_q8_1(x, out=qbuf[s])
             for gi, g in enumerate(groups):
                 ev = record[li][gi] if record is not None else None
                 if ev is not None:
                     ev[0].record()
-                run_gemm(g, lw)
+                run_gemm(g, lw, yb)
                 if ev is not None:
                     ev[1].record()
 
@@ -408,8 +414,9 @@ def mmq_arm(args):
     if not args.no_graph:
         try:
             ext_events = [[(torch.cuda.Event(enable_timing=True, external=True),
-                            torch.cuda.Event(enable_timing=True, external=True)) if g.fmt == "q4_K" else None
-                           for g in groups] for _ in layers]
+                            torch.cuda.Event(enable_timing=True, external=True))
+                           if g.fmt == "q4_K" and li % EV_STRIDE == 0 else None
+                           for g in groups] for li in range(len(layers))]
         except TypeError:
             ext_events = None
         graph = torch.cuda.CUDAGraph()
@@ -473,7 +480,8 @@ def mmq_arm(args):
                         sq_ms += ms
                         sq_macs += g.macs
                         n_sq += 1
-        kernel_timing = "events in the captured graph (last replay of the timed region)"
+        kernel_timing = (f"events in the captured graph around the q4_K launches of every {EV_STRIDE}th layer "
+                         "(last replay of the timed region)")
     if sq_ms <= 0.0:
         pairs = []
         for lw in layers:
@@ -497,27 +505,82 @@ def mmq_arm(args):
     int8_peak = ops.tensor_peak_tmacs("int8", dev)
 
     # ---------------- end to end through host buffers
+    # Every step copies its inputs from pinned host memory and its outputs back.
+    # The copies run on two copy streams, pipelined with the compute stream
+    # (inputs and outputs double-buffered, one captured graph per buffer set):
+    # step i+1's inputs and step i-1's outputs move while step i computes.
     e2e = None
     if not args.no_e2e:
         hx = {s: torch.from_numpy(x).pin_memory() for s, x in xs.items()}
         hy = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in ybuf.items()}
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
         d2h = sum(t.numel() * t.element_size() for t in hy.values())
+        x_sets = [x_dev, {s: t.clone() for s, t in x_dev.items()}]
+        y_sets = [ybuf, {n: t.clone() for n, t in ybuf.items()}]
+        e2e_graphs = None
+        if graph is not None:
+            e2e_graphs = []
+            for k in range(2):
+                gk = torch.cuda.CUDAGraph()
+                sk = torch.cuda.Stream(device=dev)
+                sk.wait_stream(torch.cuda.current_stream(dev))
+                with torch.cuda.stream(sk):
+                    with torch.cuda.graph(gk, stream=sk):
+                        step(None, x_sets[k], y_sets[k])
+                torch.cuda.current_stream(dev).wait_stream(sk)
+                e2e_graphs.append(gk)
+            torch.cuda.synchronize()
+
+        def run_set(k):
+            if e2e_graphs is not None:
+                e2e_graphs[k].replay()
+            else:
+                step(None, x_sets[k], y_sets[k])
+
+        up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev = lambda: torch.cuda.Event()
+        comp_ev, d2h_ev, h2d_ev = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        run_set(0)
+        run_set(1)
         torch.cuda.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(cur)
-        for _ in range(args.steps):
-            for s in x_dev:
-                x_dev[s].copy_(hx[s], non_blocking=True)
-            run_step()
-            for n in ybuf:
-                hy[n].copy_(ybuf[n], non_blocking=True)
-        f1.record(cur)
+        up.wait_stream(cur)
+        down.wait_stream(cur)
+
+        def issue_h2d(i):
+            k = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(comp_ev[k])            # step i-2 has read this input set
+                for s in x_sets[k]:
+                    x_sets[k][s].copy_(hx[s], non_blocking=True)
+                h2d_ev[k].record(up)
+
+        issue_h2d(0)
+        for i in range(args.steps):
+            k = i % 2
+            if i + 1 < args.steps:
+                issue_h2d(i + 1)
+            cur.wait_event(h2d_ev[k])
+            if i >= 2:
+                cur.wait_event(d2h_ev[k])                # step i-2's outputs are out
+            run_set(k)
+            comp_ev[k].record(cur)
+            with torch.cuda.stream(down):
+                down.wait_event(comp_ev[k])
+                for n in y_sets[k]:
+                    hy[n].copy_(y_sets[k][n], non_blocking=True)
+                d2h_ev[k].record(down)
+        f1.record(down)
         torch.cuda.synchronize()
         e2e_ms = f0.elapsed_time(f1)
         e2e = {"value": step_macs * args.steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TMAC/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms / args.steps}
+               "ms_per_step": e2e_ms / args.steps,
+               "copies": "pinned host buffers; H2D and D2H on two copy streams pipelined with the "
+                         "compute stream (double-buffered device inputs/outputs)"}
+        ops.check_status(dev)
 
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)

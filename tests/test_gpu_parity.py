@@ -336,6 +336,54 @@ def test_gemm_repeatable(ops):
     assert torch.equal(y1, y2) and torch.equal(z1, z2) and torch.equal(v1, v2)
 
 
+def test_pipelines_repeatable_under_graph_replay(ops):
+    """Many back-to-back launches of the production q4_K GEMM and of the
+    small-T GEMM (tiles of 16, 32 and 64 tokens), replayed from a CUDA graph
+    with timing events between the launches: no pipeline wait may give up and
+    every launch must reproduce the first result bit for bit (the kernels
+    fix their accumulation order).  Guards the barrier-phase bookkeeping of
+    the rings shared by alternating MMA issuers."""
+    g = synth.config(1).gemms[0]
+    w = _dev(g.weights())
+    _, ds, _, xa = ops.quantize_q8_1(_dev(g.x()))
+    cases = [(w, xa, ds, g.O, ops.gemm("q4_K", w, xa, ds, g.O), "prod")]
+    for i, T in enumerate((16, 32, 64)):
+        ws = _dev(synth.make_q4K(1024, 4096, 40 + i))
+        _, dss, _, xas = ops.quantize_q8_1(_dev(synth.make_x(T, 4096, 50 + i)))
+        cases.append((ws, xas, dss, 1024, ops.gemm_small(ws, xas, dss, 1024), "small"))
+    outs = [[torch.empty_like(c[4]) for _ in range(4)] for c in cases]
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2 * len(cases) * 4)]
+
+    def body():
+        e = 0
+        for j in range(4):
+            for c, o in zip(cases, outs):
+                evs[e].record()
+                if c[5] == "prod":
+                    ops.gemm("q4_K", c[0], c[1], c[2], c[3], out=o[j])
+                else:
+                    ops.gemm_small(c[0], c[1], c[2], c[3], out=o[j])
+                evs[e + 1].record()
+                e += 2
+
+    body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(graph, stream=st):
+            body()
+    torch.cuda.current_stream().wait_stream(st)
+    for r in range(200):
+        graph.replay()
+        if r % 50 == 49:
+            torch.cuda.synchronize()
+            ops.check_status()
+            for c, o in zip(cases, outs):
+                assert all(torch.equal(c[4], oj) for oj in o), c[5]
+
+
 def test_gpu_argument_errors(ops):
     from quantized_prefill_gemm_mmq_gb300._lib import MMQError
     w = torch.zeros(144 * 2, dtype=torch.uint8, device="cuda")
