@@ -1031,9 +1031,12 @@ __global__ void __launch_bounds__(q4::NTHREADS, 1)
 // MMAs keep the pipe busy, and every accumulator still sees its MMAs in one
 // fixed order, so results are reproducible bit for bit.
 // Each stage has a single "full" barrier (TMA bytes of both activation
-// planes + the 128 unpack threads' arrivals) and a single "empty" barrier;
-// the unpack warps, which wait on "empty" anyway, take turns issuing the
-// stages' activation TMA (stage ks by unpack warp ks % 4).  Stage ks uses
+// planes + the 128 unpack threads' arrivals) and a single "empty" barrier.
+// The MMA issuers request the activation tiles: when an issuer has seen its
+// previous stage ks - 2 complete, the slot of stage ks + 1 is free, and it
+// issues that stage's TMA before its own stage ks, the earliest moment the
+// slot allows (an unpack warp, busy converting, would reach it later and put
+// the copy's latency on the critical path).  Stage ks uses
 // operand slot ks % STG but barriers ks % (2 STG): a parity wait can only
 // tell apart phases one apart, so every waiter must see each phase of the
 // barriers it waits on.  With one barrier per slot and an odd ring, stages
@@ -1046,8 +1049,8 @@ __global__ void __launch_bounds__(q4::NTHREADS, 1)
 // start of a super-block and release the raw slot at once.
 // TMEM: [0,256) even-stage accumulators, [256,512) odd-stage accumulators,
 // two super-blocks each (rotating).
-// Warps: 1 and 14 MMA issuers (even / odd stages), 2-5 unpack (+ TMA), 6-13
-// epilogue, 0 and 15 scale.
+// Warps: 1 and 14 MMA issuers (even / odd stages; + activation TMA), 2-5
+// unpack (+ raw weight TMA), 6-13 epilogue, 0 and 15 scale.
 // =========================================================================
 namespace q4s {
 
@@ -1165,6 +1168,18 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         if (lane == 0) {
             const int me = warp == 1 ? 0 : 1;   // stages with ks % 2 == me
             bool ok = true;
+            // activation tiles of stage k: [2T][K] tensor, hi plane rows 0..T-1, lo plane rows T..2T-1
+            auto load_a = [&](int k) {
+                mbar_arrive_expect_tx(full(k % SBAR), A_STAGE);
+                tma_load_2d(stage_a(k % STG), &tmA, full(k % SBAR), (sb_base * 4 + k) * BK, t0);
+                tma_load_2d(stage_a(k % STG) + A_BYTES, &tmA, full(k % SBAR), (sb_base * 4 + k) * BK, T + t0);
+            };
+            int last_a = -1;   // last stage whose activation tiles this thread requested
+            if (me == 0) {
+                tma_prefetch(&tmA);
+                for (int k = 0; k < STG && k < nks; ++k) load_a(k);
+                last_a = min(STG, nks) - 1;
+            }
             for (int ks = me; ks < nks && ok; ks += 2) {
                 const int s = ks % STG, fb = ks % SBAR;
                 const int sb = ks >> 2, p4 = ks & 3, slot = sb % NACC;
@@ -1172,8 +1187,14 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 // are then queued in the tensor pipe (the other issuer's, executing, and this
                 // one), and the rest of the ring is free for loading.
                 const int n_mine = ks >> 1;   // stages this issuer has issued so far
-                ok = (n_mine == 0 || mbar_wait(done(me), (n_mine - 1) & 1, abort_flag, kKid, SITE_M_A)) &&
-                     mbar_wait(full(fb), (ks / SBAR) & 1, abort_flag, kKid, SITE_M_A) &&
+                ok = n_mine == 0 || mbar_wait(done(me), (n_mine - 1) & 1, abort_flag, kKid, SITE_M_A);
+                if (!ok) break;
+                // stage ks - 2 has completed, so the slot of stage ks + 1 is free
+                if (ks >= 2 && ks + 1 < nks) {
+                    load_a(ks + 1);
+                    last_a = ks + 1;
+                }
+                ok = mbar_wait(full(fb), (ks / SBAR) & 1, abort_flag, kKid, SITE_M_A) &&
                      (p4 > 1 || mbar_wait(acc_empty(slot), ((sb / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC));
                 if (!ok) break;
                 tc_fence_after();
@@ -1204,6 +1225,9 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             }
             umma_commit(mma_done);
             if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
+            if (!ok)   // let this thread's activation copies in flight land before the CTA exits
+                for (int i = max(0, last_a - 2 * STG + 1); i <= last_a; ++i)
+                    if (i < STG ? me == 0 : ((i - 1) & 1) == me) wait_drain(full(i % SBAR), (i / SBAR) & 1);
         }
         __syncwarp();
     } else if (warp >= UNPACK_WARP0 && warp < EPI_WARP0) {
@@ -1214,12 +1238,9 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         // into the swizzled B tile (zeros when the row's d is zero).  Thread 0
         // also issues the raw tile one super-block ahead.
         const int r = threadIdx.x - UNPACK_WARP0 * 32;
-        const bool tma_lane = (r & 31) == 0;
         bool ok = true;
-        int last_a = -1;   // last activation stage this thread issued
         int n_raw = 0;     // raw super-blocks requested (thread 0), for the drain on abort
         if (r == 0) {
-            tma_prefetch(&tmA);
             tma_prefetch(&tmW);
             mbar_arrive_expect_tx(r_full(0), RAW_BYTES);
             tma_load_2d(sbase + oRaw, &tmW, r_full(0), sb_base * 144, o0);
@@ -1271,13 +1292,6 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 ok = ks < STG ||
                      mbar_wait(empty((ks - STG) % SBAR), ((ks - STG) / SBAR) & 1, abort_flag, kKid, SITE_U_STAGE);
                 if (!ok) break;
-                if (tma_lane && (r >> 5) == (ks & 3)) {
-                    // the activation tensor is [2T][K]: hi plane rows 0..T-1, lo plane rows T..2T-1
-                    mbar_arrive_expect_tx(full(fb), A_STAGE);
-                    tma_load_2d(stage_a(s), &tmA, full(fb), (sb_base * 4 + ks) * BK, t0);
-                    tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(fb), (sb_base * 4 + ks) * BK, T + t0);
-                    last_a = ks;
-                }
                 uint8_t *brow = smem + oStage + s * STAGE_BYTES + A_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = vv[c];
@@ -1285,9 +1299,6 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 mbar_arrive(full(fb));
             }
         }
-        if (!ok && last_a >= 0)
-            for (int i = max(0, last_a - STG + 1); i <= last_a; ++i)
-                if ((i & 3) == (r >> 5)) wait_drain(full(i % SBAR), (i / SBAR) & 1);
         if (!ok && r == 0)
             for (int i = max(0, n_raw - RSTG); i < n_raw; ++i) wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
