@@ -1265,9 +1265,8 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                     n_raw = sb + 2;
                 }
             }
-#pragma unroll
-            for (int p4 = 0; p4 < 4; ++p4) {
-                const int ks = sb * 4 + p4, s = ks % STG, fb = ks % SBAR;
+            // the row's 64 values sc*q of stage p4 of this super-block as f16
+            auto convert = [&](int p4, uint4 (&vv)[8]) {
                 int sc_lo, sc_hi, unused;
                 q4::q4K_scale_min(cur[0].y, cur[0].z, cur[0].w, 2 * p4, sc_lo, unused);
                 q4::q4K_scale_min(cur[0].y, cur[0].z, cur[0].w, 2 * p4 + 1, sc_hi, unused);
@@ -1275,8 +1274,6 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 const float slo = d_zero ? 0.0f : (float)sc_lo, shi = d_zero ? 0.0f : (float)sc_hi;
                 const __half2 mlo = __float2half2_rn(slo), alo = __float2half2_rn(-1024.0f * slo);
                 const __half2 mhi = __float2half2_rn(shi * 0.0625f), ahi = __float2half2_rn(-64.0f * shi);
-                // convert before waiting for the slot: only the stores need it
-                uint4 vv[8];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 q = cur[1 + 2 * p4 + (c >> 1)];
@@ -1288,13 +1285,24 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                     vv[c + 4] = make_uint4(q4s::magic2(ha, 0x4140u, mhi, ahi), q4s::magic2(ha, 0x4342u, mhi, ahi),
                                            q4s::magic2(hb, 0x4140u, mhi, ahi), q4s::magic2(hb, 0x4342u, mhi, ahi));
                 }
+            };
+            // stage p4's values are converted before waiting for its slot, and
+            // stage p4 + 1's while stage p4's stores drain (before the proxy fence)
+            uint4 va[8], vb[8];
+            convert(0, va);
+#pragma unroll
+            for (int p4 = 0; p4 < 4; ++p4) {
+                const int ks = sb * 4 + p4, s = ks % STG, fb = ks % SBAR;
+                uint4 (&vc)[8] = (p4 & 1) ? vb : va;
+                uint4 (&vn)[8] = (p4 & 1) ? va : vb;
                 // slot s is free once stage ks - STG's MMAs have completed
                 ok = ks < STG ||
                      mbar_wait(empty((ks - STG) % SBAR), ((ks - STG) / SBAR) & 1, abort_flag, kKid, SITE_U_STAGE);
                 if (!ok) break;
                 uint8_t *brow = smem + oStage + s * STAGE_BYTES + A_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = vv[c];
+                for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = vc[c];
+                if (p4 < 3) convert(p4 + 1, vn);
                 fence_proxy_async_smem();
                 mbar_arrive(full(fb));
             }
