@@ -5,8 +5,9 @@
 // pair; "19 . r14 -- B fragments via ldmatrix", 3.2(d) for the packing):
 //   amax = max|x|, d32 = amax/127, q = clamp(round_half_away(x/d32), +-127),
 //   ssum = sum q, stored d = f16_rne(d32); all-zero block -> 0, 0, 0.
-// Both divisions are IEEE round-to-nearest (__fdiv_rn) so the result does
-// not depend on fast-math flags.
+// d32 is an IEEE round-to-nearest division (__fdiv_rn), and every quotient
+// x/d32 is rounded exactly as its IEEE division would be (round_quotient), so
+// the result does not depend on fast-math flags.
 //
 // Optional outputs: qs (int8 values), xh (the same values as f16, the integer
 // operand form) and xa (the dequantised activation f32(d16)*q as an exact
@@ -17,8 +18,7 @@
 // Layout: eight threads own one 32-block, four consecutive floats each
 // (one 16-byte load).  The block's amax and ssum are reduced across the
 // eight lanes with shuffles.  The kernel is a grid-stride loop over all
-// (t, b) blocks; it is purely bandwidth-bound (read 4 B, write up to
-// 3.125 B per element).
+// (t, b) blocks (read 4 B, write up to 5.125 B per element).
 #include <cuda_fp16.h>
 
 #include "mmq_host.h"
@@ -27,6 +27,22 @@ namespace mmq {
 namespace {
 
 constexpr int kThreads = 256;
+
+// round_half_away(x / d), the quotient rounded to f32 as IEEE division does,
+// without the division where the result cannot depend on it.  With
+// r = fl(1/d), z = fl(x * r) differs from the exact quotient y by at most
+// |y| * 2^-23 (two roundings), and the correctly rounded fl(y) from y by at
+// most |y| * 2^-24, so |z - fl(y)| < |y| * 2^-22 <= 3.1e-5 for |y| <= 127.5.
+// Unless z lies within 2^-14 (> that bound) of a half-integer, fl(y) is on
+// the same side of it and both round to the same integer; near a half-integer
+// (and when r is not a finite normal number) the quotient is taken exactly.
+__device__ __forceinline__ int round_quotient(float x, float d, float r)
+{
+    const float z = x * r;
+    const float a = fabsf(z);
+    if (r < 1e30f && a < 128.0f && fabsf(a - floorf(a) - 0.5f) > 0x1p-14f) return (int)roundf(z);
+    return (int)roundf(__fdiv_rn(x, d));
+}
 
 __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
     const float *__restrict__ x, int64_t ldx, int T, int K, int8_t *__restrict__ qs,
@@ -40,11 +56,13 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
     // every lane reaches every shuffle; lanes past the end only skip stores
     const int64_t warp_first = (((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5) * 4;
     const int64_t warp_step = ((int64_t)gridDim.x * kThreads >> 5) * 4;
+    // this lane's block blk = (token t, block b), advanced by warp_step blocks per
+    // iteration without a division
+    int64_t blk = warp_first + (lane >> 3);
+    int t = (int)(blk / nb), b = (int)(blk - (int64_t)t * nb);
+    const int step_t = (int)(warp_step / nb), step_b = (int)(warp_step - (int64_t)step_t * nb);
     for (int64_t base = warp_first; base < nblocks; base += warp_step) {
-        const int64_t blk = base + (lane >> 3);
         const bool live = blk < nblocks;
-        const int t = live ? (int)(blk / nb) : 0;
-        const int b = live ? (int)(blk - (int64_t)t * nb) : 0;
         const int k = b * 32 + sub * 4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live) v = __ldg(reinterpret_cast<const float4 *>(x + (int64_t)t * ldx + k));
@@ -55,20 +73,24 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
         float d32 = 0.0f;
         if (amax != 0.0f) {
             d32 = __fdiv_rn(amax, 127.0f);
-            q0 = (int)roundf(__fdiv_rn(v.x, d32));
-            q1 = (int)roundf(__fdiv_rn(v.y, d32));
-            q2 = (int)roundf(__fdiv_rn(v.z, d32));
-            q3 = (int)roundf(__fdiv_rn(v.w, d32));
-            q0 = min(127, max(-127, q0));
-            q1 = min(127, max(-127, q1));
-            q2 = min(127, max(-127, q2));
-            q3 = min(127, max(-127, q3));
+            const float r = __frcp_rn(d32);
+            q0 = min(127, max(-127, round_quotient(v.x, d32, r)));
+            q1 = min(127, max(-127, round_quotient(v.y, d32, r)));
+            q2 = min(127, max(-127, round_quotient(v.z, d32, r)));
+            q3 = min(127, max(-127, round_quotient(v.w, d32, r)));
         }
         int ssum = q0 + q1 + q2 + q3;
 #pragma unroll
         for (int m = 4; m >= 1; m >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m, 8);
+        const int64_t e = (int64_t)t * K + k, blk_here = blk;
+        blk += warp_step;
+        t += step_t;
+        b += step_b;
+        if (b >= nb) {
+            b -= nb;
+            ++t;
+        }
         if (!live) continue;
-        const int64_t e = (int64_t)t * K + k;
         if (qs) {
             const uint32_t packed = (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) |
                                     ((uint32_t)(uint8_t)q2 << 16) | ((uint32_t)(uint8_t)q3 << 24);
@@ -84,25 +106,23 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
         }
         const __half dh = __float2half_rn(d32);
         if (xa) {
+            // v = f32(d16) * q is exact in f32; hi = f16(v), lo = f16(v - hi), both exact
             const float df = __half2float(dh);
-            const int qv[4] = {q0, q1, q2, q3};
-            uint16_t hi[4], lo[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float v = df * (float)qv[i];              // exact in f32
-                const __half h = __float2half_rn(v);
-                hi[i] = __half_as_ushort(h);
-                lo[i] = __half_as_ushort(__float2half_rn(v - __half2float(h)));   // exact
-            }
+            const float2 v01 = make_float2(df * (float)q0, df * (float)q1);
+            const float2 v23 = make_float2(df * (float)q2, df * (float)q3);
+            const __half2 h01 = __float22half2_rn(v01), h23 = __float22half2_rn(v23);
+            const float2 b01 = __half22float2(h01), b23 = __half22float2(h23);
+            const __half2 l01 = __float22half2_rn(make_float2(v01.x - b01.x, v01.y - b01.y));
+            const __half2 l23 = __float22half2_rn(make_float2(v23.x - b23.x, v23.y - b23.y));
             uint2 hv, lv;
-            hv.x = (uint32_t)hi[0] | ((uint32_t)hi[1] << 16);
-            hv.y = (uint32_t)hi[2] | ((uint32_t)hi[3] << 16);
-            lv.x = (uint32_t)lo[0] | ((uint32_t)lo[1] << 16);
-            lv.y = (uint32_t)lo[2] | ((uint32_t)lo[3] << 16);
+            hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+            hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+            lv.x = *reinterpret_cast<const uint32_t *>(&l01);
+            lv.y = *reinterpret_cast<const uint32_t *>(&l23);
             *reinterpret_cast<uint2 *>(xa + e) = hv;
             *reinterpret_cast<uint2 *>(xa + (int64_t)T * K + e) = lv;
         }
-        if (sub == 0) ds[blk] = (uint32_t)__half_as_ushort(dh) | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
+        if (sub == 0) ds[blk_here] = (uint32_t)__half_as_ushort(dh) | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
     }
 }
 

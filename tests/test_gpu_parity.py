@@ -79,6 +79,32 @@ def test_quantize_special_blocks(ops, orc):
     assert np.array_equal(xa_np[0] + xa_np[1], orc.dequant_q8_1(qs_r, ds_r))
 
 
+def test_quantize_near_half_integers(ops, orc):
+    """Quotients x / d32 within ~2^-20 (relative) of half-integers, with block
+    scales that are not powers of two, and blocks of tiny scale (d32 subnormal):
+    the q8_1 codes and scale words must match the oracle's IEEE division and
+    half-away rounding bit for bit."""
+    rng = np.random.default_rng(7)
+    T, nb = 64, 64
+    x = np.zeros((T, nb * 32), np.float32)
+    for t in range(T):
+        for b in range(nb):
+            amax = np.float32(rng.uniform(0.01, 1000.0)) if t < T - 4 else np.float32(rng.uniform(1e-43, 1e-37))
+            d32 = np.float32(amax / np.float32(127.0))
+            n = rng.integers(-127, 127, 31).astype(np.float64) + 0.5
+            # half of the values inside the exact-division margin, half around it
+            eps = rng.integers(-16, 17, 31) * np.where(rng.random(31) < 0.5, 2.0 ** -24, 2.0 ** -16)
+            vals = (n * (1.0 + eps) * np.float64(d32)).astype(np.float32)
+            vals = np.clip(vals, -amax, amax)
+            blk = np.concatenate([[amax], vals]).astype(np.float32)
+            rng.shuffle(blk)
+            x[t, 32 * b:32 * b + 32] = blk
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    qs, ds, _, _ = _gpu_quant(ops, x)
+    assert np.array_equal(qs.cpu().numpy(), qs_r)
+    assert np.array_equal(_to_np_ds(ds), ds_r)
+
+
 def test_quantize_strided_rows(ops, orc):
     xfull = synth.make_x(50, 1024 + 64, 3)
     xt = _dev(xfull)[:, :1024]
