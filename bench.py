@@ -207,22 +207,29 @@ def small_t_lines(dev, hbm_gbs):
             copies = [w0] + [w0.clone() for _ in range(int(320e6 // w0.numel()))]
             n = 2 * len(copies)
             x = torch.from_numpy(g.x()).to(dev)
-            qs, ds, _, xa = ops.quantize_q8_1(x, want_xh=False)
+            qs, ds, xh, xa = ops.quantize_q8_1(x)
             y = torch.empty((g.T, g.O), dtype=torch.float32, device=dev)
             ks = ops.choose_ksplit(g.T, g.O, g.K)
             ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
             us_small = graph_time_us([lambda w=w: ops.gemm_small(w, xa, ds, g.O, out=y) for w in copies], n=n)
             us_imma = (graph_time_us([lambda w=w: ops.gemm_small_imma(w, qs, ds, g.O, out=y) for w in copies], n=n)
                        if g.T <= ops.SMALL_IMMA_T_MAX else None)
+            us_gemv = (graph_time_us([lambda w=w: ops.gemv(w, xh, ds, g.O, out=y) for w in copies], n=n)
+                       if g.T <= ops.GEMV_T_MAX else None)
             us_split = graph_time_us([lambda w=w: ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws, out=y)
                                       for w in copies], n=n)
             us_plain = graph_time_us([lambda w=w: ops.gemm("q4_K", w, xa, ds, g.O, out=y) for w in copies], n=n)
             nbytes = w0.numel() + g.T * g.K * 4 + g.T * g.K // 8 + g.T * g.O * 4   # W + xa + ds + Y
-            out.append({"T": g.T, "K": g.K, "O": g.O, "small_us": us_small, "small_imma_us": us_imma,
-                        "splitk_us": us_split, "ksplit": ks, "plain_us": us_plain,
-                        "small_tmacs": g.macs / (us_small * 1e-6) / 1e12,
-                        "small_gbs": nbytes / (us_small * 1e-6) / 1e9,
-                        "small_hbm_frac": nbytes / (us_small * 1e-6) / 1e9 / hbm_gbs})
+            line = {"T": g.T, "K": g.K, "O": g.O, "small_us": us_small, "small_imma_us": us_imma,
+                    "splitk_us": us_split, "ksplit": ks, "plain_us": us_plain,
+                    "small_tmacs": g.macs / (us_small * 1e-6) / 1e12,
+                    "small_gbs": nbytes / (us_small * 1e-6) / 1e9,
+                    "small_hbm_frac": nbytes / (us_small * 1e-6) / 1e9 / hbm_gbs}
+            if us_gemv is not None:
+                gbytes = w0.numel() + g.T * g.K * 2 + g.T * g.K // 8 + g.T * g.O * 4   # W + xh + ds + Y
+                line.update({"gemv_us": us_gemv, "gemv_gbs": gbytes / (us_gemv * 1e-6) / 1e9,
+                             "gemv_hbm_frac": gbytes / (us_gemv * 1e-6) / 1e9 / hbm_gbs})
+            out.append(line)
             del copies
     ops.check_status(dev)
     return out
@@ -624,7 +631,8 @@ def mmq_arm(args):
     small_t = None
     if not args.no_small_t and world == 1:
         small_t = {"kernel": "mmq_q4K_wt_kernel (mmq_gemm_q4K_small) vs mmq_q4K_small_kernel (int8 warp MMA), "
-                             "split-K (mmq_gemm_q4K_splitk) and one CTA per 128x128 tile (mmq_gemm_q4K)",
+                             "mmq_q4K_gemv_kernel (mmq_gemv_q4K, T <= 16), split-K (mmq_gemm_q4K_splitk) and one "
+                             "CTA per 128x128 tile (mmq_gemm_q4K)",
                    "timing": "CUDA-graph replay cycling through >320 MB of weight copies (HBM-resident), device "
                              "events, best of 5",
                    "bytes": "weights + xa (4 B/elem) + ds + y",

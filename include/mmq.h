@@ -171,6 +171,24 @@ int mmq_gemm_q4K_small_imma(const void *w, const int8_t *qs, const uint32_t *ds,
                             int T, int O, int K, mmq_stream_t stream);
 
 /*
+ * Decode-shaped q4_K product for 1 <= T <= 16 tokens, where the whole cost is
+ * reading W from HBM once.  The pages' per-sub-block form ("31 . r28", 2.3):
+ * for every 32-weight sub-block the exact integer dot C_b of the 4-bit
+ * quants with the int8 activations, folded in f32 as
+ * (dx*(d*sc))*C_b + (dx*ssum)*(-(dmin*m)).  The dots run on the f16 warp MMA
+ * with exact integer operands (every product and partial sum is an integer
+ * below 2^24); one CTA per 16 weight rows streams the rows' super-blocks
+ * through a shared-memory ring.
+ * xh: the int8 q8_1 values as f16 [T][K] and ds the scale words [T][K/32],
+ * both as written by mmq_quantize_q8_1.  y: f32 [T][O], overwritten.  Result
+ * as mmq_gemm_q4K up to f32 summation order; the same on every call.
+ * Allocates nothing.
+ * T <= 16 (MMQ_ERR_SHAPE above), other limits as mmq_gemm_q4K.
+ */
+int mmq_gemv_q4K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y,
+                 int T, int O, int K, mmq_stream_t stream);
+
+/*
  * mmq_gemm_q4K_splitk without caller scratch: this entry point allocates
  * nothing.  The partial sums and tile counters live in the library's own
  * statically allocated device arrays, 4 Mi f32 (16 MiB) of partial sums and

@@ -2982,3 +2982,7 @@ extern "C" int mmq_last_failure_info(int *info)
     for (int i = 0; i < 4; ++i) info[i] = g_last_failure[i];
     return MMQ_OK;
 }
+
+// decode-shaped q4_K product (mmq_gemv_q4K): in this unit for its bounded waits
+// and the status word
+#include "mmq_gemv.cuh"

@@ -147,6 +147,23 @@ def gemm_small_imma(w: torch.Tensor, qs: torch.Tensor, ds: torch.Tensor, O: int,
     return out
 
 
+GEMV_T_MAX = 16           # mmq_gemv_q4K
+
+
+def gemv(w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
+         out: torch.Tensor | None = None) -> torch.Tensor:
+    """Decode-shaped q4_K product for T <= 16 tokens from the f16 copies of the
+    int8 q8_1 values xh [T][K] and ds (per-sub-block integer dots on the f16
+    warp MMA); same result as gemm("q4_K") up to f32 summation order."""
+    T, K = _check_gemm_args("q4_K", w, xh, O, planes=1)
+    _check_ds(ds, T, K)
+    out = _out(out, T, O, xh.device)
+    with torch.cuda.device(xh.device):
+        st = load().mmq_gemv_q4K(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
+    _check("mmq_gemv_q4K", st)
+    return out
+
+
 def splitk_sizes(T: int, O: int, K: int, ksplit: int) -> tuple[int, int]:
     """(floats of partial-sum workspace, ints of tile counters) for a split-K q4_K GEMM."""
     pf, nc = ctypes.c_int64(0), ctypes.c_int64(0)

@@ -281,6 +281,58 @@ def test_gemm_small_t_imma(ops, orc, T, O, K):
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("T,O,K", [(1, 1, 256), (8, 256, 1024), (9, 131, 2816), (16, 200, 768), (3, 17, 512),
+                                   (16, 512, 4096), (5, 8, 11008), (1, 1000, 512), (12, 4096, 256), (7, 33, 3072)])
+def test_gemv(ops, orc, T, O, K):
+    """Decode-shaped kernel: one and two 8-token MMA tiles, ragged T and O
+    (token slots past T and rows past O), K from 1 to 43 super-blocks (fewer
+    super-blocks than ring stages, and more)."""
+    w = synth.make_weights("q4_K", O, K, seed=3 * T + O)
+    x = synth.make_x(T, K, seed=K + 5 * T, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q4_K", w, qs_r, ds_r, O)
+    _, ds, xh, _ = ops.quantize_q8_1(_dev(x), want_qs=False, want_xa=False)
+    y1 = ops.gemv(_dev(w), xh, ds, O)
+    y2 = ops.gemv(_dev(w), xh, ds, O)
+    ops.check_status()
+    assert _rel_err(y1.cpu().numpy(), ref) <= TOL
+    assert torch.equal(y1, y2)                       # fixed summation order
+
+
+@pytest.mark.parametrize("T", [1, 8, 16])
+def test_gemv_full_size_sampled(ops, orc, T):
+    """The token-sweep shapes (K = 4096 and 11008, O = 4096) at decode sizes."""
+    wl = synth.config(4, T)
+    rng = np.random.default_rng(5151 + T)
+    for g in wl.gemms:
+        x, w = g.x(), g.weights()
+        qs_r, ds_r = orc.quantize_q8_1(x)
+        _, ds, xh, _ = ops.quantize_q8_1(_dev(x), want_qs=False, want_xa=False)
+        y = ops.gemv(_dev(w), xh, ds, g.O)
+        ops.check_status()
+        ti, oi = _sample_points(rng, g.T, g.O)
+        ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
+        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
+        assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
+
+
+def test_gemv_closed_form_and_limits(ops):
+    """The closed-form super-block (exact 6,833,616), and T = 17 refused."""
+    from quantized_prefill_gemm_mmq_gb300._lib import MMQError
+    sc = [63, 1, 32, 17, 48, 5, 60, 33]
+    m = [0, 63, 16, 47, 31, 62, 2, 40]
+    q = np.array([(i % 32) % 16 for i in range(256)])
+    w = pack_q4K_block(1.0, 1.0, sc, m, q)
+    x = np.full((1, 256), 127.0, np.float32)
+    _, ds, xh, _ = ops.quantize_q8_1(_dev(x), want_qs=False, want_xa=False)
+    assert float(ops.gemv(_dev(w), xh, ds, 1)[0, 0]) == 6833616.0
+    x17 = synth.make_x(17, 256, seed=1)
+    _, ds17, xh17, _ = ops.quantize_q8_1(_dev(x17), want_qs=False, want_xa=False)
+    with pytest.raises(MMQError) as e:
+        ops.gemv(_dev(w), xh17, ds17, 1)
+    assert e.value.status == -1
+
+
 @pytest.mark.parametrize("T", [16, 64])
 def test_gemm_small_t_full_size_sampled(ops, orc, T):
     wl = synth.config(4, T)
@@ -470,7 +522,8 @@ def test_gemm_max_k(ops, orc):
     ys = [("production", ops.gemm("q4_K", wd, xa, ds, O)),
           ("splitk", ops.gemm_splitk(wd, xa, ds, O, ksplit=8)),
           ("small", ops.gemm_small(wd, xa, ds, O)),
-          ("small_imma", ops.gemm_small_imma(wd, qs, ds, O))]
+          ("small_imma", ops.gemm_small_imma(wd, qs, ds, O)),
+          ("gemv", ops.gemv(wd, xh, ds, O))]
     ops.check_status()
     _sampled_check(orc, "q4_K", w4, x, O, ys, seed=1)
     w6 = synth.make_weights("q6_K", O, K, seed=93)
@@ -484,11 +537,12 @@ def test_gemm_large_o(ops, orc):
     tile indexing and 64-bit offsets, sampled against the oracle."""
     T, O, K = 3, 1 << 18, 256
     x = synth.make_x(T, K, seed=94, outliers=True)
-    qs, ds, _, xa = _gpu_quant(ops, x)
+    qs, ds, xh, xa = _gpu_quant(ops, x)
     w = synth.make_weights("q4_K", O, K, seed=95)
     wd = _dev(w)
     ys = [("production", ops.gemm("q4_K", wd, xa, ds, O)),
           ("small", ops.gemm_small(wd, xa, ds, O)),
-          ("small_imma", ops.gemm_small_imma(wd, qs, ds, O))]
+          ("small_imma", ops.gemm_small_imma(wd, qs, ds, O)),
+          ("gemv", ops.gemv(wd, xh, ds, O))]
     ops.check_status()
     _sampled_check(orc, "q4_K", w, x, O, ys, seed=3)
