@@ -72,39 +72,35 @@ static_assert(2 * (Cfg<1>::SMEM + 1024) <= 233472 && 2 * (Cfg<2>::SMEM + 1024) <
 
 __device__ __forceinline__ float f16_bits(uint32_t b) { return __half2float(__ushort_as_half((unsigned short)b)); }
 
-// 6-bit scales and mins of sub-blocks 2p and 2p + 1 from the 12 packed bytes
-// (s0 = bytes 0-3, s1 = bytes 4-7, s2 = bytes 8-11; GGUF k-quant packing:
-// sub-block j < 4 keeps its scale / min in the low 6 bits of byte j / j + 4;
-// j >= 4 takes its low 4 bits from the low / high nibble of byte j + 4 and
-// its high 2 bits from the top bits of byte j - 4 / j).  p is warp-uniform.
-__device__ __forceinline__ void pair_scales(uint32_t s0, uint32_t s1, uint32_t s2, int p, int (&sc)[2], int (&m)[2])
+// Exact float of an integer 0 <= v < 2^23 (v | 2^23 read as a float is 2^23 + v).
+__device__ __forceinline__ float small_u2f(uint32_t v) { return __int_as_float((int)(0x4B000000u | v)) - 8388608.0f; }
+// Exact float of the signed 16-bit value in the high half of w (2^23 + 2^22 + v
+// for |v| < 2^22 has the integer v in its low mantissa bits).
+__device__ __forceinline__ float hi16_s2f(uint32_t w)
 {
-    if (p < 2) {
-        const int b = 16 * p;
-        sc[0] = (s0 >> b) & 63;
-        sc[1] = (s0 >> (b + 8)) & 63;
-        m[0] = (s1 >> b) & 63;
-        m[1] = (s1 >> (b + 8)) & 63;
-    } else {
-        const int b = 16 * (p - 2);
-        sc[0] = ((s2 >> b) & 15) | (((s0 >> (b + 6)) & 3) << 4);
-        sc[1] = ((s2 >> (b + 8)) & 15) | (((s0 >> (b + 14)) & 3) << 4);
-        m[0] = ((s2 >> (b + 4)) & 15) | (((s1 >> (b + 6)) & 3) << 4);
-        m[1] = ((s2 >> (b + 12)) & 15) | (((s1 >> (b + 14)) & 3) << 4);
-    }
+    return __int_as_float(((int)w >> 16) + 0x4B400000) - 12582912.0f;
 }
 
-// {d*sc_2p, -(dmin*m_2p), d*sc_2p+1 / 16, -(dmin*m_2p+1)} of one row from its
-// 16-byte block header (f16 d, f16 dmin, 12 scale bytes)
-__device__ __forceinline__ void row_scales(const uint4 &h, int p, float (&s)[4])
+// {d*sc_j (divided by 16 if j is odd), -(dmin*m_j)} of sub-block j = 2p + e of
+// one row from its 16-byte block header (f16 d, f16 dmin, 12 scale bytes in
+// the GGUF k-quant packing: sub-block j < 4 keeps its scale / min in the low 6
+// bits of byte j / j + 4; j >= 4 takes its low 4 bits from the low / high
+// nibble of byte j + 4 and its high 2 bits from the top bits of byte j - 4 /
+// j).  p is warp-uniform, e may differ between lanes.
+__device__ __forceinline__ float2 sub_scales(const uint4 &h, int p, int e)
 {
+    uint32_t sc, m;
+    if (p < 2) {
+        const int b = 16 * p + 8 * e;
+        sc = (h.y >> b) & 63u;
+        m = (h.z >> b) & 63u;
+    } else {
+        const int b = 16 * (p - 2) + 8 * e;
+        sc = ((h.w >> b) & 15u) | (((h.y >> (b + 6)) & 3u) << 4);
+        m = ((h.w >> (b + 4)) & 15u) | (((h.z >> (b + 6)) & 3u) << 4);
+    }
     const float d = f16_bits(h.x & 0xFFFFu), dmin = f16_bits(h.x >> 16);
-    int sc[2], m[2];
-    pair_scales(h.y, h.z, h.w, p, sc, m);
-    s[0] = d * (float)sc[0];
-    s[1] = -(dmin * (float)m[0]);
-    s[2] = d * (float)sc[1] * 0.0625f;
-    s[3] = -(dmin * (float)m[1]);
+    return make_float2(d * small_u2f(sc) * (e ? 0.0625f : 1.0f), -(dmin * small_u2f(m)));
 }
 
 // Quant bytes b0..b3 of one word -> f16 pairs {1024+lo(b0), 1024+lo(b1)},
@@ -195,18 +191,30 @@ __global__ void __launch_bounds__(gv::NTHREADS, 2)
         int slot = warp >> 2;
         uint32_t phase = 0u;
         for (int i = warp >> 2; i < nsb; i += GROUPS) {
-            if (!mbar_wait_warp(full0 + 8 * slot, phase, abort_flag, KID, SITE_U_STAGE)) break;
+            const bool landed = mbar_wait(full0 + 8 * slot, phase, abort_flag, KID, SITE_U_STAGE);
+            if (!__all_sync(0xffffffffu, landed)) break;
             const uint8_t *st = sm + slot * C::STAGE;
-            // rows g and g + 8: block header, and quant bytes 8 tig .. 8 tig + 7 of
-            // pair p; element e of either sub-block is byte e (low / high nibble),
-            // so word h holds elements 8 tig + 4h .. + 3: the lane's k of MMA half h
-            const uint4 hA = *reinterpret_cast<const uint4 *>(st + g * 144);
-            const uint4 hB = *reinterpret_cast<const uint4 *>(st + (g + 8) * 144);
+            // quant bytes 8 tig .. 8 tig + 7 of pair p in rows g and g + 8; element
+            // e of either sub-block is byte e (low / high nibble), so word h holds
+            // elements 8 tig + 4h .. + 3: the lane's k of MMA half h
             const uint2 wa = *reinterpret_cast<const uint2 *>(st + g * 144 + 16 + 32 * p + 8 * tig);
             const uint2 wb = *reinterpret_cast<const uint2 *>(st + (g + 8) * 144 + 16 + 32 * p + 8 * tig);
+            // scale terms of sub-blocks 2p, 2p + 1 in rows g and g + 8
+            const uint4 hA = *reinterpret_cast<const uint4 *>(st + g * 144);
+            const uint4 hB = *reinterpret_cast<const uint4 *>(st + (g + 8) * 144);
             float sA[4], sB[4];
-            row_scales(hA, p, sA);
-            row_scales(hB, p, sB);
+            {
+                const float2 a0 = sub_scales(hA, p, 0), a1 = sub_scales(hA, p, 1);
+                const float2 b0 = sub_scales(hB, p, 0), b1 = sub_scales(hB, p, 1);
+                sA[0] = a0.x;
+                sA[1] = a0.y;
+                sA[2] = a1.x;
+                sA[3] = a1.y;
+                sB[0] = b0.x;
+                sB[1] = b0.y;
+                sB[2] = b1.x;
+                sB[3] = b1.y;
+            }
             uint32_t la[2][2], ha[2][2], lb[2][2], hb[2][2];
             unpack_word(wa.x, la[0], ha[0]);
             unpack_word(wa.y, la[1], ha[1]);
@@ -222,10 +230,10 @@ __global__ void __launch_bounds__(gv::NTHREADS, 2)
                 const int t0 = 8 * n + 2 * tig;
                 const uint2 w0 = *reinterpret_cast<const uint2 *>(st + C::D_OFF + t0 * 32 + 8 * p);
                 const uint2 w1 = *reinterpret_cast<const uint2 *>(st + C::D_OFF + (t0 + 1) * 32 + 8 * p);
-                const float dxl0 = f16_bits(w0.x & 0xFFFFu), ssl0 = (float)((int)w0.x >> 16);
-                const float dxu0 = f16_bits(w0.y & 0xFFFFu), ssu0 = (float)((int)w0.y >> 16);
-                const float dxl1 = f16_bits(w1.x & 0xFFFFu), ssl1 = (float)((int)w1.x >> 16);
-                const float dxu1 = f16_bits(w1.y & 0xFFFFu), ssu1 = (float)((int)w1.y >> 16);
+                const float dxl0 = f16_bits(w0.x & 0xFFFFu), ssl0 = hi16_s2f(w0.x);
+                const float dxu0 = f16_bits(w0.y & 0xFFFFu), ssu0 = hi16_s2f(w0.y);
+                const float dxl1 = f16_bits(w1.x & 0xFFFFu), ssl1 = hi16_s2f(w1.x);
+                const float dxu1 = f16_bits(w1.y & 0xFFFFu), ssu1 = hi16_s2f(w1.y);
                 // c: rows (g, g+8) x tokens (t0, t0+1); starts at -1024*ssum
                 float cl[4] = {-1024.0f * ssl0, -1024.0f * ssl1, -1024.0f * ssl0, -1024.0f * ssl1};
                 mma_f16(cl, la[0][0], lb[0][0], la[0][1], lb[0][1], xl.x, xl.y);
