@@ -333,19 +333,22 @@ def reference_arm(args):
 
 def small_t_launches(T):
     """Three eager launches each of the small-T GEMM and of the split-K GEMM
-    per config-4 shape at T tokens."""
+    per config-4 shape at T tokens, and of the decode-shaped product for T <= 16."""
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     dev = torch.device("cuda", 0)
     for g in synth.config(4, T).gemms:
         w = torch.from_numpy(g.weights()).to(dev)
-        _, ds, _, xa = ops.quantize_q8_1(torch.from_numpy(g.x()).to(dev), want_qs=False, want_xh=False)
+        _, ds, xh, xa = ops.quantize_q8_1(torch.from_numpy(g.x()).to(dev), want_qs=False)
         ks = ops.choose_ksplit(g.T, g.O, g.K)
         ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
         for _ in range(3):
             ops.gemm_small(w, xa, ds, g.O)
         for _ in range(3):
             ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws)
+        if g.T <= ops.GEMV_T_MAX:
+            for _ in range(3):
+                ops.gemv(w, xh, ds, g.O)
     ops.check_status(dev)
     print(json.dumps({"small_t_launches": T, "status": "ok"}))
 
