@@ -11,19 +11,24 @@
 //     y += (dx_b * (d*sc_b)) * C_b + (dx_b * ssum_b) * (-(dmin*m_b)).
 //
 // GB300 design:
-//   * One CTA of four warps per 16 weight rows, the whole K range; two CTAs
-//     per SM.  A ring of 12 (T <= 8) or 8 (T <= 16) stages, one super-block
-//     column each, filled by three TMA copies per stage issued by one thread:
-//     the 16 rows' raw 144-byte blocks (one 2-D box), the tokens' 256
-//     activations (f16 copies of the int8 values) and their 8 scale words.
-//     Token rows past T and weight rows past O arrive zero-filled from the
-//     tensor maps' bounds, at no cost.  (Per-thread 16-byte cp.async copies
-//     of the same stages were measured first: their issue rate, not HBM,
-//     bounded the kernel, with the same time for L2-resident weights.)
-//   * Per stage each thread decodes at most a couple of (row, sub-block pair)
-//     scale records or (token, sub-block) activation records into shared
-//     memory; warp w then takes sub-block pair w (sub-blocks 2w, 2w+1) of the
-//     16 rows.
+//   * One CTA per 16 weight rows, the whole K range, two CTAs per SM; nine
+//     warps: one TMA producer (warp 8) and two groups of four consumer warps
+//     (warps 0-3 and 4-7) that take alternate super-blocks.
+//   * A ring of 12 (T <= 8) or 8 (T <= 16) stages, one super-block column
+//     each, filled by three TMA copies per stage: the 16 rows' raw 144-byte
+//     blocks (one 2-D box), the tokens' 256 activations (f16 copies of the
+//     int8 values) and their 8 scale words.  Token rows past T and weight
+//     rows past O arrive zero-filled from the tensor maps' bounds.  Each slot
+//     has a full barrier (the copies' bytes) and an empty barrier (the four
+//     consumer warps of its group); the ring length is a multiple of the
+//     group count, so each slot's barriers are waited on by one agent
+//     through consecutive phases.  No CTA-wide barrier inside the loop.
+//     (Per-thread 16-byte cp.async copies of the same stages, and TMA with a
+//     CTA barrier per stage, were measured first: both were bound by the
+//     per-stage chain, not by HBM.)
+//   * Consumer warp w takes sub-block pair p = w % 4 (sub-blocks 2p, 2p + 1)
+//     of the 16 rows; each lane decodes the scale terms of its two rows and
+//     the scale words of its two tokens itself.
 //   * The dots run on the f16 warp MMA (m16n8k16, f32 accumulate) with the
 //     weight rows on M and the tokens on N (one or two 8-token tiles).  The
 //     weight operand is 1024 + q (low nibbles) or 1024 + 16q (high nibbles),
@@ -33,9 +38,9 @@
 //     f32 accumulator is exact.  The accumulator starts at -1024*ssum, which
 //     removes the 1024 offset: the result is C_b (low) or 16*C_b (high; its
 //     scale d*sc/16 is pre-divided, an exact power-of-two scaling).
-//   * The four warps' partial sums are added in warp order (deterministic).
-//   * Every wait is bounded: a stage that does not arrive within the time
-//     limit records MMQ_ERR_TIMEOUT, all threads leave the loop together,
+//   * Each consumer warp adds its super-blocks in order and the eight warps'
+//     partial sums are added in warp order (deterministic).
+//   * Every wait is bounded: after a timeout all warps leave their loops,
 //     the copies still in flight are waited for (bounded) and nothing is
 //     stored.
 
