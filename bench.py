@@ -66,6 +66,25 @@ def dist_env():
     return rank, world, local
 
 
+def ranks_max_ms(values, device=None):
+    """Per-rank durations (ms) -> their maxima over the ranks of the default
+    process group (the slowest rank sets the job's time); unchanged for a
+    single process."""
+    import torch
+    import torch.distributed as dist
+    values = [float(v) for v in values]
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return values
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tmacs(macs_per_rank_step, steps, world, ms):
+    """Whole-job throughput: the MACs all ranks processed over the slowest rank's time."""
+    return macs_per_rank_step * steps * world / (ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -585,7 +604,7 @@ def mmq_arm(args):
         f1.record(down)
         torch.cuda.synchronize()
         e2e_ms = f0.elapsed_time(f1)
-        e2e = {"value": step_macs * args.steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TMAC/s",
+        e2e = {"value": job_tmacs(step_macs, args.steps, world, e2e_ms), "unit": "TMAC/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps,
                "copies": "pinned host buffers; H2D and D2H on two copy streams pipelined with the "
@@ -593,14 +612,11 @@ def mmq_arm(args):
         ops.check_status(dev)
 
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        slowest = ranks_max_ms([elapsed_ms] + ([e2e["ms_per_step"]] if e2e is not None else []), dev)
+        elapsed_ms = slowest[0]
         if e2e is not None:
-            t = torch.tensor([e2e["ms_per_step"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["ms_per_step"] = float(t.item())
-            e2e["value"] = step_macs * world / (e2e["ms_per_step"] * 1e-3) / 1e12
+            e2e["ms_per_step"] = slowest[1]
+            e2e["value"] = job_tmacs(step_macs, 1, world, e2e["ms_per_step"])
 
     if rank != 0:
         if world > 1:
@@ -609,7 +625,7 @@ def mmq_arm(args):
 
     peaks, peak_src = load_peaks()
     ms_step = elapsed_ms / args.steps
-    value = step_macs * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = job_tmacs(step_macs, args.steps, world, elapsed_ms)
     achieved = 2.0 * sq_macs / (sq_ms * 1e-3) / 1e12 if sq_ms > 0 else None
     # the q4_K launches are timed inside a long step: the sustained bf16 figure applies
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
