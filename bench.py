@@ -250,6 +250,21 @@ def small_t_lines(dev, hbm_gbs):
                              "gemv_hbm_frac": gbytes / (us_gemv * 1e-6) / 1e9 / hbm_gbs})
             out.append(line)
             del copies
+    # the decode-shaped q6_K product on the 7B attn_v shape (K = O = 4096)
+    for T in (1, 16):
+        w0 = torch.from_numpy(synth.make_weights("q6_K", 4096, 4096, 301)).to(dev)
+        copies = [w0] + [w0.clone() for _ in range(int(320e6 // w0.numel()))]
+        n = 2 * len(copies)
+        x = torch.from_numpy(synth.make_x(T, 4096, 302)).to(dev)
+        _, ds, xh, xa = ops.quantize_q8_1(x, want_qs=False)
+        y = torch.empty((T, 4096), dtype=torch.float32, device=dev)
+        us_gemv = graph_time_us([lambda w=w: ops.gemv(w, xh, ds, 4096, out=y, fmt="q6_K") for w in copies], n=n)
+        us_plain = graph_time_us([lambda w=w: ops.gemm("q6_K", w, xa, ds, 4096, out=y) for w in copies], n=n)
+        gbytes = w0.numel() + T * 4096 * 2 + T * 4096 // 8 + T * 4096 * 4   # W + xh + ds + Y
+        out.append({"fmt": "q6_K", "T": T, "K": 4096, "O": 4096, "gemv_us": us_gemv, "plain_us": us_plain,
+                    "gemv_gbs": gbytes / (us_gemv * 1e-6) / 1e9,
+                    "gemv_hbm_frac": gbytes / (us_gemv * 1e-6) / 1e9 / hbm_gbs})
+        del copies
     ops.check_status(dev)
     return out
 
@@ -651,7 +666,8 @@ def mmq_arm(args):
     if not args.no_small_t and world == 1:
         small_t = {"kernel": "mmq_q4K_wt_kernel (mmq_gemm_q4K_small) vs mmq_q4K_small_kernel (int8 warp MMA), "
                              "mmq_q4K_gemv_kernel (mmq_gemv_q4K, T <= 16), split-K (mmq_gemm_q4K_splitk) and one "
-                             "CTA per 128x128 tile (mmq_gemm_q4K)",
+                             "CTA per 128x128 tile (mmq_gemm_q4K); q6_K lines: mmq_q6K_gemv_kernel (mmq_gemv_q6K) "
+                             "vs the production q6_K GEMM",
                    "timing": "CUDA-graph replay cycling through >320 MB of weight copies (HBM-resident), device "
                              "events, best of 5",
                    "bytes": "weights + xa (4 B/elem) + ds + y",

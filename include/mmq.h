@@ -189,6 +189,21 @@ int mmq_gemv_q4K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y
                  int T, int O, int K, mmq_stream_t stream);
 
 /*
+ * Decode-shaped q6_K product for 1 <= T <= 16 tokens ("43 . r40", 5:
+ * w = d*sc_u*(q-32) on 16-weight sub-blocks u with signed 8-bit scales): for
+ * every sub-block the exact integer dot C16_u of (q-32) with the int8
+ * activations, folded in f32 as (dx_b*(d*sc_u))*C16_u, b = u/2 the q8_1
+ * block.  The dots run on the f16 warp MMA with exact integer operands; the
+ * 210-byte blocks are staged through 16-byte-aligned windows.
+ * w: O*(K/256)*210 bytes.  xh, ds: as for mmq_gemv_q4K.  y: f32 [T][O],
+ * overwritten.  Result as mmq_gemm_q6K up to f32 summation order; the same on
+ * every call.  Allocates nothing.
+ * T <= 16 (MMQ_ERR_SHAPE above), other limits as mmq_gemm_q6K.
+ */
+int mmq_gemv_q6K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y,
+                 int T, int O, int K, mmq_stream_t stream);
+
+/*
  * mmq_gemm_q4K_splitk without caller scratch: this entry point allocates
  * nothing.  The partial sums and tile counters live in the library's own
  * statically allocated device arrays, 4 Mi f32 (16 MiB) of partial sums and

@@ -29,6 +29,7 @@ SIGNATURES = {
     "mmq_gemm_q4K_small_imma": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q4K_small": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemv_q4K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_gemv_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q4K_splitk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "mmq_gemm_q4K_splitk_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "mmq_gemm_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),

@@ -2983,6 +2983,7 @@ extern "C" int mmq_last_failure_info(int *info)
     return MMQ_OK;
 }
 
-// decode-shaped q4_K product (mmq_gemv_q4K): in this unit for its bounded waits
+// decode-shaped q4_K and q6_K products (mmq_gemv_q4K, mmq_gemv_q6K): in this unit for their bounded waits
 // and the status word
 #include "mmq_gemv.cuh"
+#include "mmq_gemv_q6.cuh"

@@ -147,20 +147,21 @@ def gemm_small_imma(w: torch.Tensor, qs: torch.Tensor, ds: torch.Tensor, O: int,
     return out
 
 
-GEMV_T_MAX = 16           # mmq_gemv_q4K
+GEMV_T_MAX = 16           # mmq_gemv_q4K, mmq_gemv_q6K
 
 
 def gemv(w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
-         out: torch.Tensor | None = None) -> torch.Tensor:
-    """Decode-shaped q4_K product for T <= 16 tokens from the f16 copies of the
-    int8 q8_1 values xh [T][K] and ds (per-sub-block integer dots on the f16
-    warp MMA); same result as gemm("q4_K") up to f32 summation order."""
-    T, K = _check_gemm_args("q4_K", w, xh, O, planes=1)
+         out: torch.Tensor | None = None, fmt: str = "q4_K") -> torch.Tensor:
+    """Decode-shaped product for T <= 16 tokens from the f16 copies of the int8
+    q8_1 values xh [T][K] and ds (per-sub-block integer dots on the f16 warp
+    MMA), W in q4_K or q6_K; same result as gemm(fmt) up to f32 summation order."""
+    T, K = _check_gemm_args(fmt, w, xh, O, planes=1)
     _check_ds(ds, T, K)
     out = _out(out, T, O, xh.device)
+    fn = load().mmq_gemv_q4K if fmt == "q4_K" else load().mmq_gemv_q6K
     with torch.cuda.device(xh.device):
-        st = load().mmq_gemv_q4K(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
-    _check("mmq_gemv_q4K", st)
+        st = fn(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
+    _check(f"gemv({fmt})", st)
     return out
 
 

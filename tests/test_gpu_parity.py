@@ -316,6 +316,46 @@ def test_gemv_full_size_sampled(ops, orc, T):
         assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
 
 
+@pytest.mark.parametrize("T,O,K", [(1, 1, 256), (8, 256, 1024), (9, 131, 2816), (16, 200, 768), (3, 17, 512),
+                                   (16, 512, 4096), (5, 8, 11008), (1, 1000, 512), (12, 33, 3072), (2, 7, 256)])
+def test_gemv_q6K(ops, orc, T, O, K):
+    """Decode-shaped q6_K kernel: one and two 8-token tiles, ragged T and O, K
+    from 1 to 43 super-blocks; O*K/256*210 mod 16 takes the values 0, 2, 4, 8
+    and 14, so in most cases the buffer ends inside the last block's
+    16-byte-aligned window (its tail bytes copied one by one)."""
+    w = synth.make_weights("q6_K", O, K, seed=7 * T + O)
+    x = synth.make_x(T, K, seed=K + 11 * T, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q6_K", w, qs_r, ds_r, O)
+    _, ds, xh, _ = ops.quantize_q8_1(_dev(x), want_qs=False, want_xa=False)
+    y1 = ops.gemv(_dev(w), xh, ds, O, fmt="q6_K")
+    y2 = ops.gemv(_dev(w), xh, ds, O, fmt="q6_K")
+    ops.check_status()
+    assert _rel_err(y1.cpu().numpy(), ref) <= TOL
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_gemv_q6K_full_size_sampled(ops, orc, T):
+    """The 7B attn_v shape (q6_K, K = O = 4096) at decode sizes, full-range
+    int8 sub-block scales (-128..127) as well as the synthetic -64..63."""
+    rng = np.random.default_rng(6161 + T)
+    O, K = 4096, 4096
+    x = synth.make_x(T, K, seed=33 + T, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    _, ds, xh, _ = ops.quantize_q8_1(_dev(x), want_qs=False, want_xa=False)
+    w = synth.make_weights("q6_K", O, K, seed=34 + T)
+    wf = w.reshape(O, K // 256, 210).copy()
+    wf[: O // 2, :, 192:208] = rng.integers(0, 256, size=(O // 2, K // 256, 16), dtype=np.uint8)
+    for wt in (w, wf.reshape(w.shape)):
+        y = ops.gemv(_dev(wt), xh, ds, O, fmt="q6_K")
+        ops.check_status()
+        ti, oi = _sample_points(rng, T, O)
+        ref = orc.gemm_points("q6_K", wt, qs_r, ds_r, O, ti, oi)
+        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
+        assert _rel_err(got, ref) <= TOL, _rel_err(got, ref)
+
+
 def test_gemv_closed_form_and_limits(ops):
     """The closed-form super-block (exact 6,833,616), and T = 17 refused."""
     from quantized_prefill_gemm_mmq_gb300._lib import MMQError
@@ -528,8 +568,9 @@ def test_gemm_max_k(ops, orc):
     _sampled_check(orc, "q4_K", w4, x, O, ys, seed=1)
     w6 = synth.make_weights("q6_K", O, K, seed=93)
     y6 = ops.gemm("q6_K", _dev(w6), xa, ds, O)
+    y6v = ops.gemv(_dev(w6), xh, ds, O, fmt="q6_K")
     ops.check_status()
-    _sampled_check(orc, "q6_K", w6, x, O, [("q6_K production", y6)], seed=2)
+    _sampled_check(orc, "q6_K", w6, x, O, [("q6_K production", y6), ("q6_K gemv", y6v)], seed=2)
 
 
 def test_gemm_large_o(ops, orc):
