@@ -367,7 +367,8 @@ def reference_arm(args):
 
 def small_t_launches(T):
     """Three eager launches each of the small-T GEMM and of the split-K GEMM
-    per config-4 shape at T tokens, and of the decode-shaped product for T <= 16."""
+    per config-4 shape at T tokens, and of the decode-shaped products for
+    T <= 16 (q4_K on those shapes, q6_K on the attn_v shape)."""
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     dev = torch.device("cuda", 0)
@@ -383,6 +384,13 @@ def small_t_launches(T):
         if g.T <= ops.GEMV_T_MAX:
             for _ in range(3):
                 ops.gemv(w, xh, ds, g.O)
+    if T <= ops.GEMV_T_MAX:
+        # the decode-shaped q6_K product on the 7B attn_v shape (K = O = 4096)
+        w6 = torch.from_numpy(synth.make_weights("q6_K", 4096, 4096, 301)).to(dev)
+        _, ds, xh, _ = ops.quantize_q8_1(torch.from_numpy(synth.make_x(T, 4096, 302)).to(dev), want_qs=False,
+                                         want_xa=False)
+        for _ in range(3):
+            ops.gemv(w6, xh, ds, 4096, fmt="q6_K")
     ops.check_status(dev)
     print(json.dumps({"small_t_launches": T, "status": "ok"}))
 
