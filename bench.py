@@ -269,6 +269,39 @@ def small_t_lines(dev, hbm_gbs):
     return out
 
 
+def decode_line(dev, layers, groups, xs, hbm_gbs):
+    """Side measurement: one decode step (T = 1) of the whole layer stack through
+    the decode-shaped kernels: per layer the q8_1 quantisation of the four
+    one-token inputs and the seven projections (gate and up as one launch over
+    their concatenated rows), every layer's weights streamed from HBM; one
+    CUDA graph per three steps, device time per step (best of 5)."""
+    import torch
+    from quantized_prefill_gemm_mmq_gb300 import ops, synth
+    kk = {s: x.shape[1] for s, x in xs.items()}
+    x1 = {s: torch.from_numpy(synth.make_x(1, k, 900 + s)).to(dev) for s, k in kk.items()}
+    qb = {s: (None, torch.empty((1, k // 32), dtype=torch.int32, device=dev),
+              torch.empty((1, k), dtype=torch.float16, device=dev), None) for s, k in kk.items()}
+    yb = {g.name: torch.empty((1, g.O), dtype=torch.float32, device=dev) for g in groups}
+
+    def step():
+        for lw in layers:
+            for s, x in x1.items():
+                ops.quantize_q8_1(x, out=qb[s])
+            for g in groups:
+                _, ds, xh, _ = qb[g.x_seed]
+                ops.gemv(lw[g.name], xh, ds, g.O, out=yb[g.name], fmt=g.fmt)
+
+    us = graph_time_us(step, n=3)
+    ops.check_status(dev)
+    wbytes = sum(t.numel() for lw in layers for t in lw.values())
+    return {"kernels": "mmq_quantize_q8_1 + mmq_gemv_q4K / mmq_gemv_q6K", "tokens": 1, "layers": len(layers),
+            "us_per_step": us, "tok_s": 1e6 / us, "weight_bytes_per_step": wbytes,
+            "hbm_gbs": wbytes / (us * 1e-6) / 1e9, "hbm_frac": wbytes / (us * 1e-6) / 1e9 / hbm_gbs,
+            "launches_per_step": len(layers) * (len(x1) + len(groups)),
+            "timing": "CUDA-graph replay of 3 steps, device events, best of 5; weights from HBM (the stack "
+                      "exceeds L2)"}
+
+
 class LaunchGroup:
     """Projections run as one GEMM launch: members share the input and the
     format, the weight rows are concatenated and the output columns too."""
@@ -681,6 +714,9 @@ def mmq_arm(args):
                    "bytes": "weights + xa (4 B/elem) + ds + y",
                    "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
                    "lines": small_t_lines(dev, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))}
+    decode = None
+    if not args.no_small_t and world == 1:
+        decode = decode_line(dev, layers, groups, xs, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
     line = {
         "metric": METRIC,
         "value": value,
@@ -713,6 +749,7 @@ def mmq_arm(args):
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
         "small_t": small_t,
+        "decode": decode,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
