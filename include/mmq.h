@@ -183,6 +183,12 @@ int mmq_gemm_q4K_small_imma(const void *w, const int8_t *qs, const uint32_t *ds,
  * both as written by mmq_quantize_q8_1.  y: f32 [T][O], overwritten.  Result
  * as mmq_gemm_q4K up to f32 summation order; the same on every call.
  * Allocates nothing.
+ * Launched with programmatic stream serialisation: the kernel may start
+ * while the previous kernel on `stream` is still running and reads the first
+ * super-blocks of W before that kernel has completed (xh, ds and y are
+ * touched only after it has).  So W must not be written by the kernel
+ * launched immediately before on the same stream (weights written by a copy,
+ * or by any earlier kernel, are fine).  The same holds for mmq_gemv_q6K.
  * T <= 16 (MMQ_ERR_SHAPE above), other limits as mmq_gemm_q4K.
  */
 int mmq_gemv_q4K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y,

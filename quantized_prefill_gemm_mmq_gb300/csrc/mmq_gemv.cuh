@@ -120,6 +120,14 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&lo)[2], uint3
     hi[1] = (t8 & 0x00F000F0u) | 0x64006400u;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start its
+// launch now (its CTAs still wait for this grid to complete before reading
+// what it writes), and wait for the previous kernel in the stream to complete
+// with its writes visible.  Both are no-ops for a launch without the
+// programmatic-serialisation attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // D = A (16 x 16, f16, row) * B (16 x 8, f16, col) + D, f32
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                         uint32_t b1)
@@ -160,6 +168,7 @@ __global__ void __launch_bounds__(gv::NTHREADS, 2)
         }
         fence_mbar_init();
     }
+    pdl_launch_dependents();
     __syncthreads();
 
     int issued = 0;   // producer: stages issued
@@ -170,10 +179,25 @@ __global__ void __launch_bounds__(gv::NTHREADS, 2)
             tma_prefetch(&tmW);
             tma_prefetch(&tmX);
             tma_prefetch(&tmD);
-            int slot = 0;
+            // the weights do not depend on the previous kernel: the first ring's
+            // worth of weight copies go out before waiting for it, the
+            // activations and scale words after
+            const int first = nsb < C::S ? nsb : C::S;
+            for (int i = 0; i < first; ++i) {
+                const uint32_t bar = full0 + 8 * i;
+                mbar_arrive_expect_tx(bar, C::STAGE);
+                tma_load_2d(sbase + i * C::STAGE, &tmW, bar, i * 144, o0);
+            }
+            pdl_wait();
+            for (int i = 0; i < first; ++i) {
+                const uint32_t dst = sbase + i * C::STAGE, bar = full0 + 8 * i;
+                tma_load_2d(dst + C::X_OFF, &tmX, bar, i * 256, 0);
+                tma_load_2d(dst + C::D_OFF, &tmD, bar, i * 8, 0);
+            }
+            issued = first;
+            int slot = first == C::S ? 0 : first;
             for (; issued < nsb; ++issued) {
-                if (issued >= C::S &&
-                    !mbar_wait(empty0 + 8 * slot, (uint32_t)((issued / C::S - 1) & 1), abort_flag, KID, SITE_P_STAGE))
+                if (!mbar_wait(empty0 + 8 * slot, (uint32_t)((issued / C::S - 1) & 1), abort_flag, KID, SITE_P_STAGE))
                     break;
                 const uint32_t dst = sbase + slot * C::STAGE, bar = full0 + 8 * slot;
                 mbar_arrive_expect_tx(bar, C::STAGE);
@@ -296,7 +320,9 @@ __global__ void __launch_bounds__(gv::NTHREADS, 2)
         __syncthreads();
         return;
     }
-    // partial sums of the eight consumer warps, added in warp order
+    // partial sums of the eight consumer warps, added in warp order (y is
+    // written only once the previous kernel in the stream has completed)
+    pdl_wait();
     for (int i = tid; i < C::TOK * ROWS; i += NTHREADS) {
         const int t = i / ROWS, r = i % ROWS;
         if (t < T && o0 + r < O) {
@@ -336,9 +362,18 @@ int launch_gemv_nt(const void *w, const uint16_t *xh, const uint32_t *ds, float 
             return launch_status();
         attr_done[dev] = true;
     }
-    const dim3 grid((unsigned)((O + gv::ROWS - 1) / gv::ROWS));
-    mmq_q4K_gemv_kernel<NT><<<grid, gv::NTHREADS, C::SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(
-        tmW, tmX, tmD, y, T, O, K);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((O + gv::ROWS - 1) / gv::ROWS));
+    cfg.blockDim = dim3(gv::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // may overlap the previous kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mmq_q4K_gemv_kernel<NT>, tmW, tmX, tmD, y, T, O, K) != cudaSuccess)
+        return launch_status();
     return launch_status();
 }
 

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
         }
         fence_mbar_init();
     }
+    gv::pdl_launch_dependents();
     __syncthreads();
 
     int issued = 0;   // producer: stages issued
@@ -124,23 +125,21 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
             tma_prefetch(&tmX);
             tma_prefetch(&tmD);
         }
-        int slot = 0;
-        for (; issued < nsb; ++issued) {
-            if (issued >= C::S &&
-                !mbar_wait_warp(empty0 + 8 * slot, (uint32_t)((issued / C::S - 1) & 1), abort_flag, KID, SITE_P_RAW))
-                break;
-            const uint32_t dst = sbase + slot * C::STAGE, bar = full0 + 8 * slot;
+        // row lane's window of super-block i into the stage at dst, the lane's
+        // arrival on the stage's full barrier with its bytes (lane 0: also the
+        // activation and scale-word boxes, requested separately)
+        auto stage_w = [&](int i, uint32_t dst, uint32_t bar, uint8_t *dst_gen) {
             uint32_t mine = 0, sz = 0;
             uint64_t a = 0;
             if (lane < nrows) {
-                const uint64_t start = ((uint64_t)(o0 + lane) * nsb + issued) * 210;
+                const uint64_t start = ((uint64_t)(o0 + lane) * nsb + i) * 210;
                 a = start & ~15ull;
                 sz = WROW;
                 if (a + WROW > nbytes) {
                     // the buffer ends inside this window: bulk-copy its full
                     // 16-byte granules, the block's remaining bytes one by one
                     sz = (uint32_t)((nbytes - a) & ~15ull);
-                    uint8_t *drow = sm + slot * C::STAGE + lane * WROW;
+                    uint8_t *drow = dst_gen + lane * WROW;
                     for (uint64_t b = a + sz; b < start + 210; ++b) drow[b - a] = w[b];
                 }
                 mine = sz;
@@ -148,6 +147,26 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
             if (lane == 0) mine += C::TOK * 512 + C::TOK * 32;
             mbar_arrive_expect_tx(bar, mine);
             if (sz) bulk_load(dst + lane * WROW, w + a, sz, bar);
+        };
+        // the weights do not depend on the previous kernel: the first ring's
+        // worth of windows go out before waiting for it, the activations and
+        // scale words after
+        const int first = nsb < C::S ? nsb : C::S;
+        for (int i = 0; i < first; ++i) stage_w(i, sbase + i * C::STAGE, full0 + 8 * i, sm + i * C::STAGE);
+        gv::pdl_wait();
+        if (lane == 0)
+            for (int i = 0; i < first; ++i) {
+                const uint32_t dst = sbase + i * C::STAGE, bar = full0 + 8 * i;
+                tma_load_2d(dst + C::X_OFF, &tmX, bar, i * 256, 0);
+                tma_load_2d(dst + C::D_OFF, &tmD, bar, i * 8, 0);
+            }
+        issued = first;
+        int slot = first == C::S ? 0 : first;
+        for (; issued < nsb; ++issued) {
+            if (!mbar_wait_warp(empty0 + 8 * slot, (uint32_t)((issued / C::S - 1) & 1), abort_flag, KID, SITE_P_RAW))
+                break;
+            const uint32_t dst = sbase + slot * C::STAGE, bar = full0 + 8 * slot;
+            stage_w(issued, dst, bar, sm + slot * C::STAGE);
             if (lane == 0) {
                 tma_load_2d(dst + C::X_OFF, &tmX, bar, issued * 256, 0);
                 tma_load_2d(dst + C::D_OFF, &tmD, bar, issued * 8, 0);
@@ -247,6 +266,7 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
         __syncthreads();
         return;
     }
+    gv::pdl_wait();   // y is written only once the previous kernel in the stream has completed
     for (int i = tid; i < C::TOK * ROWS; i += NTHREADS) {
         const int t = i / ROWS, r = i % ROWS;
         if (t < T && o0 + r < O) {
@@ -281,9 +301,19 @@ int launch_gemv_q6_nt(const void *w, const uint16_t *xh, const uint32_t *ds, flo
             return launch_status();
         attr_done[dev] = true;
     }
-    const dim3 grid((unsigned)((O + gv6::ROWS - 1) / gv6::ROWS));
-    mmq_q6K_gemv_kernel<NT><<<grid, C::NTHREADS, C::SMEM, reinterpret_cast<cudaStream_t>(stream)>>>(
-        tmX, tmD, static_cast<const uint8_t *>(w), y, T, O, K);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((O + gv6::ROWS - 1) / gv6::ROWS));
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // may overlap the previous kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, mmq_q6K_gemv_kernel<NT>, tmX, tmD, static_cast<const uint8_t *>(w), y, T, O, K) !=
+        cudaSuccess)
+        return launch_status();
     return launch_status();
 }
 
