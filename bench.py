@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small-t", action="store_true", help="skip the small-T side measurement")
+    ap.add_argument("--decode-launches", action="store_true",
+                    help="only run one eager decode step (T = 1) of --layers layers through the decode-shaped "
+                         "kernels (for a launch list)")
     ap.add_argument("--small-t-launches", type=int, default=0, metavar="T",
                     help="only launch the small-T and the split-K GEMM of the config-4 shapes at T tokens three "
                          "times each (eager; for profiling) and exit")
@@ -428,6 +431,35 @@ def small_t_launches(T):
     print(json.dumps({"small_t_launches": T, "status": "ok"}))
 
 
+def decode_launches(args):
+    """One eager decode step (T = 1) of args.layers layers through the decode-shaped
+    kernels, as timed by the bench's decode line (after one warm-up step)."""
+    import numpy as np
+    import torch
+    from quantized_prefill_gemm_mmq_gb300 import ops, synth
+    dev = torch.device("cuda", 0)
+    wl, xs = build_inputs(args.tokens)
+    groups = launch_groups(wl)
+    host_w = {g.name: g.weights() for g in wl.gemms}
+    w_layer = {gr.name: torch.from_numpy(np.concatenate([host_w[m.name] for m in gr.members])).to(dev)
+               for gr in groups}
+    layers = [w_layer] + [{n: t.clone() for n, t in w_layer.items()} for _ in range(args.layers - 1)]
+    x1 = {s: torch.from_numpy(synth.make_x(1, x.shape[1], 900 + s)).to(dev) for s, x in xs.items()}
+    qb = {s: (None, torch.empty((1, x.shape[1] // 32), dtype=torch.int32, device=dev),
+              torch.empty((1, x.shape[1]), dtype=torch.float16, device=dev), None) for s, x in xs.items()}
+    yb = {g.name: torch.empty((1, g.O), dtype=torch.float32, device=dev) for g in groups}
+    for _ in range(2):
+        for lw in layers:
+            for s, x in x1.items():
+                ops.quantize_q8_1(x, out=qb[s])
+            for g in groups:
+                _, ds, xh, _ = qb[g.x_seed]
+                ops.gemv(lw[g.name], xh, ds, g.O, out=yb[g.name], fmt=g.fmt)
+    torch.cuda.synchronize()
+    ops.check_status(dev)
+    print(json.dumps({"decode_launches": args.layers, "status": "ok"}))
+
+
 def mmq_arm(args):
     import numpy as np
     import torch
@@ -437,6 +469,9 @@ def mmq_arm(args):
 
     if args.small_t_launches:
         small_t_launches(args.small_t_launches)
+        return
+    if args.decode_launches:
+        decode_launches(args)
         return
 
     rank, world, local = dist_env()
