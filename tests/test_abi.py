@@ -20,7 +20,7 @@ def test_header_declares_the_boundary():
                      "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K",
                      "mmq_gemm_q4K_splitk", "mmq_splitk_sizes", "mmq_gemm_q4K_splitk_static",
                      "mmq_gemm_q6K_subblock", "mmq_gemm_q4K_small", "mmq_gemm_q4K_small_imma",
-                     "mmq_last_failure_info"):
+                     "mmq_last_failure_info", "mmq_gemv_q4K", "mmq_gemv_q6K"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -37,7 +37,7 @@ def test_library_exports_every_header_symbol():
 @needs_lib
 def test_library_loads_and_reports():
     lib = _lib.load()
-    assert lib.mmq_version() == 6
+    assert lib.mmq_version() == 7
     assert lib.mmq_status_str(0) == b"ok"
     for code in range(-9, 0):
         assert lib.mmq_status_str(code) not in (b"", b"unknown status")
