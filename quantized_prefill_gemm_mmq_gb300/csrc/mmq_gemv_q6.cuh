@@ -34,18 +34,22 @@ namespace gv6 {
 
 constexpr int ROWS = 16;
 constexpr int KID = 13;               // kernel id in the status word
-constexpr int WROW = 224;             // staged window per row
 
 template <int NT>
 struct Cfg {
     static constexpr int TOK = 8 * NT;
+    // super-blocks per stage: two at T <= 8 (half the producer's copies per
+    // byte), one at T <= 16 (where the larger activation boxes leave room
+    // for fewer stages)
+    static constexpr int SB = NT == 1 ? 2 : 1;
+    static constexpr int WROW = SB == 2 ? 448 : 224;         // 16-byte-aligned window per row
     static constexpr int GROUPS = 2;
     static constexpr int CWARPS = 4 * GROUPS;
     static constexpr int NTHREADS = (CWARPS + 1) * 32;      // + the producer warp
-    static constexpr int X_OFF = ROWS * WROW;               // 3584: activations [TOK][256] f16
-    static constexpr int D_OFF = X_OFF + TOK * 512;         // scale words [TOK][8]
-    static constexpr int STAGE = D_OFF + TOK * 32;
-    static constexpr int S = 8;                             // ring stages, a multiple of GROUPS
+    static constexpr int X_OFF = ROWS * WROW;               // activations [SB][TOK][256] f16
+    static constexpr int D_OFF = X_OFF + SB * TOK * 512;    // scale words [TOK][8 SB]
+    static constexpr int STAGE = D_OFF + TOK * 32 * SB;
+    static constexpr int S = NT == 1 ? 6 : 8;               // ring stages, a multiple of GROUPS
     static constexpr int BAR_OFF = S * STAGE;               // S full, then S empty barriers
     static constexpr int ABORT_OFF = BAR_OFF + 16 * S;
     static constexpr int RED_OFF = ABORT_OFF + 16;          // [CWARPS][TOK][ROWS] f32
@@ -86,11 +90,13 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
     using namespace gv6;
     using C = Cfg<NT>;
     constexpr int GROUPS = C::GROUPS, CWARPS = C::CWARPS, NTHREADS = C::NTHREADS;
+    constexpr int SB = C::SB, WROW = C::WROW;
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = sm_raw + ((128u - (smem_u32(sm_raw) & 127u)) & 127u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int o0 = blockIdx.x * ROWS;
     const int nsb = K >> 8;
+    const int nst = (nsb + SB - 1) / SB;            // stages: SB super-blocks each (fewer at the end)
     const uint32_t sbase = smem_u32(sm);
     const uint32_t full0 = sbase + C::BAR_OFF;      // slot s: + 8 s (32 producer-lane arrivals + bytes)
     const uint32_t empty0 = full0 + 8 * C::S;       // slot s: + 8 s (its four consumer warps)
@@ -116,121 +122,130 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
         for (int i = 0; i < 4; ++i) acc[n][i] = 0.0f;
 
     if (warp == CWARPS) {
-        // producer: lane r < 16 stages row o0 + r's block of super-block i (the
-        // 224-byte window around it); lane 0 also the tokens' activations and
-        // scale words of k = 256 i .. 256 i + 255
+        // producer: stage j -> slot j % S holds super-blocks SB j .. SB j + SB - 1
+        // (fewer at the end of the row): lane r < 16 copies row o0 + r's window
+        // around them, lane 0 also requests the tokens' activations (one box
+        // per super-block) and scale words
         const int nrows = min(ROWS, O - o0);
         const uint64_t nbytes = (uint64_t)O * nsb * 210;
         if (lane == 0) {
             tma_prefetch(&tmX);
             tma_prefetch(&tmD);
         }
-        // row lane's window of super-block i into the stage at dst, the lane's
-        // arrival on the stage's full barrier with its bytes (lane 0: also the
-        // activation and scale-word boxes, requested separately)
-        auto stage_w = [&](int i, uint32_t dst, uint32_t bar, uint8_t *dst_gen) {
+        // row lane's window of stage j into the stage at dst, the lane's arrival
+        // on the stage's full barrier with its bytes (lane 0: also the boxes'
+        // bytes; the boxes are requested separately)
+        auto stage_w = [&](int j, uint32_t dst, uint32_t bar, uint8_t *dst_gen) {
+            const int nb = min(SB, nsb - SB * j);
             uint32_t mine = 0, sz = 0;
             uint64_t a = 0;
             if (lane < nrows) {
-                const uint64_t start = ((uint64_t)(o0 + lane) * nsb + i) * 210;
+                const uint64_t start = ((uint64_t)(o0 + lane) * nsb + SB * j) * 210;
                 a = start & ~15ull;
-                sz = WROW;
-                if (a + WROW > nbytes) {
-                    // the buffer ends inside this window: bulk-copy its full
-                    // 16-byte granules, the block's remaining bytes one by one
+                sz = nb == SB ? WROW : 224;   // covers the blocks plus their <= 14-byte lead-in
+                if (a + sz > nbytes) {
+                    // the buffer ends inside this window (it holds the buffer's last
+                    // block): bulk-copy its full 16-byte granules, the blocks'
+                    // remaining bytes one by one
                     sz = (uint32_t)((nbytes - a) & ~15ull);
                     uint8_t *drow = dst_gen + lane * WROW;
-                    for (uint64_t b = a + sz; b < start + 210; ++b) drow[b - a] = w[b];
+                    for (uint64_t b = a + sz; b < start + 210 * nb; ++b) drow[b - a] = w[b];
                 }
                 mine = sz;
             }
-            if (lane == 0) mine += C::TOK * 512 + C::TOK * 32;
+            if (lane == 0) mine += nb * C::TOK * 512 + C::TOK * 32 * SB;
             mbar_arrive_expect_tx(bar, mine);
             if (sz) bulk_load(dst + lane * WROW, w + a, sz, bar);
+        };
+        auto stage_x = [&](int j, uint32_t dst, uint32_t bar) {
+            const int nb = min(SB, nsb - SB * j);
+            for (int q = 0; q < nb; ++q)
+                tma_load_2d(dst + C::X_OFF + q * C::TOK * 512, &tmX, bar, (SB * j + q) * 256, 0);
+            tma_load_2d(dst + C::D_OFF, &tmD, bar, SB * j * 8, 0);   // words past K/32 read as zero
         };
         // the weights do not depend on the previous kernel: the first ring's
         // worth of windows go out before waiting for it, the activations and
         // scale words after
-        const int first = nsb < C::S ? nsb : C::S;
-        for (int i = 0; i < first; ++i) stage_w(i, sbase + i * C::STAGE, full0 + 8 * i, sm + i * C::STAGE);
+        const int first = nst < C::S ? nst : C::S;
+        for (int j = 0; j < first; ++j) stage_w(j, sbase + j * C::STAGE, full0 + 8 * j, sm + j * C::STAGE);
         gv::pdl_wait();
         if (lane == 0)
-            for (int i = 0; i < first; ++i) {
-                const uint32_t dst = sbase + i * C::STAGE, bar = full0 + 8 * i;
-                tma_load_2d(dst + C::X_OFF, &tmX, bar, i * 256, 0);
-                tma_load_2d(dst + C::D_OFF, &tmD, bar, i * 8, 0);
-            }
+            for (int j = 0; j < first; ++j) stage_x(j, sbase + j * C::STAGE, full0 + 8 * j);
         issued = first;
         int slot = first == C::S ? 0 : first;
-        for (; issued < nsb; ++issued) {
+        for (; issued < nst; ++issued) {
             if (!mbar_wait_warp(empty0 + 8 * slot, (uint32_t)((issued / C::S - 1) & 1), abort_flag, KID, SITE_P_RAW))
                 break;
             const uint32_t dst = sbase + slot * C::STAGE, bar = full0 + 8 * slot;
             stage_w(issued, dst, bar, sm + slot * C::STAGE);
-            if (lane == 0) {
-                tma_load_2d(dst + C::X_OFF, &tmX, bar, issued * 256, 0);
-                tma_load_2d(dst + C::D_OFF, &tmD, bar, issued * 8, 0);
-            }
+            if (lane == 0) stage_x(issued, dst, bar);
             if (++slot == C::S) slot = 0;
         }
     } else {
         // consumer warp: group w / 4 takes stages w / 4, w / 4 + GROUPS, ...;
-        // quarter p = w % 4: 32-blocks 2p + e (e = 0, 1), sub-blocks 4p + 2e + s
+        // quarter p = w % 4 of each super-block: 32-blocks 2p + e (e = 0, 1),
+        // sub-blocks 4p + 2e + s
         const int p = warp & 3, h = p >> 1, pq = p & 1;
         const int g = lane >> 2, tig = lane & 3;
         int slot = warp >> 2;
         uint32_t phase = 0u;
-        for (int i = warp >> 2; i < nsb; i += GROUPS) {
+        for (int j = warp >> 2; j < nst; j += GROUPS) {
             const bool landed = mbar_wait(full0 + 8 * slot, phase, abort_flag, KID, SITE_U_STAGE);
             if (!__all_sync(0xffffffffu, landed)) break;
             const uint8_t *st = sm + slot * C::STAGE;
-            // rows g (j = 0) and g + 8 (j = 1): the exact f16 operands (q - 32) of
-            // elements 16 s + 4 tig .. + 3 of 32-block 2p + e, and the scale terms
-            // d*sc of sub-blocks 4p + k, k = 2e + s
-            uint32_t a01[2][2][2], a23[2][2][2];   // [j][e][s]
-            float dsv[2][4];
+            const int nb = min(SB, nsb - SB * j);
+            for (int q = 0; q < nb; ++q) {
+                // rows g (jr = 0) and g + 8 (jr = 1): the exact f16 operands (q - 32)
+                // of elements 16 s + 4 tig .. + 3 of 32-block 2p + e of super-block
+                // SB j + q, and the scale terms d*sc of its sub-blocks 4p + k, k = 2e + s
+                uint32_t a01[2][2][2], a23[2][2][2];   // [jr][e][s]
+                float dsv[2][4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int r = g + 8 * j;
-                const uint8_t *wr = st + r * WROW;
-                // the block's offset in its window: start mod 16 (start = 210 * block index)
-                const int off = (int)((((uint32_t)(o0 + r) * (uint32_t)nsb + (uint32_t)i) & 7u) * 210u & 15u);
-                const uint32_t qh0 = ld_u32_at(wr, off + 128 + 32 * h + 4 * tig);
-                const uint32_t qh1 = ld_u32_at(wr, off + 128 + 32 * h + 16 + 4 * tig);
+                for (int jr = 0; jr < 2; ++jr) {
+                    const int r = g + 8 * jr;
+                    const uint8_t *wr = st + r * WROW;
+                    // the first block's offset in the window: start mod 16 (start =
+                    // 210 * block index); the stage's next block follows it
+                    const int off = (int)((((uint32_t)(o0 + r) * (uint32_t)nsb + (uint32_t)(SB * j)) & 7u) * 210u & 15u) +
+                                    210 * q;
+                    const uint32_t qh0 = ld_u32_at(wr, off + 128 + 32 * h + 4 * tig);
+                    const uint32_t qh1 = ld_u32_at(wr, off + 128 + 32 * h + 16 + 4 * tig);
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
+                    for (int e = 0; e < 2; ++e)
 #pragma unroll
-                    for (int s = 0; s < 2; ++s) {
-                        const uint32_t ql = ld_u32_at(wr, off + 64 * h + 32 * e + 16 * s + 4 * tig);
-                        const uint32_t n4 = (ql >> (4 * pq)) & 0x0F0F0F0Fu;
-                        const uint32_t h2 = (((s ? qh1 : qh0) >> (2 * (2 * pq + e))) & 0x03030303u) << 4;
-                        gv6::q6_pairs(n4 | h2, a01[j][e][s], a23[j][e][s]);
-                    }
-                const uint32_t scw = ld_u32_at(wr, off + 192 + 4 * p);
-                const float d = gv::f16_bits(*reinterpret_cast<const uint16_t *>(wr + off + 208));
+                        for (int s = 0; s < 2; ++s) {
+                            const uint32_t ql = ld_u32_at(wr, off + 64 * h + 32 * e + 16 * s + 4 * tig);
+                            const uint32_t n4 = (ql >> (4 * pq)) & 0x0F0F0F0Fu;
+                            const uint32_t h2 = (((s ? qh1 : qh0) >> (2 * (2 * pq + e))) & 0x03030303u) << 4;
+                            gv6::q6_pairs(n4 | h2, a01[jr][e][s], a23[jr][e][s]);
+                        }
+                    const uint32_t scw = ld_u32_at(wr, off + 192 + 4 * p);
+                    const float d = gv::f16_bits(*reinterpret_cast<const uint16_t *>(wr + off + 208));
 #pragma unroll
-                for (int k = 0; k < 4; ++k) dsv[j][k] = d * (float)(int)(int8_t)(uint8_t)(scw >> (8 * k));
-            }
+                    for (int k = 0; k < 4; ++k) dsv[jr][k] = d * (float)(int)(int8_t)(uint8_t)(scw >> (8 * k));
+                }
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int t0 = 8 * n + 2 * tig;
-                const uint8_t *xr = st + C::X_OFF + (8 * n + g) * 512;
+                for (int n = 0; n < NT; ++n) {
+                    const int t0 = 8 * n + 2 * tig;
+                    const uint8_t *xr = st + C::X_OFF + q * C::TOK * 512 + (8 * n + g) * 512;
+                    const uint8_t *dw = st + C::D_OFF + 32 * SB * t0 + 32 * q;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int b = 2 * p + e;
-                    const float dx0 = gv::f16_bits(*reinterpret_cast<const uint32_t *>(st + C::D_OFF + t0 * 32 + b * 4) & 0xFFFFu);
-                    const float dx1 = gv::f16_bits(*reinterpret_cast<const uint32_t *>(st + C::D_OFF + (t0 + 1) * 32 + b * 4) & 0xFFFFu);
+                    for (int e = 0; e < 2; ++e) {
+                        const int b = 2 * p + e;
+                        const float dx0 = gv::f16_bits(*reinterpret_cast<const uint32_t *>(dw + b * 4) & 0xFFFFu);
+                        const float dx1 = gv::f16_bits(*reinterpret_cast<const uint32_t *>(dw + 32 * SB + b * 4) & 0xFFFFu);
 #pragma unroll
-                    for (int s = 0; s < 2; ++s) {
-                        // token 8n + g: elements 16 s + 4 tig .. + 3 of 32-block b
-                        const uint2 xv = *reinterpret_cast<const uint2 *>(xr + 2 * (32 * b + 16 * s + 4 * tig));
-                        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        gv::mma_f16(c, a01[0][e][s], a01[1][e][s], a23[0][e][s], a23[1][e][s], xv.x, xv.y);
-                        const int k = 2 * e + s;
-                        acc[n][0] = fmaf(dx0 * dsv[0][k], c[0], acc[n][0]);
-                        acc[n][1] = fmaf(dx1 * dsv[0][k], c[1], acc[n][1]);
-                        acc[n][2] = fmaf(dx0 * dsv[1][k], c[2], acc[n][2]);
-                        acc[n][3] = fmaf(dx1 * dsv[1][k], c[3], acc[n][3]);
+                        for (int s = 0; s < 2; ++s) {
+                            // token 8n + g: elements 16 s + 4 tig .. + 3 of 32-block b
+                            const uint2 xv = *reinterpret_cast<const uint2 *>(xr + 2 * (32 * b + 16 * s + 4 * tig));
+                            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            gv::mma_f16(c, a01[0][e][s], a01[1][e][s], a23[0][e][s], a23[1][e][s], xv.x, xv.y);
+                            const int k = 2 * e + s;
+                            acc[n][0] = fmaf(dx0 * dsv[0][k], c[0], acc[n][0]);
+                            acc[n][1] = fmaf(dx1 * dsv[0][k], c[1], acc[n][1]);
+                            acc[n][2] = fmaf(dx0 * dsv[1][k], c[2], acc[n][2]);
+                            acc[n][3] = fmaf(dx1 * dsv[1][k], c[3], acc[n][3]);
+                        }
                     }
                 }
             }
@@ -284,13 +299,13 @@ int launch_gemv_q6_nt(const void *w, const uint16_t *xh, const uint32_t *ds, flo
 {
     using C = gv6::Cfg<NT>;
     CUtensorMap tmX, tmD;
-    // xh as [T][K] 16-bit, box 256 x TOK; ds as [T][K/32] words, box 8 x TOK;
-    // token rows past T read as zero
+    // xh as [T][K] 16-bit, box 256 x TOK; ds as [T][K/32] words, box 8 SB x TOK;
+    // token rows past T and words past K/32 read as zero
     int rc = make_tmap_2d(&tmX, xh, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, 256,
                           C::TOK, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != MMQ_OK) return rc;
-    rc = make_tmap_2d(&tmD, ds, CU_TENSOR_MAP_DATA_TYPE_UINT32, (uint64_t)(K / 32), (uint64_t)T, (uint64_t)(K / 8), 8,
-                      C::TOK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    rc = make_tmap_2d(&tmD, ds, CU_TENSOR_MAP_DATA_TYPE_UINT32, (uint64_t)(K / 32), (uint64_t)T, (uint64_t)(K / 8),
+                      8 * C::SB, C::TOK, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != MMQ_OK) return rc;
     static bool attr_done[64];
     int dev = 0;
