@@ -65,6 +65,14 @@ def test_argument_errors_without_gpu():
     assert lib.mmq_gemm_q4K_small(p, p, null, p, 64, 8, 256, null) == -6
     assert lib.mmq_gemm_q4K_small(p, odd, p, p, 64, 8, 256, null) == -2
     assert lib.mmq_gemm_q4K_small(p, p, p, p, 0, 8, 256, null) == 0          # T == 0 no-op
+    for gemv in (lib.mmq_gemv_q4K, lib.mmq_gemv_q6K):                         # decode-shaped products
+        assert gemv(p, p, p, p, 17, 8, 256, null) == -1                       # T > 16
+        assert gemv(p, p, p, p, 16, 8, 300, null) == -1                       # K % 256
+        assert gemv(p, p, p, p, 16, 0, 256, null) == -1                       # O < 1
+        assert gemv(p, p, p, p, 16, 8, 1 << 21, null) == -1                   # K > 2^20
+        assert gemv(p, p, null, p, 16, 8, 256, null) == -6
+        assert gemv(p, odd, p, p, 16, 8, 256, null) == -2
+        assert gemv(p, p, p, p, 0, 8, 256, null) == 0                         # T == 0 no-op
     assert lib.mmq_last_failure_info(null) == -6
     info = (ctypes.c_int * 4)(7, 7, 7, 7)
     assert lib.mmq_last_failure_info(info) == 0 and list(info) == [0, 0, 0, 0]   # nothing reported yet
