@@ -19,9 +19,10 @@ pinned host memory and reads the last layer's GEMM outputs back, the copies
 on two copy streams overlapping the compute of the neighbouring steps
 (device inputs and outputs double-buffered).
 
-`--impl reference` times the CPU oracle (plain C, one thread) on a bounded
-sample of the same workload: full q8_1 quantisation of the four inputs and
-the first rows of every GEMM's output.
+`--impl reference` times the CPU oracle (plain C, OpenMP over the output
+columns, every host core) on a bounded sample of the same workload: full
+q8_1 quantisation of the four inputs and the first rows of every GEMM's
+output.  The default run also times that oracle once as `cpu_baseline`.
 """
 from __future__ import annotations
 
@@ -52,7 +53,7 @@ def parse_args():
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-small-t", action="store_true", help="skip the small-T side measurement")
+    ap.add_argument("--no-small-t", action="store_true", help="skip the token-sweep and decode side measurements")
     ap.add_argument("--decode-launches", action="store_true",
                     help="only run one eager decode step (T = 1) of --layers layers through the decode-shaped "
                          "kernels (for a launch list)")
@@ -96,6 +97,69 @@ def load_peaks():
         return d, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+# Bytes per weight of each k-quant format (one super-block per 256 weights).
+WEIGHT_BYTES = {"q4_K": 144 / 256, "q6_K": 210 / 256}
+# f16 tensor-core MMAs per algorithmic MAC on this route: q4_K multiplies the
+# exact hi and lo activation planes (2), q6_K also splits the weight value
+# into hi and lo and runs hi*hi, lo*hi, hi*lo (3).
+ROUTE_MMAS = {"q4_K": 2, "q6_K": 3}
+
+
+def algorithmic_bytes(fmt, T, K, O):
+    """Bytes one GEMM must move: the k-quant weights, the q8_1 activations
+    (int8 values plus one 4-byte scale word per 32: 1.125 B per element) and
+    the f32 output."""
+    return WEIGHT_BYTES[fmt] * O * K + 1.125 * T * K + 4.0 * T * O
+
+
+def layout_bytes(fmt, T, K, O, act_bytes_per_elem):
+    """Bytes the kernel reads and writes in this library's layout: the weights,
+    the activation operand planes it reads (xa: 4 B per element, xh: 2), the
+    scale words (0.125 B per element) and the f32 output."""
+    return WEIGHT_BYTES[fmt] * O * K + (act_bytes_per_elem + 0.125) * T * K + 4.0 * T * O
+
+
+def choose_peak(peaks, clk):
+    """bf16 dense peak (TFLOP/s) for the kernels timed here: the burst figure
+    when the sampled SM clock stayed at its maximum with no throttle reason
+    during the timed region, the sustained (power-capped) figure otherwise."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    sm, smax = (clk or {}).get("sm_mhz"), (clk or {}).get("sm_max_mhz")
+    if sm and smax and sm >= 0.98 * smax and not (clk or {}).get("reasons"):
+        return burst, "burst (median SM clock at its maximum, no throttle reason in the timed region)"
+    return sustained, "sustained (SM clock below its maximum or a throttle reason in the timed region)"
+
+
+def cpu_info():
+    """Host CPU as seen by this process: model name, logical CPUs, affinity."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for line in fh:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except AttributeError:
+        affinity = os.cpu_count()
+    import platform
+    return {"model": model or platform.processor() or "unknown", "arch": platform.machine(),
+            "nproc": os.cpu_count(), "affinity": affinity}
 
 
 class ClockSampler:
@@ -214,16 +278,21 @@ def graph_time_us(fns, n=20, reps=5):
     return best
 
 
-def small_t_lines(dev, hbm_gbs):
-    """Side measurement of the small-T tier (config 4 shapes at T = 1, 16 and 64),
-    device time per launch with the weights streamed from HBM (the timed
-    launches cycle through copies of W larger than L2 together): the
-    weight-stationary small-T GEMM, the int8 warp-MMA form (T <= 16), the
-    split-K GEMM and the one-CTA-per-tile production GEMM."""
+def sweep_lines(dev, hbm_gbs, mac_peak, fast=False):
+    """The token sweep (K = 4096 and 11008 into O = 4096) at T = 1, 16, 64, 256,
+    1024 and 4096, device time per launch with the weights streamed from HBM
+    (the timed launches cycle through copies of W larger than L2 together).
+    Every kernel that takes the shape is timed: the weight-stationary small-T
+    GEMM and the int8 warp-MMA form (T <= 64 / 16), the decode-shaped product
+    (T <= 16), split-K (T <= 256) and the one-CTA-per-tile production GEMM.
+    Each line reports TMAC/s, the fraction of the f16 dense MAC peak and of
+    this route's own ceiling, and algorithmic GB/s (weights + q8_1 activations
+    at 1.125 B/element + f32 output) as a fraction of the HBM copy rate."""
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     out = []
-    for T in (1, 16, 64):
+    Ts = (1, 16) if fast else (1, 16, 64, 256, 1024, 4096)
+    for T in Ts:
         for g in synth.config(4, T).gemms:
             w0 = torch.from_numpy(g.weights()).to(dev)
             copies = [w0] + [w0.clone() for _ in range(int(320e6 // w0.numel()))]
@@ -231,26 +300,33 @@ def small_t_lines(dev, hbm_gbs):
             x = torch.from_numpy(g.x()).to(dev)
             qs, ds, xh, xa = ops.quantize_q8_1(x)
             y = torch.empty((g.T, g.O), dtype=torch.float32, device=dev)
-            ks = ops.choose_ksplit(g.T, g.O, g.K)
-            ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
-            us_small = graph_time_us([lambda w=w: ops.gemm_small(w, xa, ds, g.O, out=y) for w in copies], n=n)
-            us_imma = (graph_time_us([lambda w=w: ops.gemm_small_imma(w, qs, ds, g.O, out=y) for w in copies], n=n)
-                       if g.T <= ops.SMALL_IMMA_T_MAX else None)
-            us_gemv = (graph_time_us([lambda w=w: ops.gemv(w, xh, ds, g.O, out=y) for w in copies], n=n)
-                       if g.T <= ops.GEMV_T_MAX else None)
-            us_split = graph_time_us([lambda w=w: ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws, out=y)
-                                      for w in copies], n=n)
-            us_plain = graph_time_us([lambda w=w: ops.gemm("q4_K", w, xa, ds, g.O, out=y) for w in copies], n=n)
-            nbytes = w0.numel() + g.T * g.K * 4 + g.T * g.K // 8 + g.T * g.O * 4   # W + xa + ds + Y
-            line = {"T": g.T, "K": g.K, "O": g.O, "small_us": us_small, "small_imma_us": us_imma,
-                    "splitk_us": us_split, "ksplit": ks, "plain_us": us_plain,
-                    "small_tmacs": g.macs / (us_small * 1e-6) / 1e12,
-                    "small_gbs": nbytes / (us_small * 1e-6) / 1e9,
-                    "small_hbm_frac": nbytes / (us_small * 1e-6) / 1e9 / hbm_gbs}
-            if us_gemv is not None:
-                gbytes = w0.numel() + g.T * g.K * 2 + g.T * g.K // 8 + g.T * g.O * 4   # W + xh + ds + Y
-                line.update({"gemv_us": us_gemv, "gemv_gbs": gbytes / (us_gemv * 1e-6) / 1e9,
-                             "gemv_hbm_frac": gbytes / (us_gemv * 1e-6) / 1e9 / hbm_gbs})
+            kern = {}
+            if g.T <= ops.SMALL_T_MAX:
+                kern["small"] = graph_time_us([lambda w=w: ops.gemm_small(w, xa, ds, g.O, out=y) for w in copies], n=n)
+            if g.T <= ops.SMALL_IMMA_T_MAX:
+                kern["small_imma"] = graph_time_us([lambda w=w: ops.gemm_small_imma(w, qs, ds, g.O, out=y)
+                                                    for w in copies], n=n)
+            if g.T <= ops.GEMV_T_MAX:
+                kern["gemv"] = graph_time_us([lambda w=w: ops.gemv(w, xh, ds, g.O, out=y) for w in copies], n=n)
+            ks = None
+            if g.T <= 256:
+                ks = ops.choose_ksplit(g.T, g.O, g.K)
+                ws = ops.SplitKWorkspace(dev, *ops.splitk_sizes(g.T, g.O, g.K, ks))
+                kern["splitk"] = graph_time_us([lambda w=w: ops.gemm_splitk(w, xa, ds, g.O, ksplit=ks, workspace=ws,
+                                                                            out=y) for w in copies], n=n)
+            kern["production"] = graph_time_us([lambda w=w: ops.gemm("q4_K", w, xa, ds, g.O, out=y) for w in copies],
+                                               n=n)
+            abytes = algorithmic_bytes("q4_K", g.T, g.K, g.O)
+            best = min(kern, key=kern.get)
+            us = kern[best]
+            line = {"T": g.T, "K": g.K, "O": g.O, "us": {k: round(v, 3) for k, v in kern.items()}, "best": best,
+                    "tmacs": g.macs / (us * 1e-6) / 1e12,
+                    "f16_dense_frac": g.macs / (us * 1e-6) / 1e12 / mac_peak,
+                    "route_ceiling_frac": g.macs / (us * 1e-6) / 1e12 / (mac_peak / ROUTE_MMAS["q4_K"]),
+                    "algorithmic_bytes": int(abytes),
+                    "gbs": abytes / (us * 1e-6) / 1e9, "hbm_frac": abytes / (us * 1e-6) / 1e9 / hbm_gbs}
+            if ks is not None:
+                line["ksplit"] = ks
             out.append(line)
             del copies
     # the decode-shaped q6_K product on the 7B attn_v shape (K = O = 4096)
@@ -261,12 +337,14 @@ def small_t_lines(dev, hbm_gbs):
         x = torch.from_numpy(synth.make_x(T, 4096, 302)).to(dev)
         _, ds, xh, xa = ops.quantize_q8_1(x, want_qs=False)
         y = torch.empty((T, 4096), dtype=torch.float32, device=dev)
-        us_gemv = graph_time_us([lambda w=w: ops.gemv(w, xh, ds, 4096, out=y, fmt="q6_K") for w in copies], n=n)
-        us_plain = graph_time_us([lambda w=w: ops.gemm("q6_K", w, xa, ds, 4096, out=y) for w in copies], n=n)
-        gbytes = w0.numel() + T * 4096 * 2 + T * 4096 // 8 + T * 4096 * 4   # W + xh + ds + Y
-        out.append({"fmt": "q6_K", "T": T, "K": 4096, "O": 4096, "gemv_us": us_gemv, "plain_us": us_plain,
-                    "gemv_gbs": gbytes / (us_gemv * 1e-6) / 1e9,
-                    "gemv_hbm_frac": gbytes / (us_gemv * 1e-6) / 1e9 / hbm_gbs})
+        kern = {"gemv": graph_time_us([lambda w=w: ops.gemv(w, xh, ds, 4096, out=y, fmt="q6_K") for w in copies], n=n),
+                "production": graph_time_us([lambda w=w: ops.gemm("q6_K", w, xa, ds, 4096, out=y) for w in copies],
+                                            n=n)}
+        abytes = algorithmic_bytes("q6_K", T, 4096, 4096)
+        us = min(kern.values())
+        out.append({"fmt": "q6_K", "T": T, "K": 4096, "O": 4096, "us": {k: round(v, 3) for k, v in kern.items()},
+                    "best": min(kern, key=kern.get), "algorithmic_bytes": int(abytes),
+                    "gbs": abytes / (us * 1e-6) / 1e9, "hbm_frac": abytes / (us * 1e-6) / 1e9 / hbm_gbs})
         del copies
     ops.check_status(dev)
     return out
@@ -340,6 +418,18 @@ def workload_desc(T, layers):
             f"11008->4096, 4 q8_1 quantisations")
 
 
+def workload_config(args, wl, world=1):
+    """The `config` object both arms print: the workload, not how it is run."""
+    wbytes = sum(WEIGHT_BYTES[g.fmt] * g.O * g.K for g in wl.gemms)
+    return {
+        "workload": workload_desc(args.tokens, args.layers),
+        "tokens": args.tokens, "layers": args.layers, "macs_per_layer": wl.macs,
+        "parallelism": f"replicas x{world} (independent copies per GPU)",
+        "l2": "inputs larger than L2: each layer has its own weight buffers (weights per step "
+              f"{wbytes * args.layers / 1e9:.2f} GB)",
+    }
+
+
 def build_inputs(T):
     from quantized_prefill_gemm_mmq_gb300 import synth
     wl = synth.layer_7b(T)
@@ -352,31 +442,58 @@ def build_inputs(T):
 
 # ------------------------------------------------------------ CPU oracle --
 
-def run_oracle_sample(wl, xs, weights, rows_per_gemm):
+def run_oracle_sample(wl, xs, weights, rows_per_gemm, threads=None, split=False):
     """Quantise every input fully and compute the first rows_per_gemm output
-    columns of each GEMM with the oracle; returns (seconds, MACs)."""
+    columns of each GEMM with the oracle (OpenMP over the output columns,
+    `threads` threads, None = every core); returns (seconds, MACs), or
+    (quantisation seconds, GEMM seconds, MACs) with split=True."""
     import oracle
     macs = 0
     t0 = time.perf_counter()
     q = {s: oracle.quantize_q8_1(x) for s, x in xs.items()}
+    t1 = time.perf_counter()
     for g in wl.gemms:
         r = min(rows_per_gemm, g.O)
         qs, ds = q[g.x_seed]
-        oracle.gemm(g.fmt, weights[g.name][:r], qs, ds, r)   # first r weight rows
+        oracle.gemm(g.fmt, weights[g.name][:r], qs, ds, r, threads=threads)   # first r weight rows
         macs += g.T * g.K * r
-    return time.perf_counter() - t0, macs
+    t2 = time.perf_counter()
+    return (t1 - t0, t2 - t1, macs) if split else (t2 - t0, macs)
+
+
+def oracle_rows_for(wl, xs, weights, seconds):
+    """Rows per GEMM for an oracle sample of about `seconds` (from a short
+    calibration run), at least 1 and at most the smallest O."""
+    import oracle
+    cal_rows = 8 * oracle.max_threads()      # enough output columns to keep every thread busy
+    tq, tg, macs = run_oracle_sample(wl, xs, weights, cal_rows, split=True)
+    rate = macs / max(tg, 1e-9)
+    macs_per_row = sum(g.T * g.K for g in wl.gemms)
+    return max(1, min(min(g.O for g in wl.gemms), int(max(seconds - tq, 0.1) * rate / macs_per_row)))
+
+
+def cpu_baseline_leg(wl, xs, weights, seconds=12.0):
+    import oracle
+    rows = oracle_rows_for(wl, xs, weights, seconds)
+    secs, macs = run_oracle_sample(wl, xs, weights, rows)
+    info = cpu_info()
+    return {"value": macs / secs / 1e12, "unit": "TMAC/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "cpu": info,
+            "sample": f"q8_1 quantisation of the 4 layer inputs (one thread) and the first {rows} output rows of each "
+                      f"of the 7 GEMMs of one layer ({macs} MACs, {secs:.1f} s; OpenMP over the output columns on "
+                      f"{oracle.max_threads()} threads); every layer of the stack is a copy of that layer"}
 
 
 def reference_arm(args):
+    import oracle
     rank, world, _ = dist_env()
     if rank != 0:
         return
     wl, xs = build_inputs(args.tokens)
     weights = {g.name: g.weights() for g in wl.gemms}
-    # size each step so the whole run stays within ~2 minutes at ~0.25 GMAC/s
+    # size each step so the whole run stays within about two minutes
     budget_s = max(0.5, 120.0 / max(1, args.steps + args.warmup))
-    macs_per_row = sum(g.T * g.K for g in wl.gemms)
-    rows = max(1, int(budget_s * 0.25e9 / macs_per_row))
+    rows = oracle_rows_for(wl, xs, weights, budget_s)
     for _ in range(args.warmup):
         run_oracle_sample(wl, xs, weights, rows)
     total_s, total_macs = 0.0, 0
@@ -385,15 +502,17 @@ def reference_arm(args):
         total_s += s
         total_macs += m
     value = total_macs / total_s / 1e12
-    sample = (f"per step: q8_1 quantisation of the 4 layer inputs (T={args.tokens}) and the first {rows} output "
-              f"rows of each of the 7 GEMMs of one layer ({total_macs // args.steps} MACs)")
+    sample = (f"per step: q8_1 quantisation of the 4 layer inputs (T={args.tokens}, one thread) and the first {rows} "
+              f"output rows of each of the 7 GEMMs of one layer ({total_macs // args.steps} MACs; OpenMP over the "
+              f"output columns on {oracle.max_threads()} threads); every layer of the stack is a copy of that layer")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TMAC/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32 dots, f32 terms, f64 sum",
-        "data": "synthetic (seeded; no checkpoint)",
-        "config": {"workload": workload_desc(args.tokens, 1) + " (bounded CPU sample)", "tokens": args.tokens},
-        "cpu_baseline": {"value": value, "unit": "TMAC/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "data": "synthetic (seeded random k-quant weights and N(0,1) activations with 1% x20 outlier channels)",
+        "config": workload_config(args, wl),
+        "cpu_baseline": {"value": value, "unit": "TMAC/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "cpu": cpu_info(), "sample": sample},
         "e2e": {"value": value, "unit": "TMAC/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -578,31 +697,31 @@ def mmq_arm(args):
     ops.check_status(dev)
     elapsed_ms = e0.elapsed_time(e1)
 
-    # per-launch durations of the dominant kernel (q4_K GEMM); the roofline
-    # is reported on its 4096x4096 launches (q, k, o) so that the ncu
-    # counters of that shape apply, and over all q4_K launches for reference
-    sq_ms = sq_macs = all_ms = all_macs = 0.0
-    n_sq = 0
+    # per-launch durations of the dominant kernel (the production q4_K GEMM),
+    # by launch shape: the headline roofline is taken on its 4096 x 4096
+    # launches (q, k, o; the shape of the committed ncu counters), and the
+    # gate+up (4096 -> 22016) and down (11008 -> 4096) launches get their own
+    shape_stats = {}     # shape key -> [ms, macs, launches, group]
     kernel_timing = None
 
-    def is_square(g):
-        return g.fmt == "q4_K" and g.K == 4096 and g.O == 4096
+    def shape_key(g):
+        return f"T={g.T} K={g.K} O={g.O}"
+
+    def add_time(g, ms):
+        st = shape_stats.setdefault(shape_key(g), [0.0, 0, 0, g])
+        st[0] += ms
+        st[1] += g.macs
+        st[2] += 1
 
     if ext_events is not None:
         for li in range(len(layers)):
             for gi, g in enumerate(groups):
                 ev = ext_events[li][gi]
                 if ev is not None:
-                    ms = ev[0].elapsed_time(ev[1])
-                    all_ms += ms
-                    all_macs += g.macs
-                    if is_square(g):
-                        sq_ms += ms
-                        sq_macs += g.macs
-                        n_sq += 1
+                    add_time(g, ev[0].elapsed_time(ev[1]))
         kernel_timing = (f"events in the captured graph around the q4_K launches of every {EV_STRIDE}th layer "
                          "(last replay of the timed region)")
-    if sq_ms <= 0.0:
+    if not shape_stats:
         pairs = []
         for lw in layers:
             for g in groups:
@@ -614,13 +733,7 @@ def mmq_arm(args):
                     pairs.append((a, b, g))
         torch.cuda.synchronize()
         for a, b, g in pairs:
-            ms = a.elapsed_time(b)
-            all_ms += ms
-            all_macs += g.macs
-            if is_square(g):
-                sq_ms += ms
-                sq_macs += g.macs
-                n_sq += 1
+            add_time(g, a.elapsed_time(b))
         kernel_timing = "eager per-launch events"
     int8_peak = ops.tensor_peak_tmacs("int8", dev)
 
@@ -717,41 +830,67 @@ def mmq_arm(args):
     peaks, peak_src = load_peaks()
     ms_step = elapsed_ms / args.steps
     value = job_tmacs(step_macs, args.steps, world, elapsed_ms)
-    achieved = 2.0 * sq_macs / (sq_ms * 1e-3) / 1e12 if sq_ms > 0 else None
-    # the q4_K launches are timed inside a long step: the sustained bf16 figure applies
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
+    peak, peak_kind = choose_peak(peaks, clk)
+    mac_peak = peak / 2.0                       # f16 dense TMAC/s (f16 runs at the bf16 rate)
+    hbm_gbs = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+
+    def shape_line(st):
+        ms, macs, n, g = st
+        us = 1e3 * ms / n
+        tflops = 2.0 * macs / (ms * 1e-3) / 1e12
+        return {"shape": shape_key(g), "launch": g.name, "launches_timed": n, "avg_launch_us": us,
+                "achieved_tflops": tflops, "frac": tflops / peak,
+                "route_ceiling_frac": tflops / (peak / ROUTE_MMAS[g.fmt]),
+                "algorithmic_bytes_per_launch": int(algorithmic_bytes(g.fmt, g.T, g.K, g.O)),
+                "layout_bytes_per_launch": int(layout_bytes(g.fmt, g.T, g.K, g.O, 4))}
+
+    shapes = [shape_line(st) for st in shape_stats.values()]
+    sq = shape_stats.get(shape_key(next(g for g in groups if g.fmt == "q4_K" and g.K == g.O == 4096)))
+    sq_line = shape_line(sq) if sq else None
     roofline = {
-        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-        "frac": achieved / peak if achieved else None,
+        "bound": "tensor",
+        "achieved": sq_line["achieved_tflops"] if sq_line else None,
+        "peak": peak, "unit": "TFLOP/s",
+        "frac": sq_line["frac"] if sq_line else None,
         "traffic": traffic_bytes("mmq_q4K_sb_kernel"),
-        "kernel": "mmq_q4K_sb_kernel (q4_K GEMM), launches of shape T=512 K=4096 O=4096",
-        "algorithmic_bytes_per_launch": 4096 * 4096 * 9 // 16 + 512 * 4096 * 4 + 512 * 4096 // 8 + 512 * 4096 * 4,
-        "peak_source": f"{peak_src} bf16 dense, sustained (timed inside the step); f16 runs at the bf16 rate",
+        "kernel": f"mmq_q4K_sb_kernel (production q4_K GEMM), launches of shape T={args.tokens} K=4096 O=4096",
+        "algorithmic_bytes_per_launch": sq_line["algorithmic_bytes_per_launch"] if sq_line else None,
+        "layout_bytes_per_launch": sq_line["layout_bytes_per_launch"] if sq_line else None,
+        "algorithmic_work": "2*T*O*K flop; bytes = 0.5625*O*K (q4_K) + 1.125*T*K (q8_1) + 4*T*O (f32 Y); the layout "
+                            "reads the activations as exact f16 hi/lo planes (4 B per element) + scale words",
+        "peak_source": f"{peak_src} bf16 dense, {peak_kind}; f16 runs at the bf16 rate",
+        "route_ceiling_frac": sq_line["route_ceiling_frac"] if sq_line else None,
+        "route_ceiling_note": "exact results take 2 f16 MMAs per 16-k step for q4_K (activation hi and lo planes), "
+                              "3 for q6_K: the route's ceiling is 1/2 (1/3) of the dense peak",
         "timing": kernel_timing,
-        "avg_launch_us": 1e3 * sq_ms / max(1, n_sq),
-        "all_q4K_launches_tflops": 2.0 * all_macs / (all_ms * 1e-3) / 1e12 if all_ms > 0 else None,
+        "avg_launch_us": sq_line["avg_launch_us"] if sq_line else None,
+        "shapes": shapes,
+    }
+    # the step's ceiling on this route: every GEMM at its route's MMA count, the quantisations free
+    step_ceiling = layer_macs / sum(g.macs * ROUTE_MMAS[g.fmt] / mac_peak for g in groups)
+    fractions = {
+        "f16_dense": value / world / mac_peak,
+        "route_ceiling": value / world / step_ceiling,
+        "f16_dense_mac_peak_tmacs": mac_peak,
+        "route_ceiling_tmacs": step_ceiling,
     }
     cpu = None
     if not args.no_cpu and world == 1:
-        rows = 160
-        secs, macs = run_oracle_sample(wl, xs, host_w, rows)
-        cpu = {"value": macs / secs / 1e12, "unit": "TMAC/s", "cores": 1, "kind": "oracle",
-               "sample": f"q8_1 quantisation of the 4 layer inputs and the first {rows} output rows of each of the "
-                         f"7 GEMMs of one layer ({macs} MACs, {secs:.1f} s, one thread)"}
-    small_t = None
+        cpu = cpu_baseline_leg(wl, xs, host_w)
+    sweep = None
     if not args.no_small_t and world == 1:
-        small_t = {"kernel": "mmq_q4K_wt_kernel (mmq_gemm_q4K_small) vs mmq_q4K_small_kernel (int8 warp MMA), "
-                             "mmq_q4K_gemv_kernel (mmq_gemv_q4K, T <= 16), split-K (mmq_gemm_q4K_splitk) and one "
-                             "CTA per 128x128 tile (mmq_gemm_q4K); q6_K lines: mmq_q6K_gemv_kernel (mmq_gemv_q6K) "
-                             "vs the production q6_K GEMM",
-                   "timing": "CUDA-graph replay cycling through >320 MB of weight copies (HBM-resident), device "
-                             "events, best of 5",
-                   "bytes": "weights + xa (4 B/elem) + ds + y",
-                   "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
-                   "lines": small_t_lines(dev, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))}
+        sweep = {"kernels": "per line every kernel that takes the shape: mmq_gemm_q4K_small (weight-stationary "
+                            "tcgen05, T <= 64), mmq_gemm_q4K_small_imma (int8 warp MMA, T <= 16), mmq_gemv_q4K "
+                            "(decode-shaped, T <= 16), mmq_gemm_q4K_splitk (T <= 256) and mmq_gemm_q4K (production); "
+                            "q6_K lines: mmq_gemv_q6K vs the production q6_K GEMM on the attn_v shape",
+                 "timing": "CUDA-graph replay cycling through >320 MB of weight copies (HBM-resident), device "
+                           "events, best of 5; the line's rates are the fastest kernel's",
+                 "bytes": "algorithmic: weights + q8_1 activations (1.125 B/element) + f32 Y",
+                 "hbm_peak_gbs": hbm_gbs, "f16_dense_mac_peak_tmacs": mac_peak,
+                 "lines": sweep_lines(dev, hbm_gbs, mac_peak)}
     decode = None
     if not args.no_small_t and world == 1:
-        decode = decode_line(dev, layers, groups, xs, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])))
+        decode = decode_line(dev, layers, groups, xs, hbm_gbs)
     line = {
         "metric": METRIC,
         "value": value,
@@ -765,17 +904,14 @@ def mmq_arm(args):
         "vs_baseline": None,
         "dtype": "f16 tensor-core operands holding exact int8/int4 integers, f32 accumulate and fold",
         "data": "synthetic (seeded random k-quant weights and N(0,1) activations with 1% x20 outlier channels)",
-        "config": {
-            "workload": workload_desc(args.tokens, args.layers),
-            "tokens": args.tokens, "layers": args.layers, "macs_per_layer": layer_macs,
-            "parallelism": f"replicas x{world} (independent copies per GPU)",
-            "l2": "inputs larger than L2: each layer has its own weight buffers (weights per step "
-                  f"{sum(t.numel() for t in w_layer.values()) * args.layers / 1e9:.2f} GB)",
-            "launch": timing_mode,
-        },
-        "int8_peak_tmacs": int8_peak,
-        "int8_peak_source": "measured live: mma.sync m16n8k32 s8 (no int8 tcgen05 kind on sm_103a)",
+        "config": workload_config(args, wl, world),
+        "launch": timing_mode,
+        "fractions": fractions,
         "int8_frac": value / world / int8_peak if int8_peak else None,
+        "int8_frac_note": "labelled extra: TMAC/s over the legacy warp-level int8 MMA rate (mma.sync m16n8k32 s8, "
+                          "measured live); sm_103a has no int8 tcgen05 kind and this route runs on the f16 tensor "
+                          "cores, so the figure can exceed 1",
+        "int8_peak_tmacs": int8_peak,
         "layer_tok_s": args.tokens * args.layers * args.steps * world / (elapsed_ms * 1e-3),
         "model_tok_s_gemm_only": args.tokens * args.steps * world / (elapsed_ms * 1e-3),
         "roofline": roofline,
@@ -783,7 +919,7 @@ def mmq_arm(args):
         "e2e": e2e,
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
-        "small_t": small_t,
+        "sweep": sweep,
         "decode": decode,
     }
     print(json.dumps(line), flush=True)

@@ -79,7 +79,8 @@ enum {
     MMQ_ERR_NULL = -6,      /* a required pointer is NULL                          */
     MMQ_ERR_DRIVER = -7,    /* the driver could not build a TMA tensor map         */
     MMQ_ERR_CUDA = -8,      /* (mmq_check_status) a CUDA error is pending          */
-    MMQ_ERR_SCRATCH = -9    /* the call needs more than the library's static scratch */
+    MMQ_ERR_SCRATCH = -9,   /* the call needs more than the library's static scratch */
+    MMQ_ERR_DEVICE = -10    /* current device index >= 64 (the library's per-device tables) */
 };
 
 /* Library ABI version; bumped on any signature or format change. */
@@ -132,7 +133,9 @@ int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *ds,
  * order differs.
  * part, counters: caller-owned device scratch; mmq_splitk_sizes gives their
  * sizes.  counters (int32, 4-byte aligned) must be all zero before the first
- * call and are left all zero by every completed call.  Two calls that use
+ * call and are left all zero by every call whose kernel ran, one that timed
+ * out included; after a call whose mmq_check_status is not MMQ_OK, y from that
+ * call is undefined.  Two calls that use
  * the same part/counters at the same time (different streams) race.
  * ksplit == 1 is mmq_gemm_q4K (part and counters unused, may be NULL).
  * Limits as mmq_gemm_q4K; ksplit >= 1; part 16-byte aligned.
@@ -216,13 +219,21 @@ int mmq_gemv_q6K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y
  * 8192 tile counters per device.  (The pages have no counterpart: their
  * kernel never splits K.)
  *   - The scratch address is obtained once per device, with that device
- *     current, on the first call for that device.  Make that first call
- *     before any stream capture.
- *   - Calls whose mmq_splitk_sizes exceed that scratch return
- *     MMQ_ERR_SCRATCH and launch nothing.
+ *     current, on the first call for that device that needs scratch (under a
+ *     lock: first calls from several host threads are safe).  Make that
+ *     first call before any stream capture.  The address belongs to the
+ *     device's CUDA context of that moment: after cudaDeviceReset of the
+ *     device, do not call this entry point again in the same process.
+ *   - Calls with one split (ksplit == 1, or K == 256) need no scratch and
+ *     run as mmq_gemm_q4K whatever their size.  Calls whose
+ *     mmq_splitk_sizes exceed the scratch return MMQ_ERR_SCRATCH and
+ *     launch nothing.
  *   - What must start at zero: the tile counters.  They are zero when the
  *     library is loaded, and every call that launched leaves them at zero
- *     when its kernel ends (a kernel that timed out included).
+ *     when its kernel ends (a kernel that timed out included).  After a call
+ *     whose mmq_check_status is not MMQ_OK, y from that call is undefined
+ *     (an aborted split may have skipped its partial sums); the counters
+ *     are still valid for the next call.
  *   - The scratch is shared by every call on the device: calls that may
  *     overlap in time (different streams, no ordering between them) race
  *     and give wrong results.  Order them on one stream.

@@ -46,6 +46,8 @@ def lib():
         L.orc_gemm_q6K.argtypes = [P, P, P, i32, i32, i32, P, i64]
         L.orc_gemm_points.argtypes = [i32, P, P, P, i32, i32, P, P, P]
         L.orc_dequant_q8_1.argtypes = [P, P, i32, i32, P]
+        L.orc_gemm_mt.argtypes = [i32, P, P, P, i32, i32, i32, P, i64, i32]
+        L.orc_max_threads.restype = i32
         L.orc_version.restype = i32
         _lib = L
     return _lib
@@ -149,16 +151,27 @@ def subdots(fmt: str, w: np.ndarray, qs: np.ndarray, O: int) -> np.ndarray:
     return out
 
 
-def gemm(fmt: str, w: np.ndarray, qs: np.ndarray, ds: np.ndarray, O: int) -> np.ndarray:
-    """Method-form Y [T][O] f32."""
+def gemm(fmt: str, w: np.ndarray, qs: np.ndarray, ds: np.ndarray, O: int, threads: int | None = None) -> np.ndarray:
+    """Method-form Y [T][O] f32.  threads=1: the single-thread loop; otherwise the
+    output columns are divided among `threads` OpenMP threads (None: every core
+    the process may use).  The result is the same bit for bit either way."""
     qs = _c(qs, np.int8)
     ds = _c(ds, np.uint32)
     T, K = qs.shape
     w = _check_w(w, fmt, O, K)
     y = np.empty((T, O), np.float32)
-    fn = lib().orc_gemm_q4K if fmt == "q4_K" else lib().orc_gemm_q6K
-    fn(_p(w), _p(qs), _p(ds), T, O, K, _p(y), O)
+    if threads == 1:
+        fn = lib().orc_gemm_q4K if fmt == "q4_K" else lib().orc_gemm_q6K
+        fn(_p(w), _p(qs), _p(ds), T, O, K, _p(y), O)
+    else:
+        lib().orc_gemm_mt(6 if fmt == "q6_K" else 4, _p(w), _p(qs), _p(ds), T, O, K, _p(y), O,
+                          0 if threads is None else int(threads))
     return y
+
+
+def max_threads() -> int:
+    """Threads the multi-threaded oracle uses by default."""
+    return lib().orc_max_threads()
 
 
 def gemm_points(fmt: str, w: np.ndarray, qs: np.ndarray, ds: np.ndarray, O: int,

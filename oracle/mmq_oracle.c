@@ -44,6 +44,9 @@
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_QK 256
 #define ORC_QK8 32
@@ -384,7 +387,45 @@ void orc_dequant_q8_1(const int8_t *qs, const uint32_t *ds, int T, int K, double
                 (double)act_d(ds[(size_t)t * (K / 32) + k / 32]) * qs[(size_t)t * K + k];
 }
 
-int orc_version(void) { return 1; }
+/* ------------------------------------------- all host cores (OpenMP) -- */
+
+/* The same outputs as orc_gemm_q4K / orc_gemm_q6K, with the output columns o
+ * (weight rows) shared among `nthreads` OpenMP threads (<= 0: the runtime's
+ * default, i.e. every core the process may use).  Every output is still
+ * computed by one call of the plain per-output function above, so the result
+ * is bit-identical to the single-thread form; only the work is divided.
+ * fmt 4 = q4_K, 6 = q6_K. */
+void orc_gemm_mt(int fmt, const uint8_t *w, const int8_t *qs, const uint32_t *ds,
+                 int T, int O, int K, float *y, int64_t ldy, int nthreads)
+{
+    const size_t bb = (fmt == 6) ? ORC_Q6K_BYTES : ORC_Q4K_BYTES;
+    const size_t row_bytes = (size_t)(K / ORC_QK) * bb;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (int o = 0; o < O; ++o) {
+        const uint8_t *wrow = w + (size_t)o * row_bytes;
+        for (int t = 0; t < T; ++t) {
+            const int8_t *qrow = qs + (size_t)t * K;
+            const uint32_t *dsrow = ds + (size_t)t * (K / 32);
+            y[(size_t)t * ldy + o] = (fmt == 6) ? point_q6K(wrow, qrow, dsrow, K) : point_q4K(wrow, qrow, dsrow, K);
+        }
+    }
+    (void)nthreads;
+}
+
+/* Threads orc_gemm_mt uses by default (1 without OpenMP). */
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int orc_version(void) { return 2; }
 
 /* Array forms of the f16 conversions, for exhaustive checks. */
 void orc_f16_to_f32_array(const uint16_t *h, int64_t n, float *out)

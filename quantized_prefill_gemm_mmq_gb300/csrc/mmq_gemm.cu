@@ -34,6 +34,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "mmq_dev.cuh"
 #include "mmq_host.h"
@@ -1540,7 +1541,7 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     static bool attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(mmq_q4K_sb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)q4s::kDynSmem) != cudaSuccess)
@@ -1988,7 +1989,7 @@ int launch_q6K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     static bool attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(mmq_q6K_sb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)q6s::kDynSmem) != cudaSuccess)
@@ -2222,7 +2223,7 @@ int launch_q4K_small(const void *w, const int8_t *qs, const uint32_t *ds, float 
     static bool attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(mmq_q4K_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
             cudaSuccess)
@@ -2749,7 +2750,7 @@ int launch_wt_n(const void *w, const uint16_t *xa, const uint32_t *ds, float *y,
     static bool attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(mmq_q4K_wt_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::kDynSmem) != cudaSuccess)
@@ -2830,7 +2831,7 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
     static bool attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) != cudaSuccess)
             return launch_status();
@@ -2905,20 +2906,37 @@ extern "C" int mmq_gemm_q4K_splitk_static(const void *w, const uint16_t *xa, con
     int64_t part_floats = 0, tiles = 0;
     const int rc = mmq_splitk_sizes(T, O, K, ksplit, &part_floats, &tiles);
     if (rc != MMQ_OK) return rc;
+    // one split (ksplit == 1, or a single super-block per row) uses no scratch at all
+    if (part_floats == 0) return mmq_gemm_q4K_splitk(w, xa, ds, y, T, O, K, 1, nullptr, nullptr, stream);
     if (part_floats > kStaticPartFloats || tiles > kStaticCounters) return MMQ_ERR_SCRATCH;
+    // device addresses of the two arrays, looked up once per device (with that
+    // device current) under a lock, so that concurrent first calls from several
+    // host threads do not race on the table
     static float *part[64];
     static int *cnt[64];
+    static std::mutex mu;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
-    if (!part[dev] || !cnt[dev]) {
-        void *a = nullptr, *b = nullptr;
-        if (cudaGetSymbolAddress(&a, g_splitk_part) != cudaSuccess ||
-            cudaGetSymbolAddress(&b, g_splitk_cnt) != cudaSuccess)
-            return mmq::launch_status();
-        part[dev] = static_cast<float *>(a);
-        cnt[dev] = static_cast<int *>(b);
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_ARCH;
     }
-    return mmq_gemm_q4K_splitk(w, xa, ds, y, T, O, K, ksplit, part[dev], cnt[dev], stream);
+    if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
+    float *pp = nullptr;
+    int *cc = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!part[dev] || !cnt[dev]) {
+            void *a = nullptr, *b = nullptr;
+            if (cudaGetSymbolAddress(&a, g_splitk_part) != cudaSuccess ||
+                cudaGetSymbolAddress(&b, g_splitk_cnt) != cudaSuccess)
+                return mmq::launch_status();
+            part[dev] = static_cast<float *>(a);
+            cnt[dev] = static_cast<int *>(b);
+        }
+        pp = part[dev];
+        cc = cnt[dev];
+    }
+    return mmq_gemm_q4K_splitk(w, xa, ds, y, T, O, K, ksplit, pp, cc, stream);
 }
 
 extern "C" int mmq_gemm_q4K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O,

@@ -309,7 +309,11 @@ int launch_gemv_q6_nt(const void *w, const uint16_t *xh, const uint32_t *ds, flo
     if (rc != MMQ_OK) return rc;
     static bool attr_done[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MMQ_ERR_ARCH;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_ARCH;
+    }
+    if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
         if (cudaFuncSetAttribute(mmq_q6K_gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
             cudaSuccess)

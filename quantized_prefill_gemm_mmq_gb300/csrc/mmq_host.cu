@@ -45,7 +45,7 @@ int check_arch()
         cudaGetLastError();
         return MMQ_ERR_ARCH;
     }
-    if (dev < 0 || dev >= kMaxDevices) return MMQ_ERR_ARCH;
+    if (dev < 0 || dev >= kMaxDevices) return MMQ_ERR_DEVICE;
     {
         std::lock_guard<std::mutex> lk(g_arch_mu);
         if (g_arch_ok[dev] == 0) {
@@ -120,6 +120,7 @@ extern "C" const char *mmq_status_str(int status)
     case MMQ_ERR_DRIVER: return "driver could not encode a TMA tensor map";
     case MMQ_ERR_CUDA: return "CUDA error pending on the stream";
     case MMQ_ERR_SCRATCH: return "split-K scratch needed exceeds the library's static scratch (4 Mi f32 partial sums, 8192 tiles)";
+    case MMQ_ERR_DEVICE: return "current device index is beyond the library's per-device tables (64 devices)";
     default: return "unknown status";
     }
 }

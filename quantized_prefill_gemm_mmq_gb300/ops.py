@@ -172,8 +172,23 @@ def splitk_sizes(T: int, O: int, K: int, ksplit: int) -> tuple[int, int]:
     return pf.value, nc.value
 
 
-def choose_ksplit(T: int, O: int, K: int, sms: int = 148) -> int:
-    """Splits of K that bring the grid near one wave when the output has few tiles."""
+_SM_COUNT: dict[int, int] = {}
+
+
+def sm_count(device: torch.device | int | None = None) -> int:
+    """Streaming multiprocessors of a CUDA device (the current one by default)."""
+    idx = torch.cuda.current_device() if device is None else torch.device("cuda", device).index \
+        if isinstance(device, int) else (device.index if device.index is not None else torch.cuda.current_device())
+    if idx not in _SM_COUNT:
+        _SM_COUNT[idx] = torch.cuda.get_device_properties(idx).multi_processor_count
+    return _SM_COUNT[idx]
+
+
+def choose_ksplit(T: int, O: int, K: int, sms: int | None = None) -> int:
+    """Splits of K that bring the grid near one wave when the output has few
+    tiles; `sms` defaults to the current device's SM count."""
+    if sms is None:
+        sms = sm_count()
     tiles = -(-O // 128) * -(-T // 128)
     return max(1, min(K // 256, sms // max(1, tiles)))
 

@@ -17,3 +17,21 @@ def orc():
     import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def oracle_ref(orc):
+    """Oracle results for synthetic GEMMs (synth.Gemm), computed once per
+    session on every host core: (qs, ds, Y) of the q8_1-quantised input and
+    the method-form output, shared by the tests that check different kernels
+    on the same configuration."""
+    cache = {}
+
+    def ref(g):
+        key = (g.fmt, g.T, g.K, g.O, g.w_seed, g.x_seed, g.outliers)
+        if key not in cache:
+            qs, ds = orc.quantize_q8_1(g.x())
+            cache[key] = (qs, ds, orc.gemm(g.fmt, g.weights(), qs, ds, g.O))
+        return cache[key]
+
+    return ref

@@ -39,7 +39,7 @@ def test_library_loads_and_reports():
     lib = _lib.load()
     assert lib.mmq_version() == 7
     assert lib.mmq_status_str(0) == b"ok"
-    for code in range(-9, 0):
+    for code in range(-10, 0):
         assert lib.mmq_status_str(code) not in (b"", b"unknown status")
 
 
@@ -93,6 +93,10 @@ def test_argument_errors_without_gpu():
     # static-scratch variant: oversize requests are refused before anything else
     assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 4096, 4096, 4096, 4, null) == -9
     assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 16, 256, 1024, 0, null) == -1
+    # one split needs no scratch: a shape with more output tiles than the static counters
+    # (8192 x 16512: 64 x 129 tiles) is not refused for lack of scratch with ksplit == 1
+    assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 8192, 16512, 4096, 1, null) != -9
+    assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 8192, 16512, 256, 4, null) != -9   # K = 256: one split
 
 
 @needs_lib

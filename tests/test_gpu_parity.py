@@ -194,41 +194,25 @@ def test_gemm_closed_form_superblock(ops, kernel):
     assert y[0, 0] == 6833616.0
 
 
-def _sample_points(rng, T, O, n=1500):
-    ti = rng.integers(0, T, n)
-    oi = rng.integers(0, O, n)
-    # always include the corners and the ragged tails
-    ti = np.concatenate([ti, [0, 0, T - 1, T - 1]])
-    oi = np.concatenate([oi, [0, O - 1, 0, O - 1]])
-    return ti.astype(np.int32), oi.astype(np.int32)
-
-
 @pytest.mark.parametrize("cfg,T", [(1, None), (2, None), (3, None), (4, 16), (4, 64), (4, 256), (4, 1024), (4, 4096)])
-def test_gemm_full_size_sampled(ops, orc, cfg, T):
+def test_gemm_full_size(ops, oracle_ref, cfg, T):
+    """Every output of every GEMM of the 7B configurations and of the token
+    sweep, production kernels (and the per-sub-block kernels on configs 1-3),
+    element by element against the oracle."""
     wl = synth.config(cfg, T)
-    rng = np.random.default_rng(cfg * 10000 + (T or 0))
-    xs = {}
     for g in wl.gemms:
-        if g.x_seed not in xs:
-            xs[g.x_seed] = g.x()
-        x = xs[g.x_seed]
-        w = g.weights()
-        qs_r, ds_r = orc.quantize_q8_1(x)
-        qs, ds, xh, xa = _gpu_quant(ops, x)
+        qs_r, ds_r, ref = oracle_ref(g)
+        qs, ds, xh, xa = _gpu_quant(ops, g.x())
         assert np.array_equal(qs.cpu().numpy(), qs_r)
         assert np.array_equal(_to_np_ds(ds), ds_r)
-        wd = _dev(w)
-        outs = []
-        outs.append(("production", ops.gemm(g.fmt, wd, xa, ds, g.O)))
-        if g.fmt == "q6_K" or cfg in (1, 2):
+        wd = _dev(g.weights())
+        outs = [("production", ops.gemm(g.fmt, wd, xa, ds, g.O))]
+        if cfg in (1, 2, 3):
             outs.append(("subblock", ops.gemm_subblock(g.fmt, wd, xh, ds, g.O)))
         ops.check_status()
-        ti, oi = _sample_points(rng, g.T, g.O)
-        ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
         for kernel, y in outs:
-            got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-            assert _rel_err(got, ref) <= TOL, (g.name, kernel, _rel_err(got, ref))
-            assert torch.isfinite(y).all()
+            err = _rel_err(y.cpu().numpy(), ref)
+            assert err <= TOL, (g.name, kernel, err)
 
 
 @pytest.mark.parametrize("T,O,K,ksplit", [(16, 256, 1024, 4), (1, 129, 2816, 3), (130, 300, 1280, 2),
@@ -300,20 +284,15 @@ def test_gemv(ops, orc, T, O, K):
 
 
 @pytest.mark.parametrize("T", [1, 8, 16])
-def test_gemv_full_size_sampled(ops, orc, T):
-    """The token-sweep shapes (K = 4096 and 11008, O = 4096) at decode sizes."""
-    wl = synth.config(4, T)
-    rng = np.random.default_rng(5151 + T)
-    for g in wl.gemms:
-        x, w = g.x(), g.weights()
-        qs_r, ds_r = orc.quantize_q8_1(x)
-        _, ds, xh, _ = ops.quantize_q8_1(_dev(x), want_qs=False, want_xa=False)
-        y = ops.gemv(_dev(w), xh, ds, g.O)
+def test_gemv_full_size(ops, oracle_ref, T):
+    """The token-sweep shapes (K = 4096 and 11008, O = 4096) at decode sizes,
+    every output against the oracle."""
+    for g in synth.config(4, T).gemms:
+        _, _, ref = oracle_ref(g)
+        _, ds, xh, _ = ops.quantize_q8_1(_dev(g.x()), want_qs=False, want_xa=False)
+        y = ops.gemv(_dev(g.weights()), xh, ds, g.O)
         ops.check_status()
-        ti, oi = _sample_points(rng, g.T, g.O)
-        ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
-        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-        assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
+        assert _rel_err(y.cpu().numpy(), ref) <= TOL, g.name
 
 
 @pytest.mark.parametrize("T,O,K", [(1, 1, 256), (8, 256, 1024), (9, 131, 2816), (16, 200, 768), (3, 17, 512),
@@ -336,9 +315,10 @@ def test_gemv_q6K(ops, orc, T, O, K):
 
 
 @pytest.mark.parametrize("T", [1, 16])
-def test_gemv_q6K_full_size_sampled(ops, orc, T):
+def test_gemv_q6K_full_size(ops, orc, T):
     """The 7B attn_v shape (q6_K, K = O = 4096) at decode sizes, full-range
-    int8 sub-block scales (-128..127) as well as the synthetic -64..63."""
+    int8 sub-block scales (-128..127) as well as the synthetic -64..63, every
+    output against the oracle."""
     rng = np.random.default_rng(6161 + T)
     O, K = 4096, 4096
     x = synth.make_x(T, K, seed=33 + T, outliers=True)
@@ -350,10 +330,8 @@ def test_gemv_q6K_full_size_sampled(ops, orc, T):
     for wt in (w, wf.reshape(w.shape)):
         y = ops.gemv(_dev(wt), xh, ds, O, fmt="q6_K")
         ops.check_status()
-        ti, oi = _sample_points(rng, T, O)
-        ref = orc.gemm_points("q6_K", wt, qs_r, ds_r, O, ti, oi)
-        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-        assert _rel_err(got, ref) <= TOL, _rel_err(got, ref)
+        ref = orc.gemm("q6_K", wt, qs_r, ds_r, O)
+        assert _rel_err(y.cpu().numpy(), ref) <= TOL
 
 
 def test_gemv_closed_form_and_limits(ops):
@@ -374,22 +352,18 @@ def test_gemv_closed_form_and_limits(ops):
 
 
 @pytest.mark.parametrize("T", [16, 64])
-def test_gemm_small_t_full_size_sampled(ops, orc, T):
-    wl = synth.config(4, T)
-    rng = np.random.default_rng(4242 + T)
-    for g in wl.gemms:
-        x, w = g.x(), g.weights()
-        qs_r, ds_r = orc.quantize_q8_1(x)
-        qs, ds, _, xa = ops.quantize_q8_1(_dev(x), want_xh=False)
-        outs = [("small", ops.gemm_small(_dev(w), xa, ds, g.O))]
+def test_gemm_small_t_full_size(ops, oracle_ref, T):
+    """The small-T kernels on the token-sweep shapes, every output against the oracle."""
+    for g in synth.config(4, T).gemms:
+        _, _, ref = oracle_ref(g)
+        qs, ds, _, xa = ops.quantize_q8_1(_dev(g.x()), want_xh=False)
+        w = _dev(g.weights())
+        outs = [("small", ops.gemm_small(w, xa, ds, g.O))]
         if T <= ops.SMALL_IMMA_T_MAX:
-            outs.append(("small_imma", ops.gemm_small_imma(_dev(w), qs, ds, g.O)))
+            outs.append(("small_imma", ops.gemm_small_imma(w, qs, ds, g.O)))
         ops.check_status()
-        ti, oi = _sample_points(rng, g.T, g.O)
-        ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
         for kernel, y in outs:
-            got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-            assert _rel_err(got, ref) <= TOL, (g.name, kernel, _rel_err(got, ref))
+            assert _rel_err(y.cpu().numpy(), ref) <= TOL, (g.name, kernel)
 
 
 def test_gemm_small_t_closed_form(ops):
@@ -403,21 +377,15 @@ def test_gemm_small_t_closed_form(ops):
     assert float(ops.gemm_small_imma(_dev(w), qs, ds, 1)[0, 0]) == 6833616.0
 
 
-@pytest.mark.parametrize("cfg,T", [(4, 16), (4, 64), (4, 256)])
-def test_gemm_splitk_full_size_sampled(ops, orc, cfg, T):
-    wl = synth.config(cfg, T)
-    rng = np.random.default_rng(cfg * 777 + T)
-    for g in wl.gemms:
-        x = g.x()
-        qs_r, ds_r = orc.quantize_q8_1(x)
-        _, ds, _, xa = _gpu_quant(ops, x)
-        w = g.weights()
-        y = ops.gemm_splitk(_dev(w), xa, ds, g.O)
+@pytest.mark.parametrize("T", [16, 64, 256])
+def test_gemm_splitk_full_size(ops, oracle_ref, T):
+    """Split-K on the token-sweep shapes, every output against the oracle."""
+    for g in synth.config(4, T).gemms:
+        _, _, ref = oracle_ref(g)
+        _, ds, _, xa = ops.quantize_q8_1(_dev(g.x()), want_qs=False, want_xh=False)
+        y = ops.gemm_splitk(_dev(g.weights()), xa, ds, g.O)
         ops.check_status()
-        ti, oi = _sample_points(rng, g.T, g.O)
-        ref = orc.gemm_points(g.fmt, w, qs_r, ds_r, g.O, ti, oi)
-        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-        assert _rel_err(got, ref) <= TOL, (g.name, _rel_err(got, ref))
+        assert _rel_err(y.cpu().numpy(), ref) <= TOL, g.name
 
 
 @pytest.mark.parametrize("kernel", ["production", "subblock"])
@@ -534,23 +502,18 @@ def test_gemm_concatenated_rows_equal_separate(ops):
     assert torch.equal(y12[:, O1:], y2)
 
 
-def _sampled_check(orc, fmt, w, x, O, ys, n=24, seed=0):
+def _full_check(orc, fmt, w, x, O, ys):
     qs_r, ds_r = orc.quantize_q8_1(x)
-    rng = np.random.default_rng(seed)
-    T = x.shape[0]
-    ti = rng.integers(0, T, n).astype(np.int32)
-    oi = rng.integers(0, O, n).astype(np.int32)
-    ti[0], oi[0] = T - 1, O - 1                      # the last row and column
-    ref = orc.gemm_points(fmt, w, qs_r, ds_r, O, ti, oi)
+    ref = orc.gemm(fmt, w, qs_r, ds_r, O)
     for name, y in ys:
-        got = y[torch.from_numpy(ti).long().cuda(), torch.from_numpy(oi).long().cuda()].cpu().numpy()
-        assert _rel_err(got, ref) <= TOL, (name, _rel_err(got, ref))
         assert torch.isfinite(y).all(), name
+        assert _rel_err(y.cpu().numpy(), ref) <= TOL, (name, _rel_err(y.cpu().numpy(), ref))
 
 
 def test_gemm_max_k(ops, orc):
     """K at the library's limit (2^20: 4096 super-blocks per row): long
-    accumulation in every q4_K and q6_K GEMM form, sampled against the oracle."""
+    accumulation in every q4_K and q6_K GEMM form, every output against the
+    oracle."""
     T, O, K = 4, 128, 1 << 20
     x = synth.make_x(T, K, seed=91, outliers=True)
     qs, ds, xh, xa = _gpu_quant(ops, x)
@@ -565,17 +528,17 @@ def test_gemm_max_k(ops, orc):
           ("small_imma", ops.gemm_small_imma(wd, qs, ds, O)),
           ("gemv", ops.gemv(wd, xh, ds, O))]
     ops.check_status()
-    _sampled_check(orc, "q4_K", w4, x, O, ys, seed=1)
+    _full_check(orc, "q4_K", w4, x, O, ys)
     w6 = synth.make_weights("q6_K", O, K, seed=93)
     y6 = ops.gemm("q6_K", _dev(w6), xa, ds, O)
     y6v = ops.gemv(_dev(w6), xh, ds, O, fmt="q6_K")
     ops.check_status()
-    _sampled_check(orc, "q6_K", w6, x, O, [("q6_K production", y6), ("q6_K gemv", y6v)], seed=2)
+    _full_check(orc, "q6_K", w6, x, O, [("q6_K production", y6), ("q6_K gemv", y6v)])
 
 
 def test_gemm_large_o(ops, orc):
     """2^18 output rows (2048 row tiles, 37.7 MB of q4_K weights at K = 256):
-    tile indexing and 64-bit offsets, sampled against the oracle."""
+    tile indexing and 64-bit offsets, every output against the oracle."""
     T, O, K = 3, 1 << 18, 256
     x = synth.make_x(T, K, seed=94, outliers=True)
     qs, ds, xh, xa = _gpu_quant(ops, x)
@@ -586,4 +549,4 @@ def test_gemm_large_o(ops, orc):
           ("small_imma", ops.gemm_small_imma(wd, qs, ds, O)),
           ("gemv", ops.gemv(wd, xh, ds, O))]
     ops.check_status()
-    _sampled_check(orc, "q4_K", w, x, O, ys, seed=3)
+    _full_check(orc, "q4_K", w, x, O, ys)

@@ -330,3 +330,17 @@ def test_gemm_points_match_full(orc):
 def test_f16_bits_helper_matches_oracle(orc):
     for v in [0.0, 1.0, 1e-3, 6e-5, 65504.0, -2.5]:
         assert f16_bits(v) == int(orc.f32_to_f16(np.array([v], np.float32))[0])
+
+
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K"])
+def test_oracle_threads_do_not_change_results(orc, fmt):
+    """The OpenMP form divides output columns among threads; each output is the
+    same single-thread computation, so the result must be identical bit for bit
+    to the single-thread loop (also with more threads than columns)."""
+    from quantized_prefill_gemm_mmq_gb300 import synth
+    T, O, K = 9, 37, 768
+    w = synth.make_weights(fmt, O, K, seed=5)
+    qs, ds = orc.quantize_q8_1(synth.make_x(T, K, seed=6))
+    y1 = orc.gemm(fmt, w, qs, ds, O, threads=1)
+    for nt in (None, 3, 64):
+        assert np.array_equal(orc.gemm(fmt, w, qs, ds, O, threads=nt).view(np.uint32), y1.view(np.uint32))

@@ -1,7 +1,10 @@
-"""The split-K q4_K GEMM on the library's static scratch (no allocation
-anywhere) against the caller-workspace entry point.  Kept in a file of its
-own that is collected last: it must pass alone and after every other test
-(the static counters carry over between calls and processes' tests)."""
+"""The split-K q4_K GEMM on the library's static scratch against the
+caller-workspace entry point.  For callers that cannot allocate device memory
+(an allocator-less host runtime, code running while device allocation is not
+allowed): the entry point itself allocates nothing, which the tests check
+through the CUDA free-memory count and torch's allocator.  Kept in a file of
+its own that is collected last: it must pass alone and after every other test
+(the static counters carry over between calls)."""
 from __future__ import annotations
 
 import numpy as np
@@ -31,9 +34,16 @@ def test_static_scratch_matches_caller_workspace(ops, T, O, K, ksplit):
     x = torch.from_numpy(synth.make_x(T, K, seed=O + 5, outliers=True)).cuda()
     _, ds, _, xa = ops.quantize_q8_1(x, want_qs=False, want_xh=False)
     ref = ops.gemm_splitk(w, xa, ds, O, ksplit=ksplit)
-    a = ops.gemm_splitk_static(w, xa, ds, O, ksplit=ksplit)
-    b = ops.gemm_splitk_static(w, xa, ds, O, ksplit=ksplit)   # two calls in a row: counters were reset
+    a = torch.empty_like(ref)
+    b = torch.empty_like(ref)
+    ops.gemm_splitk_static(w, xa, ds, O, ksplit=ksplit, out=a)   # first call: the library's one-time set-up
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    ops.gemm_splitk_static(w, xa, ds, O, ksplit=ksplit, out=a)
+    ops.gemm_splitk_static(w, xa, ds, O, ksplit=ksplit, out=b)   # two calls in a row: counters were reset
     ops.check_status()
+    assert torch.cuda.mem_get_info()[0] == free0                 # no device memory taken by the calls
+    assert torch.cuda.memory_allocated() == alloc0
     assert torch.equal(a, ref)
     assert torch.equal(b, ref)
 
