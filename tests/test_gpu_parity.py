@@ -162,8 +162,10 @@ KERNELS = [("q4_K", "production"), ("q4_K", "subblock"), ("q6_K", "production"),
 
 @pytest.mark.parametrize("fmt,kernel", KERNELS)
 @pytest.mark.parametrize("T,O,K", [(64, 256, 512), (1, 1, 256), (130, 300, 768), (129, 129, 1280),
-                                   (256, 512, 2048)])
+                                   (256, 512, 2048), (300, 200, 1024), (640, 136, 512)])
 def test_gemm_full_small(ops, orc, fmt, kernel, T, O, K):
+    """Whole outputs against the oracle, ragged T and O; T = 300 and 640 give
+    an odd number of 128-token tiles."""
     w = synth.make_weights(fmt, O, K, seed=7 * T + O)
     x = synth.make_x(T, K, seed=K + T, outliers=T > 1)
     qs_r, ds_r = orc.quantize_q8_1(x)
@@ -216,7 +218,7 @@ def test_gemm_full_size(ops, oracle_ref, cfg, T):
 
 
 @pytest.mark.parametrize("T,O,K,ksplit", [(16, 256, 1024, 4), (1, 129, 2816, 3), (130, 300, 1280, 2),
-                                          (64, 512, 4096, 16), (200, 128, 768, 7)])
+                                          (64, 512, 4096, 16), (200, 128, 768, 7), (300, 256, 2048, 3)])
 def test_gemm_splitk_small(ops, orc, T, O, K, ksplit):
     w = synth.make_weights("q4_K", O, K, seed=3 * T + O)
     x = synth.make_x(T, K, seed=K + T + 1, outliers=True)
