@@ -414,8 +414,9 @@ def launch_groups(wl):
 
 def workload_desc(T, layers):
     return (f"LLaMA-7B decoder-stack projections, prefill T={T}, {layers} layers: per layer q/k/o q4_K 4096x4096, "
-            f"v q6_K 4096x4096, gate/up q4_K 4096->11008 (one launch over the concatenated rows), down q4_K "
-            f"11008->4096, 4 q8_1 quantisations")
+            f"v q6_K 4096x4096, gate/up q4_K 4096->11008 chained into down q4_K 11008->4096 (one launch over the "
+            f"interleaved gate/up rows whose epilogue writes silu(gate)*up as the down input's q8_1 planes), "
+            f"3 q8_1 quantisations (attention input, o input, FFN input)")
 
 
 def workload_config(args, wl, world=1):
@@ -602,23 +603,36 @@ def mmq_arm(args):
     wl, xs = build_inputs(args.tokens)
     groups = launch_groups(wl)
     host_w = {g.name: g.weights() for g in wl.gemms}
-    # one device weight tensor per launch group (gate and up: their rows concatenated)
-    w_layer = {gr.name: torch.from_numpy(np.concatenate([host_w[m.name] for m in gr.members])).to(dev)
+    # The FFN is chained: gate and up run as one launch over their rows
+    # interleaved in groups of 64 (mmq_gemm_q4K_swiglu), whose epilogue writes
+    # h = silu(gate)*up as the down projection's q8_1 operand planes; the down
+    # input is therefore produced on the device, not quantised from X.
+    ffn = next(g for g in groups if g.name == "gate+up")
+    down = next(g for g in groups if g.name == "down")
+    F = ffn.O // 2
+
+    def interleave(wg, wu):
+        rb = wg.size // F
+        return np.concatenate([wg.reshape(F // 64, 64, rb), wu.reshape(F // 64, 64, rb)], axis=1).reshape(-1)
+
+    w_layer = {gr.name: torch.from_numpy(interleave(host_w["gate"], host_w["up"]) if gr is ffn else
+                                         np.concatenate([host_w[m.name] for m in gr.members])).to(dev)
                for gr in groups}
     layers = [w_layer] + [{n: t.clone() for n, t in w_layer.items()} for _ in range(args.layers - 1)]
-    x_dev = {s: torch.from_numpy(x).to(dev) for s, x in xs.items()}
-    # q8_1 planes per input: both production GEMMs read xa (the exact hi/lo
-    # dequantised values) and ds
+    x_dev = {s: torch.from_numpy(x).to(dev) for s, x in xs.items() if s != down.x_seed}
+    # q8_1 planes per input: the production GEMMs read xa (the exact hi/lo
+    # dequantised values) and ds; the down input's planes are written by the
+    # fused FFN launch
     qbuf = {s: (None,
                 torch.empty((x.shape[0], x.shape[1] // 32), dtype=torch.int32, device=dev),
                 None,
                 torch.empty((2,) + x.shape, dtype=torch.float16, device=dev))
             for s, x in xs.items()}
-    ybuf = {g.name: torch.empty((g.T, g.O), dtype=torch.float32, device=dev) for g in groups}
+    ybuf = {g.name: torch.empty((g.T, g.O), dtype=torch.float32, device=dev) for g in groups if g is not ffn}
     layer_macs = wl.macs
     assert layer_macs == sum(g.macs for g in groups)
     step_macs = layer_macs * args.layers
-    launches_per_step = args.layers * (len(xs) + len(groups))
+    launches_per_step = args.layers * (len(x_dev) + len(groups))
 
     ext_events = None   # per-launch events of the q4_K GEMMs, recorded inside the graph
     # Events are recorded around the q4_K launches of every EV_STRIDE-th layer
@@ -628,7 +642,11 @@ def mmq_arm(args):
 
     def run_gemm(g, lw, yb=None):
         _, ds, _, xa = qbuf[g.x_seed]
-        ops.gemm(g.fmt, lw[g.name], xa, ds, g.O, out=(yb if yb is not None else ybuf)[g.name])
+        if g is ffn:
+            _, hds, _, hxa = qbuf[down.x_seed]
+            ops.gemm_swiglu(lw[g.name], xa, ds, F, out=(None, hds, hxa))
+        else:
+            ops.gemm(g.fmt, lw[g.name], xa, ds, g.O, out=(yb if yb is not None else ybuf)[g.name])
 
     def step(record=None, xd=None, yb=None):
         for li, lw in enumerate(layers):
@@ -744,7 +762,7 @@ def mmq_arm(args):
     # step i+1's inputs and step i-1's outputs move while step i computes.
     e2e = None
     if not args.no_e2e:
-        hx = {s: torch.from_numpy(x).pin_memory() for s, x in xs.items()}
+        hx = {s: torch.from_numpy(xs[s]).pin_memory() for s in x_dev}
         hy = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in ybuf.items()}
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
         d2h = sum(t.numel() * t.element_size() for t in hy.values())

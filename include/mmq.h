@@ -145,6 +145,28 @@ int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint32_t *ds, f
                         int T, int O, int K, int ksplit, float *part, int *counters, mmq_stream_t stream);
 
 /*
+ * The 7B FFN's first half as one launch, chained into the down projection
+ * (the pages' workload is whole-model prefill, "31 . r28", 5 "Results"; the
+ * FFN activation is not printed there, so this follows the LLaMA-family
+ * SwiGLU: h = silu(g) * u, silu(g) = g / (1 + e^-g)).
+ *   g = X . W_gate^T and u = X . W_up^T are computed as mmq_gemm_q4K computes
+ *   y; the epilogue then evaluates h in f32, one rounding per operation
+ *   (expf, add, divide, multiply), and quantises h to q8_1 exactly as
+ *   mmq_quantize_q8_1 quantises x: the outputs are the down projection's
+ *   operands, ready for mmq_gemm_q4K with K = F.
+ * w_gu: 2F q4_K rows, gate and up interleaved in groups of 64 rows: rows
+ *   128j .. 128j+63 are gate rows 64j .. 64j+63 and rows 128j+64 .. 128j+127
+ *   the up rows of the same features (O*(K/256)*144 bytes with O = 2F).
+ * xa, ds: the input's planes as written by mmq_quantize_q8_1 (K columns).
+ * h_xa: f16 bits [2][T][F] (hi, lo planes), h_ds: uint32 [T][F/32] (4-byte
+ *   aligned), h_qs: int8 [T][F] or NULL; all written.
+ * T >= 0, 64 <= F <= 2^20, F % 64 == 0, K as mmq_gemm_q4K.  Deterministic.
+ */
+int mmq_gemm_q4K_swiglu(const void *w_gu, const uint16_t *xa, const uint32_t *ds,
+                        uint16_t *h_xa, uint32_t *h_ds, int8_t *h_qs,
+                        int T, int F, int K, mmq_stream_t stream);
+
+/*
  * q4_K GEMM for few tokens (1 <= T <= 64), where the GEMM is bound by
  * streaming W from HBM.  Same operands and result as mmq_gemm_q4K (xa, ds
  * from mmq_quantize_q8_1; y [T][O] f32, overwritten), computed with the

@@ -48,6 +48,7 @@ def lib():
         L.orc_dequant_q8_1.argtypes = [P, P, i32, i32, P]
         L.orc_gemm_mt.argtypes = [i32, P, P, P, i32, i32, i32, P, i64, i32]
         L.orc_max_threads.restype = i32
+        L.orc_swiglu.argtypes = [P, P, i64, P]
         L.orc_version.restype = i32
         _lib = L
     return _lib
@@ -195,6 +196,17 @@ def gemm_dequant(fmt: str, w: np.ndarray, qs: np.ndarray, ds: np.ndarray, O: int
     """Full-dequant form: f64 product of dequant(W) and dequant(q8_1(X))."""
     T, K = np.asarray(qs).shape
     return dequant_q8_1(qs, ds) @ dequant(fmt, w, O, K).T
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """h = silu(g) * u elementwise in f32 (reading R14), same shape as g."""
+    g = _c(g, np.float32)
+    u = _c(u, np.float32)
+    if g.shape != u.shape:
+        raise ValueError("g and u must have the same shape")
+    h = np.empty(g.shape, np.float32)
+    lib().orc_swiglu(_p(g), _p(u), g.size, _p(h))
+    return h
 
 
 def version() -> int:

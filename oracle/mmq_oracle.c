@@ -37,6 +37,11 @@
  *      stored d = f16 round-to-nearest-even of d32; an all-zero block gets
  *      d = 0, q = 0, ssum = 0.
  *   R8 q6_K sub-block dot is taken on the centred value q-32.
+ *   R14 FFN activation between the gate/up and down projections of the pages'
+ *      7B workload ([r28] 5 "Results": whole-model prefill): the pages print
+ *      none; the reading is the LLaMA-family SwiGLU h = silu(g) * u with
+ *      silu(g) = g / (1 + e^-g), evaluated in f32 (the kernel's precision)
+ *      one operation at a time, h then quantised to q8_1 like any activation.
  *   Method-form rounding: each fold term is evaluated in f32 exactly as
  *   written (no contraction: build with -ffp-contract=off), the terms are
  *   summed in f64 in sub-block order, and the result is rounded to f32.
@@ -385,6 +390,20 @@ void orc_dequant_q8_1(const int8_t *qs, const uint32_t *ds, int T, int K, double
         for (int k = 0; k < K; ++k)
             out[(size_t)t * K + k] =
                 (double)act_d(ds[(size_t)t * (K / 32) + k / 32]) * qs[(size_t)t * K + k];
+}
+
+/* --------------------------------------------------------- SwiGLU ---- */
+
+/* h[i] = silu(g[i]) * u[i], silu(g) = g / (1 + e^-g), in f32 with every
+ * operation rounded on its own (reading R14; built without contraction). */
+void orc_swiglu(const float *g, const float *u, int64_t n, float *h)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const float e = expf(-g[i]);
+        const float den = 1.0f + e;
+        const float s = g[i] / den;
+        h[i] = s * u[i];
+    }
 }
 
 /* ------------------------------------------- all host cores (OpenMP) -- */

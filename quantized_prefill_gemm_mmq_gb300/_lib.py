@@ -32,6 +32,7 @@ SIGNATURES = {
     "mmq_gemv_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q4K_splitk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "mmq_gemm_q4K_splitk_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "mmq_gemm_q4K_swiglu": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q6K_subblock": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q4K": (_I, [_P, _P, _P, _I, _I, _I, _P]),

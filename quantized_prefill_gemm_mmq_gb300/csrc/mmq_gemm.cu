@@ -33,6 +33,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cstring>
 #include <mutex>
 
@@ -111,6 +112,14 @@ struct Params {
     int sb_per_split;
     float *part;
     int *cnt;
+    // SwiGLU output (production q4_K kernel): with h_xa != nullptr the O = 2F weight
+    // rows are gate and up rows interleaved in groups of 64 (tile j: gate rows
+    // 64j..64j+63, then up rows 64j..64j+63), and instead of y the kernel writes
+    // h = silu(gate)*up quantised to q8_1: h_xa [2][T][F] (hi, lo planes), h_ds
+    // [T][F/32], h_qs [T][F] (optional)
+    uint16_t *h_xa;
+    uint32_t *h_ds;
+    int8_t *h_qs;
 };
 
 // wait sites recorded with a timeout
@@ -1097,8 +1106,17 @@ __device__ __forceinline__ uint32_t magic2(uint32_t x, uint32_t sel, __half2 m, 
     return q4::h2bits(__hfma2(*reinterpret_cast<const __half2 *>(&h), m, a));
 }
 
+// silu(g) * u in f32: g / (1 + e^-g) with each operation rounded once (no contraction)
+__device__ __forceinline__ float swiglu_f32(float g, float u)
+{
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
 }  // namespace q4s
 
+// SWIGLU: the tile's output is not stored as y but finished as silu(gate)*up and
+// quantised to q8_1 (Params::h_xa).
+template <bool SWIGLU>
 __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     mmq_q4K_sb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                       const Params p)
@@ -1360,6 +1378,92 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(slot));
         }
+        if constexpr (SWIGLU) {
+            // ---------------------------------------------- SwiGLU + q8_1 --
+            // Columns 0..63 of this tile are gate rows of features 64*bx ..,
+            // columns 64..127 the up rows of the same features.  The gate
+            // thread of token t hands its gate values 32..63 to the up thread
+            // of t, which hands back up values 0..31 (through the operand ring,
+            // idle now that every MMA has completed); then each computes
+            // h = silu(g)*u for 32 features (one q8_1 block) and quantises it
+            // exactly as mmq_quantize_q8_1 does.
+            constexpr int XS = 36;   // floats per token row: 16-byte stores of 8 lanes in 8 bank groups
+            float *xg = reinterpret_cast<float *>(smem + oStage);
+            float *xu = xg + BM * XS;
+            const bool gate = c0 == 0;
+            auto finish = [&](auto gate_tag) {
+                constexpr bool G = decltype(gate_tag)::value;
+                float *mine = (G ? xg : xu) + tl * XS;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4 *>(mine + i) =
+                        G ? make_float4(yv[32 + i], yv[33 + i], yv[34 + i], yv[35 + i])
+                          : make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+                named_bar_sync(1, NUM_EPI_WARPS * 32);
+                const float *oth = (G ? xu : xg) + tl * XS;
+                float h[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 o4 = *reinterpret_cast<const float4 *>(oth + i);
+                    const float ov[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        h[i + j] = G ? q4s::swiglu_f32(yv[i + j], ov[j]) : q4s::swiglu_f32(ov[j], yv[32 + i + j]);
+                }
+                if (!(ok && tok_ok)) return;
+                const int F = O >> 1;
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+                const float d32 = amax != 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f;
+                const __half dh = __float2half_rn(d32);
+                const float df = __half2float(dh);
+                const int f0 = blockIdx.x * 64 + (G ? 0 : 32);
+                uint4 *ph = reinterpret_cast<uint4 *>(p.h_xa + (size_t)t * F + f0);
+                uint4 *pl = reinterpret_cast<uint4 *>(p.h_xa + (size_t)T * F + (size_t)t * F + f0);
+                uint32_t qw[8];
+                int ssum = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const int i = 8 * c + e;
+                        int qa = 0, qb = 0;
+                        if (amax != 0.0f) {
+                            qa = min(127, max(-127, (int)roundf(__fdiv_rn(h[i], d32))));
+                            qb = min(127, max(-127, (int)roundf(__fdiv_rn(h[i + 1], d32))));
+                        }
+                        ssum += qa + qb;
+                        const uint32_t pair = (uint32_t)(uint8_t)qa | ((uint32_t)(uint8_t)qb << 8);
+                        if ((i & 2) == 0)
+                            qw[i >> 2] = pair;
+                        else
+                            qw[i >> 2] |= pair << 16;
+                        // v = f32(d16)*q exact in f32; hi = f16(v), lo = f16(v - hi), both exact
+                        const float2 v = make_float2(df * (float)qa, df * (float)qb);
+                        const __half2 hv = __float22half2_rn(v);
+                        const float2 bv = __half22float2(hv);
+                        const __half2 lv = __float22half2_rn(make_float2(v.x - bv.x, v.y - bv.y));
+                        hw[e >> 1] = q4::h2bits(hv);
+                        lw[e >> 1] = q4::h2bits(lv);
+                    }
+                    ph[c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    pl[c] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+                p.h_ds[(size_t)t * (F / 32) + f0 / 32] =
+                    (uint32_t)__half_as_ushort(dh) | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
+                if (p.h_qs != nullptr) {
+                    uint4 *pq = reinterpret_cast<uint4 *>(p.h_qs + (size_t)t * F + f0);
+                    pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+                }
+            };
+            if (gate)
+                finish(std::true_type{});
+            else
+                finish(std::false_type{});
+        }
         const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
         auto store_row = [&](float *row) {
             if (vec) {
@@ -1372,7 +1476,9 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                     if (o0 + c0 + i < O) row[i] = yv[i];
             }
         };
-        if (p.part == nullptr || gridDim.z == 1) {
+        if (SWIGLU) {
+            // written above
+        } else if (p.part == nullptr || gridDim.z == 1) {
             if (ok && tok_ok) store_row(p.y + (size_t)t * O + o0 + c0);
         } else {
             // split-K: publish this split's partial sums; the last CTA of the
@@ -1514,13 +1620,18 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
 
 // Production q4_K launch: activations as the [2T][K] f16 hi/lo planes.
 // ksplit <= 1 or part == nullptr: one CTA per output tile covers all of K.
+// With swiglu outputs (h_xa != nullptr): y unused, O = 2F gate/up rows interleaved by 64, no split.
 int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K, int ksplit,
-                  float *part, int *cnt, mmq_stream_t stream)
+                  float *part, int *cnt, mmq_stream_t stream, uint16_t *h_xa = nullptr, uint32_t *h_ds = nullptr,
+                  int8_t *h_qs = nullptr)
 {
     if (T < 0 || O < 1 || K < 256 || K > (1 << 20) || (K & 255)) return MMQ_ERR_SHAPE;
+    if (h_xa && (O % 128 != 0 || ksplit > 1)) return MMQ_ERR_SHAPE;
     if (T == 0) return MMQ_OK;
-    if (!w || !xa || !ds || !y) return MMQ_ERR_NULL;
-    if (!aligned16(w) || !aligned16(xa) || !aligned16(ds) || !aligned16(y)) return MMQ_ERR_ALIGN;
+    if (!w || !xa || !ds || (!y && !h_xa) || (h_xa && !h_ds)) return MMQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(xa) || !aligned16(ds) || (y && !aligned16(y)) || (h_xa && !aligned16(h_xa)) ||
+        (h_ds && ((uintptr_t)h_ds & 3u)) || (h_qs && !aligned16(h_qs)))
+        return MMQ_ERR_ALIGN;
     const int nsb = K / 256;
     int sbps = nsb, splits = 1;
     if (part != nullptr && ksplit > 1) {
@@ -1543,12 +1654,14 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(mmq_q4K_sb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(mmq_q4K_sb_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)q4s::kDynSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(mmq_q4K_sb_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)q4s::kDynSmem) != cudaSuccess)
             return launch_status();
         attr_done[dev] = true;
     }
-    Params prm;
+    Params prm{};
     prm.w = static_cast<const uint8_t *>(w);
     prm.ds = ds;
     prm.y = y;
@@ -1559,8 +1672,16 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     prm.sb_per_split = sbps;
     prm.part = splits > 1 ? part : nullptr;
     prm.cnt = splits > 1 ? cnt : nullptr;
+    prm.h_xa = h_xa;
+    prm.h_ds = h_ds;
+    prm.h_qs = h_qs;
     const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM), (unsigned)splits);
-    mmq_q4K_sb_kernel<<<grid, q4s::NTHREADS, q4s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
+    if (h_xa)
+        mmq_q4K_sb_kernel<true><<<grid, q4s::NTHREADS, q4s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
+            tmA, tmW, prm);
+    else
+        mmq_q4K_sb_kernel<false><<<grid, q4s::NTHREADS, q4s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
+            tmA, tmW, prm);
     return launch_status();
 }
 
@@ -1996,7 +2117,7 @@ int launch_q6K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
             return launch_status();
         attr_done[dev] = true;
     }
-    Params prm;
+    Params prm{};
     prm.w = static_cast<const uint8_t *>(w);
     prm.ds = ds;
     prm.y = y;
@@ -2837,7 +2958,7 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
             return launch_status();
         attr_done[dev] = true;
     }
-    Params prm;
+    Params prm{};
     prm.w = static_cast<const uint8_t *>(w);
     prm.ds = ds;
     prm.y = y;
@@ -2889,6 +3010,14 @@ extern "C" int mmq_gemm_q4K_splitk(const void *w, const uint16_t *xa, const uint
     if (ksplit < 1) return MMQ_ERR_SHAPE;
     if (ksplit > 1 && (!part || !counters)) return MMQ_ERR_NULL;
     return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, ksplit, part, counters, stream);
+}
+
+extern "C" int mmq_gemm_q4K_swiglu(const void *w_gu, const uint16_t *xa, const uint32_t *ds, uint16_t *h_xa,
+                                   uint32_t *h_ds, int8_t *h_qs, int T, int F, int K, mmq_stream_t stream)
+{
+    if (F < 64 || F % 64 != 0 || F > (1 << 20)) return MMQ_ERR_SHAPE;
+    if (!h_xa || !h_ds) return MMQ_ERR_NULL;
+    return mmq::launch_q4K_sb(w_gu, xa, ds, nullptr, T, 2 * F, K, 1, nullptr, nullptr, stream, h_xa, h_ds, h_qs);
 }
 
 // Scratch of mmq_gemm_q4K_splitk_static: partial sums and tile counters in

@@ -165,6 +165,42 @@ def gemv(w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
     return out
 
 
+def interleave_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor, F: int) -> torch.Tensor:
+    """The weight layout of gemm_swiglu: gate and up q4_K rows interleaved in groups
+    of 64 rows (a permutation of whole rows; no arithmetic)."""
+    if w_gate.shape != w_up.shape or w_gate.dtype != torch.uint8 or w_gate.numel() % F or F % 64:
+        raise ValueError("gate and up must be uint8 buffers of F rows each, F % 64 == 0")
+    rb = w_gate.numel() // F
+    g = w_gate.reshape(F // 64, 64, rb)
+    u = w_up.reshape(F // 64, 64, rb)
+    return torch.cat([g, u], dim=1).reshape(-1).contiguous()
+
+
+def gemm_swiglu(w_gu: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, F: int, out=None, want_qs: bool = True):
+    """h = silu(X W_gate^T) * (X W_up^T) quantised to q8_1, from the interleaved
+    gate/up weights (interleave_gate_up) and the input's xa/ds planes.
+    Returns (qs or None, ds, xa) of h [T][F]: the operands of the down projection."""
+    T, K = _check_gemm_args("q4_K", w_gu, xa, 2 * F, planes=2)
+    _check_ds(ds, T, K)
+    dev = xa.device
+    if out is not None:
+        hq, hd, hx = out
+        if hd is None or hx is None:
+            raise ValueError("ds and xa buffers required")
+        for t, dt, shape in ((hq, torch.int8, (T, F)), (hd, torch.int32, (T, F // 32)), (hx, torch.float16, (2, T, F))):
+            if t is not None and (t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous()):
+                raise ValueError("bad output buffer")
+    else:
+        hq = torch.empty((T, F), dtype=torch.int8, device=dev) if want_qs else None
+        hd = torch.empty((T, F // 32), dtype=torch.int32, device=dev)
+        hx = torch.empty((2, T, F), dtype=torch.float16, device=dev)
+    with torch.cuda.device(dev):
+        st = load().mmq_gemm_q4K_swiglu(_ptr(w_gu), _ptr(xa), _ptr(ds), _ptr(hx), _ptr(hd), _ptr(hq), T, F, K,
+                                        _stream(dev))
+    _check("mmq_gemm_q4K_swiglu", st)
+    return hq, hd, hx
+
+
 def splitk_sizes(T: int, O: int, K: int, ksplit: int) -> tuple[int, int]:
     """(floats of partial-sum workspace, ints of tile counters) for a split-K q4_K GEMM."""
     pf, nc = ctypes.c_int64(0), ctypes.c_int64(0)

@@ -20,7 +20,7 @@ def test_header_declares_the_boundary():
                      "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K",
                      "mmq_gemm_q4K_splitk", "mmq_splitk_sizes", "mmq_gemm_q4K_splitk_static",
                      "mmq_gemm_q6K_subblock", "mmq_gemm_q4K_small", "mmq_gemm_q4K_small_imma",
-                     "mmq_last_failure_info", "mmq_gemv_q4K", "mmq_gemv_q6K"):
+                     "mmq_last_failure_info", "mmq_gemv_q4K", "mmq_gemv_q6K", "mmq_gemm_q4K_swiglu"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -90,6 +90,14 @@ def test_argument_errors_without_gpu():
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, p, null, null) == -6
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 0, p, p, null) == -1
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, odd, p, null) == -2
+    # fused gate/up + SwiGLU + q8_1: F a multiple of 64, outputs required, alignment
+    assert lib.mmq_gemm_q4K_swiglu(p, p, p, p, p, null, 16, 96, 256, null) == -1       # F % 64
+    assert lib.mmq_gemm_q4K_swiglu(p, p, p, p, p, null, 16, 0, 256, null) == -1        # F < 64
+    assert lib.mmq_gemm_q4K_swiglu(p, p, p, p, p, null, 16, 64, 300, null) == -1       # K % 256
+    assert lib.mmq_gemm_q4K_swiglu(p, p, p, null, p, null, 16, 64, 256, null) == -6    # no h_xa
+    assert lib.mmq_gemm_q4K_swiglu(p, p, p, p, null, null, 16, 64, 256, null) == -6    # no h_ds
+    assert lib.mmq_gemm_q4K_swiglu(p, p, p, odd, p, null, 16, 64, 256, null) == -2
+    assert lib.mmq_gemm_q4K_swiglu(p, p, p, p, p, null, 0, 64, 256, null) == 0          # T == 0 no-op
     # static-scratch variant: oversize requests are refused before anything else
     assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 4096, 4096, 4096, 4, null) == -9
     assert lib.mmq_gemm_q4K_splitk_static(p, p, p, p, 16, 256, 1024, 0, null) == -1

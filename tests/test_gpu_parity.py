@@ -552,3 +552,86 @@ def test_gemm_large_o(ops, orc):
           ("gemv", ops.gemv(wd, xh, ds, O))]
     ops.check_status()
     _full_check(orc, "q4_K", w, x, O, ys)
+
+
+# ------------------------------------------------ chained FFN (SwiGLU) ----
+
+def _swiglu_gpu(ops, w_gate, w_up, x, F):
+    w_gu = ops.interleave_gate_up(_dev(w_gate), _dev(w_up), F)
+    _, ds, _, xa = ops.quantize_q8_1(_dev(x), want_qs=False, want_xh=False)
+    hq, hd, hx = ops.gemm_swiglu(w_gu, xa, ds, F)
+    ops.check_status()
+    return hq.cpu().numpy(), hd.cpu().numpy().view(np.uint32), hx.cpu().numpy()
+
+
+def _f16_scale(ds):
+    return (ds & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64)
+
+
+def test_swiglu_exact_integers(ops, orc):
+    """Gate and up outputs that are exact integers on both sides (unit scales,
+    integer activations with amax 127 in every block so that q = x, every partial
+    sum below 2^24) and gate values >= 512, where e^-g underflows and
+    silu(g) = g exactly: h = g*u is then the same f32 on both sides, so the fused
+    q8_1 codes, scale words and operand planes must equal the oracle's bit for
+    bit.  Two 128-row tiles, ragged T."""
+    rng = np.random.default_rng(11)
+    T, F, K = 9, 128, 512
+    nsb = K // 256
+    w_gate = np.concatenate([pack_q4K_block(1.0, 0.0, rng.integers(1, 8, 8), [0] * 8, rng.integers(1, 16, 256))
+                             for _ in range(F * nsb)])
+    w_up = np.concatenate([pack_q4K_block(1.0, 1.0, rng.integers(0, 8, 8), rng.integers(0, 64, 8),
+                                          rng.integers(0, 16, 256)) for _ in range(F * nsb)])
+    x = rng.integers(1, 128, (T, K)).astype(np.float32)
+    x[:, ::32] = 127.0
+    qs, ds = orc.quantize_q8_1(x)
+    G = orc.gemm("q4_K", w_gate, qs, ds, F)
+    U = orc.gemm("q4_K", w_up, qs, ds, F)
+    assert G.min() >= 512 and np.array_equal(G, np.round(G)) and np.array_equal(U, np.round(U))
+    qs_r, ds_r = orc.quantize_q8_1(orc.swiglu(G, U))
+    hq, hd, hx = _swiglu_gpu(ops, w_gate, w_up, x, F)
+    assert np.array_equal(hq, qs_r)
+    assert np.array_equal(hd, ds_r)
+    hx64 = hx.astype(np.float64)
+    assert np.array_equal(hx64[0] + hx64[1], orc.dequant_q8_1(qs_r, ds_r))
+
+
+def test_swiglu_config2_chain(ops, orc, oracle_ref):
+    """The 7B FFN of config 2 (T = 512, K = 4096, F = 11008) through the fused
+    gate/up + SwiGLU + q8_1 launch and then the down projection, against the
+    oracle's gate and up GEMMs, its SwiGLU and its quantiser.
+    Tolerance rule for the codes: the GPU's gate/up sums differ from the
+    oracle's by at most the GEMM tolerance (TOL * max|G|, TOL * max|U|), which
+    bounds |h_gpu - h_ref| per element by dh = 1.1 TOL max|G| |u| + |g| TOL max|U|
+    (|silu'| <= 1.1, |silu(g)| <= |g|) plus an ulp.  A block's f16 scale may
+    then differ by one f16 step, and a code may differ from the oracle's by one
+    only where the oracle's quotient h/d lies within dh/d of a rounding
+    boundary (n + 1/2); elsewhere codes are equal.  The down projection on the
+    fused operands must match the oracle's down projection on its own codes
+    within TOL."""
+    gg, gu, gd = synth.config(2).gemms
+    _, _, G = oracle_ref(gg)
+    _, _, U = oracle_ref(gu)
+    F = gg.O
+    h = orc.swiglu(G, U)
+    qs_r, ds_r = orc.quantize_q8_1(h)
+    hq, hd, hx = _swiglu_gpu(ops, gg.weights(), gu.weights(), gg.x(), F)
+    hx64 = hx.astype(np.float64)
+    assert np.array_equal(hx64[0] + hx64[1], orc.dequant_q8_1(hq, hd))     # the planes match the codes
+    d16_g, d16_r = (hd & 0xFFFF).astype(np.int64), (ds_r & 0xFFFF).astype(np.int64)
+    assert np.all(np.abs(d16_g - d16_r) <= 1)
+    same = np.repeat(d16_g == d16_r, 32, axis=1)
+    d_r = np.repeat(_f16_scale(ds_r), 32, axis=1)
+    dh = 1.1 * TOL * np.abs(G).max() * np.abs(U) + np.abs(G) * TOL * np.abs(U).max() + np.spacing(np.abs(h))
+    qg, qr = hq.astype(np.int64), qs_r.astype(np.int64)
+    diff = qg != qr
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quot = np.abs(h.astype(np.float64) / d_r)
+        near = np.abs(quot - np.floor(quot) - 0.5) <= dh / d_r + 1e-6
+    assert np.all(np.abs(qg - qr)[same] <= 1)
+    assert np.all(near[diff & same])
+    assert diff.mean() < 1e-3, diff.mean()
+    yd = ops.gemm("q4_K", _dev(gd.weights()), _dev(hx), _dev(hd.view(np.int32)), gd.O)
+    ops.check_status()
+    ref_down = orc.gemm("q4_K", gd.weights(), qs_r, ds_r, gd.O)
+    assert _rel_err(yd.cpu().numpy(), ref_down) <= TOL

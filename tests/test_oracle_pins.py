@@ -344,3 +344,46 @@ def test_oracle_threads_do_not_change_results(orc, fmt):
     y1 = orc.gemm(fmt, w, qs, ds, O, threads=1)
     for nt in (None, 3, 64):
         assert np.array_equal(orc.gemm(fmt, w, qs, ds, O, threads=nt).view(np.uint32), y1.view(np.uint32))
+
+
+# ------------------------------------------------------------ SwiGLU ----
+
+def _silu(orc, x):
+    x = np.asarray(x, np.float32)
+    return orc.swiglu(x, np.ones_like(x))
+
+
+def test_swiglu_identities(orc):
+    """silu pinned by identities of the function, not by its formula:
+    silu(0) = 0; silu(x) - silu(-x) = x (odd part); silu(x) = x once e^-x is
+    below half an f32 ulp of 1 (x >= 17); silu(x) = -0 where e^-x overflows;
+    h is linear in u (times 2 is exact)."""
+    assert _silu(orc, [0.0])[0] == 0.0
+    x = np.linspace(-30.0, 30.0, 6001, dtype=np.float32)
+    d = _silu(orc, x).astype(np.float64) - _silu(orc, -x).astype(np.float64)
+    assert np.all(np.abs(d - x) <= 4 * np.spacing(np.maximum(np.abs(x), 1.0).astype(np.float32)))
+    big = np.array([17.0, 20.0, 100.0, 1e4, 3e38], np.float32)
+    assert np.array_equal(_silu(orc, big), big)
+    neg = np.array([-89.0, -100.0, -1e4], np.float32)
+    out = _silu(orc, neg)
+    assert np.all(out == 0.0) and np.all(np.signbit(out))
+    rng = np.random.default_rng(3)
+    g = rng.standard_normal(1000).astype(np.float32) * 8
+    u = rng.standard_normal(1000).astype(np.float32)
+    assert np.array_equal(orc.swiglu(g, 2 * u), 2 * orc.swiglu(g, u))
+    # sign: silu(x) > 0 for x > 0 and < 0 for x < 0, |silu(x)| < |x| below 17
+    s = _silu(orc, x)
+    assert np.all(s[x > 0] > 0) and np.all(s[x < 0] < 0)
+    mid = (np.abs(x) < 16) & (x != 0)
+    assert np.all(np.abs(s[mid]) < np.abs(x[mid]))
+
+
+def test_swiglu_against_closed_form_values(orc):
+    """silu(x) = x / (1 + e^-x) against values of the same function evaluated in
+    f64 by Python's math.exp: within 2 f32 ulps (expf and the f32 division each
+    round once)."""
+    import math
+    xs = np.array([-8.0, -2.5, -1.0, -0.5, 0.25, 1.0, 3.0, 7.5], np.float32)
+    ref = np.array([float(v) / (1.0 + math.exp(-float(v))) for v in xs])
+    got = _silu(orc, xs).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2 * np.spacing(np.abs(ref).astype(np.float32)))
