@@ -51,7 +51,9 @@
  *     xa  uint16   [2][T][K]  the dequantised value v = f32(d)*q as two f16
  *                             planes, hi = f16(v) then lo = f16(v - hi); both
  *                             are exact and hi + lo == v (v is a multiple of
- *                             2^-24 with at most 18 significant bits): the
+ *                             2^-24 with at most 18 significant bits) as long
+ *                             as |v| <= 65504, the f16 range (activations of
+ *                             larger magnitude overflow the hi plane): the
  *                             operand of the production GEMMs;
  *     ds  uint32   [T][K/32]  low 16 bits: f16 d of the 32-block,
  *                             high 16 bits: int16 sum of its 32 values.

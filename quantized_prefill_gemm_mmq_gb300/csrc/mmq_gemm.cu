@@ -1106,10 +1106,30 @@ __device__ __forceinline__ uint32_t magic2(uint32_t x, uint32_t sel, __half2 m, 
     return q4::h2bits(__hfma2(*reinterpret_cast<const __half2 *>(&h), m, a));
 }
 
+// SwiGLU pass: gate [128][GU_STRIDE] then up [128][GU_STRIDE] f32 in the operand
+// ring (a row stride of 17 x 16 bytes puts eight consecutive tokens' 16-byte
+// accesses in eight different bank groups)
+constexpr int GU_STRIDE = 68;
+static_assert(2 * BM * GU_STRIDE * 4 <= STG * STAGE_BYTES, "SwiGLU staging fits the operand ring");
+
 // silu(g) * u in f32: g / (1 + e^-g) with each operation rounded once (no contraction)
 __device__ __forceinline__ float swiglu_f32(float g, float u)
 {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+// round_half_away(x / d) with the quotient rounded to f32 as IEEE division
+// does, without the division where the result cannot depend on it: with
+// r = fl(1/d), z = fl(x * r) is within |y| * 2^-22 of the correctly rounded
+// quotient fl(y) (y = x / d), which for |y| <= 127.5 is below 2^-14; unless z
+// lies within 2^-14 of a half-integer (or r is not a finite normal number)
+// both round to the same integer, and otherwise the IEEE quotient is taken.
+__device__ __forceinline__ int q8_round_quotient(float x, float d, float r)
+{
+    const float z = x * r;
+    const float a = fabsf(z);
+    if (r < 1e30f && a < 128.0f && fabsf(a - floorf(a) - 0.5f) > 0x1p-14f) return (int)roundf(z);
+    return (int)roundf(__fdiv_rn(x, d));
 }
 
 }  // namespace q4s
@@ -1379,90 +1399,14 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             if (lane == 0) mbar_arrive(acc_empty(slot));
         }
         if constexpr (SWIGLU) {
-            // ---------------------------------------------- SwiGLU + q8_1 --
-            // Columns 0..63 of this tile are gate rows of features 64*bx ..,
-            // columns 64..127 the up rows of the same features.  The gate
-            // thread of token t hands its gate values 32..63 to the up thread
-            // of t, which hands back up values 0..31 (through the operand ring,
-            // idle now that every MMA has completed); then each computes
-            // h = silu(g)*u for 32 features (one q8_1 block) and quantises it
-            // exactly as mmq_quantize_q8_1 does.
-            constexpr int XS = 36;   // floats per token row: 16-byte stores of 8 lanes in 8 bank groups
-            float *xg = reinterpret_cast<float *>(smem + oStage);
-            float *xu = xg + BM * XS;
-            const bool gate = c0 == 0;
-            auto finish = [&](auto gate_tag) {
-                constexpr bool G = decltype(gate_tag)::value;
-                float *mine = (G ? xg : xu) + tl * XS;
+            // Park the tile in shared memory for the CTA-wide SwiGLU pass at the
+            // end (the operand ring is idle now that every MMA has completed):
+            // columns 0..63 are the gate rows of features 64*bx .., columns
+            // 64..127 the up rows of the same features.
+            float *gu = reinterpret_cast<float *>(smem + oStage) + (c0 ? BM * q4s::GU_STRIDE : 0) + tl * q4s::GU_STRIDE;
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4 *>(mine + i) =
-                        G ? make_float4(yv[32 + i], yv[33 + i], yv[34 + i], yv[35 + i])
-                          : make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
-                named_bar_sync(1, NUM_EPI_WARPS * 32);
-                const float *oth = (G ? xu : xg) + tl * XS;
-                float h[32];
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 o4 = *reinterpret_cast<const float4 *>(oth + i);
-                    const float ov[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        h[i + j] = G ? q4s::swiglu_f32(yv[i + j], ov[j]) : q4s::swiglu_f32(ov[j], yv[32 + i + j]);
-                }
-                if (!(ok && tok_ok)) return;
-                const int F = O >> 1;
-                float amax = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-                const float d32 = amax != 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f;
-                const __half dh = __float2half_rn(d32);
-                const float df = __half2float(dh);
-                const int f0 = blockIdx.x * 64 + (G ? 0 : 32);
-                uint4 *ph = reinterpret_cast<uint4 *>(p.h_xa + (size_t)t * F + f0);
-                uint4 *pl = reinterpret_cast<uint4 *>(p.h_xa + (size_t)T * F + (size_t)t * F + f0);
-                uint32_t qw[8];
-                int ssum = 0;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t hw[4], lw[4];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const int i = 8 * c + e;
-                        int qa = 0, qb = 0;
-                        if (amax != 0.0f) {
-                            qa = min(127, max(-127, (int)roundf(__fdiv_rn(h[i], d32))));
-                            qb = min(127, max(-127, (int)roundf(__fdiv_rn(h[i + 1], d32))));
-                        }
-                        ssum += qa + qb;
-                        const uint32_t pair = (uint32_t)(uint8_t)qa | ((uint32_t)(uint8_t)qb << 8);
-                        if ((i & 2) == 0)
-                            qw[i >> 2] = pair;
-                        else
-                            qw[i >> 2] |= pair << 16;
-                        // v = f32(d16)*q exact in f32; hi = f16(v), lo = f16(v - hi), both exact
-                        const float2 v = make_float2(df * (float)qa, df * (float)qb);
-                        const __half2 hv = __float22half2_rn(v);
-                        const float2 bv = __half22float2(hv);
-                        const __half2 lv = __float22half2_rn(make_float2(v.x - bv.x, v.y - bv.y));
-                        hw[e >> 1] = q4::h2bits(hv);
-                        lw[e >> 1] = q4::h2bits(lv);
-                    }
-                    ph[c] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    pl[c] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                }
-                p.h_ds[(size_t)t * (F / 32) + f0 / 32] =
-                    (uint32_t)__half_as_ushort(dh) | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
-                if (p.h_qs != nullptr) {
-                    uint4 *pq = reinterpret_cast<uint4 *>(p.h_qs + (size_t)t * F + f0);
-                    pq[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-                    pq[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-                }
-            };
-            if (gate)
-                finish(std::true_type{});
-            else
-                finish(std::false_type{});
+            for (int i = 0; i < 64; i += 4)
+                *reinterpret_cast<float4 *>(gu + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
         }
         const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
         auto store_row = [&](float *row) {
@@ -1612,6 +1556,76 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (SWIGLU) {
+        // ------------------------------------- SwiGLU + q8_1, all threads --
+        // Thread i takes half hh = i % 2 (16 features) of q8_1 block
+        // blk = (i / 2) % 2 of token tl = i / 4: h = silu(g)*u for its 16
+        // features, then the block's amax and sum through the lane pair, and
+        // the block quantised exactly as mmq_quantize_q8_1 quantises.
+        const int i = threadIdx.x;
+        const int hh = i & 1, blk = (i >> 1) & 1, tl = i >> 2;
+        const int t = t0 + tl;
+        const int j0 = 32 * blk + 16 * hh;   // first feature of this thread within the tile
+        const float *gp = reinterpret_cast<const float *>(smem + oStage) + tl * q4s::GU_STRIDE + j0;
+        const float *up = gp + BM * q4s::GU_STRIDE;
+        float h[16];
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
+            const float4 g4 = *reinterpret_cast<const float4 *>(gp + c);
+            const float4 u4 = *reinterpret_cast<const float4 *>(up + c);
+            h[c] = q4s::swiglu_f32(g4.x, u4.x);
+            h[c + 1] = q4s::swiglu_f32(g4.y, u4.y);
+            h[c + 2] = q4s::swiglu_f32(g4.z, u4.z);
+            h[c + 3] = q4s::swiglu_f32(g4.w, u4.w);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) amax = fmaxf(amax, fabsf(h[c]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const float d32 = amax != 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f;
+        const float rd = amax != 0.0f ? __frcp_rn(d32) : 0.0f;
+        const __half dh = __float2half_rn(d32);
+        const float df = __half2float(dh);
+        uint32_t hw[8], lw[8], qw[4];
+        int ssum = 0;
+#pragma unroll
+        for (int c = 0; c < 16; c += 2) {
+            int qa = 0, qb = 0;
+            if (amax != 0.0f) {
+                qa = min(127, max(-127, q4s::q8_round_quotient(h[c], d32, rd)));
+                qb = min(127, max(-127, q4s::q8_round_quotient(h[c + 1], d32, rd)));
+            }
+            ssum += qa + qb;
+            const uint32_t pair = (uint32_t)(uint8_t)qa | ((uint32_t)(uint8_t)qb << 8);
+            if ((c & 2) == 0)
+                qw[c >> 2] = pair;
+            else
+                qw[c >> 2] |= pair << 16;
+            // v = f32(d16)*q exact in f32; hi = f16(v), lo = f16(v - hi), both exact
+            const float2 v = make_float2(df * (float)qa, df * (float)qb);
+            const __half2 hv = __float22half2_rn(v);
+            const float2 bv = __half22float2(hv);
+            const __half2 lv = __float22half2_rn(make_float2(v.x - bv.x, v.y - bv.y));
+            hw[c >> 1] = q4::h2bits(hv);
+            lw[c >> 1] = q4::h2bits(lv);
+        }
+        ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+        if (t < T && *abort_flag == 0u) {
+            const int F = O >> 1;
+            const int f0 = blockIdx.x * 64 + j0;
+            uint4 *ph = reinterpret_cast<uint4 *>(p.h_xa + (size_t)t * F + f0);
+            uint4 *pl = reinterpret_cast<uint4 *>(p.h_xa + (size_t)T * F + (size_t)t * F + f0);
+            ph[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            ph[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+            pl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            pl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+            if (hh == 0)
+                p.h_ds[(size_t)t * (F / 32) + f0 / 32] =
+                    (uint32_t)__half_as_ushort(dh) | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
+            if (p.h_qs != nullptr)
+                *reinterpret_cast<uint4 *>(p.h_qs + (size_t)t * F + f0) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+        }
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);

@@ -569,25 +569,28 @@ def _f16_scale(ds):
 
 
 def test_swiglu_exact_integers(ops, orc):
-    """Gate and up outputs that are exact integers on both sides (unit scales,
-    integer activations with amax 127 in every block so that q = x, every partial
-    sum below 2^24) and gate values >= 512, where e^-g underflows and
-    silu(g) = g exactly: h = g*u is then the same f32 on both sides, so the fused
-    q8_1 codes, scale words and operand planes must equal the oracle's bit for
-    bit.  Two 128-row tiles, ragged T."""
+    """Gate and up outputs that are exact on both sides (power-of-two weight
+    scales, integer activations with amax 127 in every block so that q = x,
+    every partial sum an integer below 2^24 times the scale) and gate values
+    >= 17, where e^-g is below half an f32 ulp of 1 and silu(g) = g exactly:
+    h = g*u is then the same f32 on both sides, so the fused q8_1 codes, scale
+    words and operand planes must equal the oracle's bit for bit.  Two 128-row
+    tiles, ragged T."""
     rng = np.random.default_rng(11)
     T, F, K = 9, 128, 512
     nsb = K // 256
-    w_gate = np.concatenate([pack_q4K_block(1.0, 0.0, rng.integers(1, 8, 8), [0] * 8, rng.integers(1, 16, 256))
-                             for _ in range(F * nsb)])
-    w_up = np.concatenate([pack_q4K_block(1.0, 1.0, rng.integers(0, 8, 8), rng.integers(0, 64, 8),
+    w_gate = np.concatenate([pack_q4K_block(2.0 ** -12, 0.0, rng.integers(1, 8, 8), [0] * 8,
+                                            rng.integers(1, 16, 256)) for _ in range(F * nsb)])
+    w_up = np.concatenate([pack_q4K_block(2.0 ** -12, 2.0 ** -12, rng.integers(0, 8, 8), rng.integers(0, 64, 8),
                                           rng.integers(0, 16, 256)) for _ in range(F * nsb)])
     x = rng.integers(1, 128, (T, K)).astype(np.float32)
     x[:, ::32] = 127.0
     qs, ds = orc.quantize_q8_1(x)
     G = orc.gemm("q4_K", w_gate, qs, ds, F)
     U = orc.gemm("q4_K", w_up, qs, ds, F)
-    assert G.min() >= 512 and np.array_equal(G, np.round(G)) and np.array_equal(U, np.round(U))
+    assert G.min() >= 17 and np.array_equal(G * 4096, np.round(G * 4096)) and \
+        np.array_equal(U * 4096, np.round(U * 4096))
+    assert np.abs(G * U).max() < 65504            # the xa planes hold |v| within the f16 range
     qs_r, ds_r = orc.quantize_q8_1(orc.swiglu(G, U))
     hq, hd, hx = _swiglu_gpu(ops, w_gate, w_up, x, F)
     assert np.array_equal(hq, qs_r)
