@@ -49,6 +49,15 @@ def lib():
         L.orc_gemm_mt.argtypes = [i32, P, P, P, i32, i32, i32, P, i64, i32]
         L.orc_max_threads.restype = i32
         L.orc_swiglu.argtypes = [P, P, i64, P]
+        L.orc_q5K_quant.argtypes = [P, i32]
+        L.orc_q5K_quant.restype = i32
+        L.orc_q8_0_quant.argtypes = [P, i32]
+        L.orc_q8_0_quant.restype = i32
+        L.orc_q8_0_d.argtypes = [P]
+        L.orc_q8_0_d.restype = ctypes.c_float
+        L.orc_dequant_q5K.argtypes = [P, i32, i32, P]
+        L.orc_dequant_q8_0.argtypes = [P, i32, i32, P]
+        L.orc_subdots_b32.argtypes = [i32, P, P, i32, i32, i32, P]
         L.orc_version.restype = i32
         _lib = L
     return _lib
@@ -62,8 +71,13 @@ def _p(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
+# bytes per 256 weights of one row, and the format code of the C side
+BYTES_PER_256 = {"q4_K": 144, "q6_K": 210, "q5_K": 176, "q8_0": 8 * 34}
+FMT_CODE = {"q4_K": 4, "q6_K": 6, "q5_K": 5, "q8_0": 8}
+
+
 def _check_w(w: np.ndarray, fmt: str, O: int, K: int) -> np.ndarray:
-    bb = {"q4_K": 144, "q6_K": 210}[fmt]
+    bb = BYTES_PER_256[fmt]
     w = _c(w, np.uint8)
     if K % 256 or w.size != O * (K // 256) * bb:
         raise ValueError("weight buffer does not match O, K")
@@ -100,6 +114,17 @@ def q4K_quants(blk: np.ndarray) -> np.ndarray:
     return np.array([lib().orc_q4K_quant(_p(blk), e) for e in range(256)], np.int32)
 
 
+def q5K_quants(blk: np.ndarray) -> np.ndarray:
+    blk = _c(blk, np.uint8)
+    return np.array([lib().orc_q5K_quant(_p(blk), e) for e in range(256)], np.int32)
+
+
+def q8_0_block(blk: np.ndarray):
+    """(d, the 32 int8 quants) of one 34-byte q8_0 block."""
+    blk = _c(blk, np.uint8)
+    return lib().orc_q8_0_d(_p(blk)), np.array([lib().orc_q8_0_quant(_p(blk), i) for i in range(32)], np.int32)
+
+
 def q6K_quants(blk: np.ndarray) -> np.ndarray:
     blk = _c(blk, np.uint8)
     return np.array([lib().orc_q6K_quant(_p(blk), e) for e in range(256)], np.int32)
@@ -108,7 +133,8 @@ def q6K_quants(blk: np.ndarray) -> np.ndarray:
 def dequant(fmt: str, w: np.ndarray, O: int, K: int) -> np.ndarray:
     w = _check_w(w, fmt, O, K)
     out = np.empty((O, K), np.float64)
-    fn = lib().orc_dequant_q4K if fmt == "q4_K" else lib().orc_dequant_q6K
+    fn = {"q4_K": lib().orc_dequant_q4K, "q6_K": lib().orc_dequant_q6K, "q5_K": lib().orc_dequant_q5K,
+          "q8_0": lib().orc_dequant_q8_0}[fmt]
     fn(_p(w), O, K, _p(out))
     return out
 
@@ -139,11 +165,14 @@ def dequant_q8_1(qs: np.ndarray, ds: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------- GEMM --
 
 def subdots(fmt: str, w: np.ndarray, qs: np.ndarray, O: int) -> np.ndarray:
-    """Per-sub-block int32 dots: [T][O][K/32] (q4_K) or [T][O][K/16] (q6_K)."""
+    """Per-sub-block int32 dots: [T][O][K/32] (q4_K, q5_K, q8_0) or [T][O][K/16] (q6_K)."""
     qs = _c(qs, np.int8)
     T, K = qs.shape
     w = _check_w(w, fmt, O, K)
-    if fmt == "q4_K":
+    if fmt in ("q5_K", "q8_0"):
+        out = np.empty((T, O, K // 32), np.int32)
+        lib().orc_subdots_b32(FMT_CODE[fmt], _p(w), _p(qs), T, O, K, _p(out))
+    elif fmt == "q4_K":
         out = np.empty((T, O, K // 32), np.int32)
         lib().orc_subdots_q4K(_p(w), _p(qs), T, O, K, _p(out))
     else:
@@ -161,11 +190,11 @@ def gemm(fmt: str, w: np.ndarray, qs: np.ndarray, ds: np.ndarray, O: int, thread
     T, K = qs.shape
     w = _check_w(w, fmt, O, K)
     y = np.empty((T, O), np.float32)
-    if threads == 1:
+    if threads == 1 and fmt in ("q4_K", "q6_K"):
         fn = lib().orc_gemm_q4K if fmt == "q4_K" else lib().orc_gemm_q6K
         fn(_p(w), _p(qs), _p(ds), T, O, K, _p(y), O)
     else:
-        lib().orc_gemm_mt(6 if fmt == "q6_K" else 4, _p(w), _p(qs), _p(ds), T, O, K, _p(y), O,
+        lib().orc_gemm_mt(FMT_CODE[fmt], _p(w), _p(qs), _p(ds), T, O, K, _p(y), O,
                           0 if threads is None else int(threads))
     return y
 

@@ -37,6 +37,17 @@
  *      stored d = f16 round-to-nearest-even of d32; an all-zero block gets
  *      d = 0, q = 0, ssum = 0.
  *   R8 q6_K sub-block dot is taken on the centred value q-32.
+ *   R15 q5_K layout (a sibling of q4_K in the same k-quant family; the pages
+ *      name the family, not this member's bytes): the GGUF order, 176 bytes
+ *      = d, dmin (f16), the 12 scale/min bytes packed as q4_K's (R2), qh[32]
+ *      at +16 and qs[128] at +48; element 32j+i takes q4_K's nibble of qs
+ *      (R3) as its low 4 bits and bit j of qh[i] as bit 4, so q is 0..31 and
+ *      w = d*sc_j*q - dmin*m_j.  Parity unpinned w.r.t. GGUF interoperability.
+ *   R16 q8_0 layout: 34 bytes per 32 weights, f16 d then 32 int8 values,
+ *      w = d*q; blocks of a row contiguous.  Its dot follows the pages' fold
+ *      with the scale d_w of the weight block in place of d*sc and no min
+ *      term: y += (dx*d_w)*C_b, C_b the exact integer dot of the 32 int8
+ *      weights with the 32 int8 activations.
  *   R14 FFN activation between the gate/up and down projections of the pages'
  *      7B workload ([r28] 5 "Results": whole-model prefill): the pages print
  *      none; the reading is the LLaMA-family SwiGLU h = silu(g) * u with
@@ -57,6 +68,8 @@
 #define ORC_QK8 32
 #define ORC_Q4K_BYTES 144
 #define ORC_Q6K_BYTES 210
+#define ORC_Q5K_BYTES 176
+#define ORC_Q8_0_BYTES 34
 
 /* ---------------------------------------------------------------- f16 -- */
 
@@ -132,6 +145,31 @@ int orc_q4K_quant(const uint8_t *blk, int e)
     return (j % 2 == 0) ? (byte & 0x0f) : (byte >> 4);
 }
 
+/* ------------------------------------------------------- q5_K decode -- */
+
+/* 5-bit quant (0..31) of element e (0..255) of one 176-byte block (R15). */
+int orc_q5K_quant(const uint8_t *blk, int e)
+{
+    const int j = e / 32, i = e % 32;
+    const uint8_t byte = blk[48 + 32 * (j / 2) + i];
+    const int lo = (j % 2 == 0) ? (byte & 0x0f) : (byte >> 4);
+    const int hi = (blk[16 + i] >> j) & 1;
+    return lo | (hi << 4);
+}
+
+/* ------------------------------------------------------- q8_0 decode -- */
+
+/* int8 quant of element i (0..31) of one 34-byte block (R16). */
+int orc_q8_0_quant(const uint8_t *blk, int i)
+{
+    return (int)(int8_t)blk[2 + i];
+}
+
+float orc_q8_0_d(const uint8_t *blk)
+{
+    return orc_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+}
+
 /* ------------------------------------------------------- q6_K decode -- */
 
 /* 6-bit quant (0..63) of element e (0..255) of one 210-byte block
@@ -163,6 +201,7 @@ float orc_q6K_d(const uint8_t *blk)
     return orc_f16_to_f32((uint16_t)(blk[208] | (blk[209] << 8)));
 }
 
+/* d and dmin of a q4_K or q5_K block (the first four bytes, R1). */
 static float q4K_d(const uint8_t *blk)
 {
     return orc_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
@@ -190,6 +229,35 @@ void orc_dequant_q4K(const uint8_t *w, int O, int K, double *out)
                 out[(size_t)o * K + (size_t)sb * ORC_QK + e] =
                     d * sc * orc_q4K_quant(blk, e) - dmin * m;
             }
+        }
+}
+
+/* W[o][k] as f64: d*sc*q - dmin*m with 5-bit q (R15). */
+void orc_dequant_q5K(const uint8_t *w, int O, int K, double *out)
+{
+    const int nsb = K / ORC_QK;
+    for (int o = 0; o < O; ++o)
+        for (int sb = 0; sb < nsb; ++sb) {
+            const uint8_t *blk = w + ((size_t)o * nsb + sb) * ORC_Q5K_BYTES;
+            const double d = q4K_d(blk), dmin = q4K_dmin(blk);
+            for (int e = 0; e < ORC_QK; ++e) {
+                int sc, m;
+                orc_q4K_scale_min(blk + 4, e / 32, &sc, &m);
+                out[(size_t)o * K + (size_t)sb * ORC_QK + e] = d * sc * orc_q5K_quant(blk, e) - dmin * m;
+            }
+        }
+}
+
+/* W[o][k] as f64: d*q (R16). */
+void orc_dequant_q8_0(const uint8_t *w, int O, int K, double *out)
+{
+    const int nb = K / 32;
+    for (int o = 0; o < O; ++o)
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t *blk = w + ((size_t)o * nb + b) * ORC_Q8_0_BYTES;
+            const double d = orc_q8_0_d(blk);
+            for (int i = 0; i < 32; ++i)
+                out[(size_t)o * K + (size_t)b * 32 + i] = d * orc_q8_0_quant(blk, i);
         }
 }
 
@@ -263,6 +331,43 @@ static int32_t subdot_q6K(const uint8_t *blk, int u, const int8_t *a)
     return c;
 }
 
+/* C[j] over a 32-weight q5_K sub-block: 5-bit quant times int8 activation. */
+static int32_t subdot_q5K(const uint8_t *blk, int j, const int8_t *a)
+{
+    int32_t c = 0;
+    for (int i = 0; i < 32; ++i)
+        c += orc_q5K_quant(blk, 32 * j + i) * (int32_t)a[32 * j + i];
+    return c;
+}
+
+/* C_b of a q8_0 block: int8 weight times int8 activation over 32 (R16). */
+static int32_t subdot_q8_0(const uint8_t *blk, const int8_t *a)
+{
+    int32_t c = 0;
+    for (int i = 0; i < 32; ++i) c += orc_q8_0_quant(blk, i) * (int32_t)a[i];
+    return c;
+}
+
+/* out: [T][O][K/32] int32 (q5_K and q8_0: fmt 5 / 8). */
+void orc_subdots_b32(int fmt, const uint8_t *w, const int8_t *qs, int T, int O, int K, int32_t *out)
+{
+    const int nb = K / 32;
+    for (int t = 0; t < T; ++t)
+        for (int o = 0; o < O; ++o)
+            for (int b = 0; b < nb; ++b) {
+                const int8_t *a = qs + (size_t)t * K;
+                int32_t c;
+                if (fmt == 5) {
+                    const uint8_t *blk = w + ((size_t)o * (K / ORC_QK) + b / 8) * ORC_Q5K_BYTES;
+                    c = subdot_q5K(blk, b % 8, a + (size_t)(b / 8) * ORC_QK);
+                } else {
+                    const uint8_t *blk = w + ((size_t)o * nb + b) * ORC_Q8_0_BYTES;
+                    c = subdot_q8_0(blk, a + (size_t)b * 32);
+                }
+                out[((size_t)t * O + o) * nb + b] = c;
+            }
+}
+
 /* out: [T][O][K/32] int32. */
 void orc_subdots_q4K(const uint8_t *w, const int8_t *qs, int T, int O, int K, int32_t *out)
 {
@@ -322,6 +427,53 @@ static float point_q4K(const uint8_t *wrow, const int8_t *qrow, const uint32_t *
             acc += (double)t1;
             acc += (double)t2;
         }
+    }
+    return (float)acc;
+}
+
+/* One output of the q5_K GEMM: the q4_K method form (above) with the 5-bit
+ * quant (R15). */
+static float point_q5K(const uint8_t *wrow, const int8_t *qrow, const uint32_t *dsrow, int K)
+{
+    const int nsb = K / ORC_QK;
+    double acc = 0.0;
+    for (int sb = 0; sb < nsb; ++sb) {
+        const uint8_t *blk = wrow + (size_t)sb * ORC_Q5K_BYTES;
+        const float d = q4K_d(blk), dmin = q4K_dmin(blk);
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            orc_q4K_scale_min(blk + 4, j, &sc, &m);
+            const float dsv = d * (float)sc;
+            const float dmv = -(dmin * (float)m);
+            const uint32_t dsb = dsrow[sb * 8 + j];
+            const float dx = act_d(dsb);
+            const int ssum = act_ssum(dsb);
+            const int32_t c = subdot_q5K(blk, j, qrow + (size_t)sb * ORC_QK);
+            const float dxs = dx * dsv;
+            const float t1 = dxs * (float)c;
+            const float dma = dx * (float)ssum;
+            const float t2 = dma * dmv;
+            acc += (double)t1;
+            acc += (double)t2;
+        }
+    }
+    return (float)acc;
+}
+
+/* One output of the q8_0 GEMM (R16): per 32-block b, t = (dx_b*d_w)*C_b in
+ * f32, acc += t in f64. */
+static float point_q8_0(const uint8_t *wrow, const int8_t *qrow, const uint32_t *dsrow, int K)
+{
+    const int nb = K / 32;
+    double acc = 0.0;
+    for (int b = 0; b < nb; ++b) {
+        const uint8_t *blk = wrow + (size_t)b * ORC_Q8_0_BYTES;
+        const float dw = orc_q8_0_d(blk);
+        const float dx = act_d(dsrow[b]);
+        const int32_t c = subdot_q8_0(blk, qrow + (size_t)b * 32);
+        const float dxs = dx * dw;
+        const float t = dxs * (float)c;
+        acc += (double)t;
     }
     return (float)acc;
 }
@@ -417,7 +569,8 @@ void orc_swiglu(const float *g, const float *u, int64_t n, float *h)
 void orc_gemm_mt(int fmt, const uint8_t *w, const int8_t *qs, const uint32_t *ds,
                  int T, int O, int K, float *y, int64_t ldy, int nthreads)
 {
-    const size_t bb = (fmt == 6) ? ORC_Q6K_BYTES : ORC_Q4K_BYTES;
+    const size_t bb = (fmt == 6) ? ORC_Q6K_BYTES : (fmt == 5) ? ORC_Q5K_BYTES : (fmt == 8) ? 8 * ORC_Q8_0_BYTES
+                                                                                  : ORC_Q4K_BYTES;
     const size_t row_bytes = (size_t)(K / ORC_QK) * bb;
 #ifdef _OPENMP
     if (nthreads <= 0) nthreads = omp_get_max_threads();
@@ -428,7 +581,10 @@ void orc_gemm_mt(int fmt, const uint8_t *w, const int8_t *qs, const uint32_t *ds
         for (int t = 0; t < T; ++t) {
             const int8_t *qrow = qs + (size_t)t * K;
             const uint32_t *dsrow = ds + (size_t)t * (K / 32);
-            y[(size_t)t * ldy + o] = (fmt == 6) ? point_q6K(wrow, qrow, dsrow, K) : point_q4K(wrow, qrow, dsrow, K);
+            y[(size_t)t * ldy + o] = (fmt == 6)   ? point_q6K(wrow, qrow, dsrow, K)
+                                     : (fmt == 5) ? point_q5K(wrow, qrow, dsrow, K)
+                                     : (fmt == 8) ? point_q8_0(wrow, qrow, dsrow, K)
+                                                  : point_q4K(wrow, qrow, dsrow, K);
         }
     }
     (void)nthreads;

@@ -27,6 +27,9 @@ Distributions (the pages' 7B-class workload, redrawn synthetically):
   zero allowed).
 * q6_K: ``ql`` and ``qh`` bytes uniform (so every 6-bit q is uniform on
   0..63); scales uniform int8 on -64..63; ``d = f16(|N(0, 1e-3)|)``.
+* q5_K (176 B: d, dmin, scales as q4_K, ``qh[32]``, ``qs[128]``): bytes
+  uniform, so every 5-bit q is uniform on 0..31; q8_0 (34 B per 32: f16
+  ``d``, 32 int8): values uniform on -127..127, ``d`` as above.
 """
 from __future__ import annotations
 
@@ -38,6 +41,8 @@ QK_K = 256            # weights per k-quant super-block
 QK8_1 = 32            # activations per q8_1 block
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
+Q5K_BLOCK_BYTES = 176
+Q8_0_BLOCK_BYTES = 34
 
 
 def _f16_bits(values: np.ndarray) -> np.ndarray:
@@ -95,11 +100,52 @@ def make_q6K(O: int, K: int, seed: int) -> np.ndarray:
     return blk.reshape(O, nsb * Q6K_BLOCK_BYTES)
 
 
+def make_q5K(O: int, K: int, seed: int) -> np.ndarray:
+    """Random q5_K weight bytes, shape [O, K/256*176] uint8: d, dmin and the
+    12 scale bytes as make_q4K, qh and qs bytes uniform (every 5-bit q uniform
+    on 0..31)."""
+    if K % QK_K:
+        raise ValueError("K must be a multiple of 256")
+    nsb = K // QK_K
+    rng = np.random.default_rng(seed)
+    d = _abs_normal_f16_bits(rng, (O, nsb))
+    dmin = _abs_normal_f16_bits(rng, (O, nsb))
+    scales = rng.integers(0, 256, size=(O, nsb, 12), dtype=np.uint8)
+    qh = rng.integers(0, 256, size=(O, nsb, 32), dtype=np.uint8)
+    qs = rng.integers(0, 256, size=(O, nsb, 128), dtype=np.uint8)
+    blk = np.empty((O, nsb, Q5K_BLOCK_BYTES), dtype=np.uint8)
+    blk[:, :, 0:2] = d.view(np.uint8).reshape(O, nsb, 2)
+    blk[:, :, 2:4] = dmin.view(np.uint8).reshape(O, nsb, 2)
+    blk[:, :, 4:16] = scales
+    blk[:, :, 16:48] = qh
+    blk[:, :, 48:176] = qs
+    return blk.reshape(O, nsb * Q5K_BLOCK_BYTES)
+
+
+def make_q8_0(O: int, K: int, seed: int) -> np.ndarray:
+    """Random q8_0 weight bytes, shape [O, K/32*34] uint8: d = f16(|N(0, 1e-3)|),
+    32 int8 values uniform on -127..127 per block."""
+    if K % QK_K:
+        raise ValueError("K must be a multiple of 256")
+    nb = K // 32
+    rng = np.random.default_rng(seed)
+    d = _abs_normal_f16_bits(rng, (O, nb))
+    q = rng.integers(-127, 128, size=(O, nb, 32)).astype(np.int8)
+    blk = np.empty((O, nb, Q8_0_BLOCK_BYTES), dtype=np.uint8)
+    blk[:, :, 0:2] = d.view(np.uint8).reshape(O, nb, 2)
+    blk[:, :, 2:34] = q.view(np.uint8)
+    return blk.reshape(O, nb * Q8_0_BLOCK_BYTES)
+
+
 def make_weights(fmt: str, O: int, K: int, seed: int) -> np.ndarray:
     if fmt == "q4_K":
         return make_q4K(O, K, seed)
     if fmt == "q6_K":
         return make_q6K(O, K, seed)
+    if fmt == "q5_K":
+        return make_q5K(O, K, seed)
+    if fmt == "q8_0":
+        return make_q8_0(O, K, seed)
     raise ValueError(f"unknown weight format {fmt!r}")
 
 
@@ -202,4 +248,6 @@ def layer_7b(T: int = 512) -> Workload:
 
 
 def block_bytes(fmt: str) -> int:
-    return {"q4_K": Q4K_BLOCK_BYTES, "q6_K": Q6K_BLOCK_BYTES}[fmt]
+    """Bytes per 256 weights of one row."""
+    return {"q4_K": Q4K_BLOCK_BYTES, "q6_K": Q6K_BLOCK_BYTES, "q5_K": Q5K_BLOCK_BYTES,
+            "q8_0": 8 * Q8_0_BLOCK_BYTES}[fmt]

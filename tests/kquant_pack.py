@@ -12,6 +12,9 @@ statements of the pages and the readings recorded in the design notes:
 * 12-byte scale packing: GGUF k-quant packing (a reading; the pages elide it).
 * q6_K (210 B): ql[128], qh[64], int8 scales[16], d f16 (GGUF order, a
   reading; the pages list the fields only).
+* q5_K (176 B): d, dmin, the q4_K scale packing, qh[32], qs[128] (GGUF
+  order, a reading: the pages name only the k-quant family); q8_0 (34 B):
+  f16 d and 32 int8 values.
 """
 from __future__ import annotations
 
@@ -71,4 +74,33 @@ def pack_q6K_block(d: float, sc, q) -> np.ndarray:
             blk[128 + 32 * h + l] = (q0 >> 4) | ((q1 >> 4) << 2) | ((q2 >> 4) << 4) | ((q3 >> 4) << 6)
     blk[192:208] = sc.astype(np.int8).view(np.uint8)
     blk[208:210] = np.array([f16_bits(d)], np.uint16).view(np.uint8)
+    return blk
+
+
+def pack_q5K_block(d: float, dmin: float, sc, m, q) -> np.ndarray:
+    """One 176-byte q5_K block (d, dmin, the q4_K scale packing, qh[32], qs[128])
+    from 8 scales, 8 mins and 256 values q in 0..31: the low 4 bits go where
+    q4_K keeps its nibble, bit 4 of element 32j+i into bit j of qh[i]."""
+    q = np.asarray(q, np.int64)
+    assert q.shape == (256,) and q.min() >= 0 and q.max() <= 31
+    blk = np.zeros(176, np.uint8)
+    blk[0:2] = np.array([f16_bits(d)], np.uint16).view(np.uint8)
+    blk[2:4] = np.array([f16_bits(dmin)], np.uint16).view(np.uint8)
+    blk[4:16] = pack_q4K_scales(sc, m)
+    qh = np.zeros(32, np.int64)
+    for e in range(256):
+        j, i = divmod(e, 32)
+        qh[i] |= ((q[e] >> 4) & 1) << j
+    blk[16:48] = qh.astype(np.uint8)
+    blk[48:176] = pack_q4K_qs(q & 15)
+    return blk
+
+
+def pack_q8_0_block(d: float, q) -> np.ndarray:
+    """One 34-byte q8_0 block: f16 d, then 32 int8 values."""
+    q = np.asarray(q, np.int64)
+    assert q.shape == (32,) and q.min() >= -128 and q.max() <= 127
+    blk = np.zeros(34, np.uint8)
+    blk[0:2] = np.array([f16_bits(d)], np.uint16).view(np.uint8)
+    blk[2:34] = q.astype(np.int8).view(np.uint8)
     return blk

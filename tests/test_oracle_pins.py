@@ -12,7 +12,7 @@ import os
 import numpy as np
 import pytest
 
-from tests.kquant_pack import (f16_bits, pack_q4K_block, pack_q4K_qs, pack_q4K_scales,
+from tests.kquant_pack import (f16_bits, pack_q4K_block, pack_q4K_qs, pack_q4K_scales, pack_q5K_block, pack_q8_0_block,
                                pack_q6K_block)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -266,7 +266,7 @@ def test_q8_1_invariants_random(orc):
 
 # ------------------------------------------- fold identity (P-e) ----
 
-@pytest.mark.parametrize("fmt", ["q4_K", "q6_K"])
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q5_K", "q8_0"])
 @pytest.mark.parametrize("T,O,K", [(3, 5, 256), (7, 4, 768), (16, 9, 1024)])
 def test_method_form_matches_full_dequant(orc, fmt, T, O, K):
     from quantized_prefill_gemm_mmq_gb300 import synth
@@ -387,3 +387,101 @@ def test_swiglu_against_closed_form_values(orc):
     ref = np.array([float(v) / (1.0 + math.exp(-float(v))) for v in xs])
     got = _silu(orc, xs).astype(np.float64)
     assert np.all(np.abs(got - ref) <= 2 * np.spacing(np.abs(ref).astype(np.float32)))
+
+
+
+# ------------------------------------------------------- q5_K and q8_0 ----
+
+def test_q5K_values_every_position(orc):
+    """Every 5-bit value at every position reads back (the fifth bit of element
+    32j+i is bit j of qh[i]); the low nibbles sit where q4_K keeps them."""
+    rng = np.random.default_rng(21)
+    for rep in range(40):
+        q = (np.arange(256) * 7 + rep) % 32 if rep < 32 else rng.integers(0, 32, 256)
+        blk = pack_q5K_block(1.0, 0.0, [1] * 8, [0] * 8, q)
+        assert np.array_equal(orc.q5K_quants(blk), q)
+        assert np.array_equal(blk[48:], pack_q4K_qs(np.asarray(q) & 15))
+
+
+def test_q5K_high_bits_one_at_a_time(orc):
+    """Setting one bit of qh moves exactly one element up by 16."""
+    base = pack_q5K_block(1.0, 0.0, [1] * 8, [0] * 8, np.zeros(256, np.int64))
+    for i in range(32):
+        for j in range(8):
+            blk = base.copy()
+            blk[16 + i] = 1 << j
+            want = np.zeros(256, np.int64)
+            want[32 * j + i] = 16
+            assert np.array_equal(orc.q5K_quants(blk), want)
+
+
+def test_q5K_one_hot_reads_back_weights(orc):
+    rng = np.random.default_rng(22)
+    q = rng.integers(0, 32, 256)
+    sc = rng.integers(0, 64, 8)
+    m = rng.integers(0, 64, 8)
+    blk = pack_q5K_block(1.0, 1.0, sc, m, q)
+    x = 127.0 * np.eye(256, dtype=np.float32)
+    qs, ds = orc.quantize_q8_1(x)
+    y = orc.gemm("q5_K", blk, qs, ds, 1)[:, 0]
+    want = np.array([sc[k // 32] * q[k] - m[k // 32] for k in range(256)], np.float64)
+    assert np.array_equal(y / 127.0, want)
+    assert np.array_equal(orc.dequant("q5_K", blk, 1, 256)[0], want)
+
+
+def test_q5K_single_superblock_closed_form(orc):
+    """All 5-bit values 17 (both the low nibble and the fifth bit in use), d =
+    dmin = 1, X = 127: C = 127*17*32 = 69088 per sub-block, so
+    Y = 69088*sum(sc) - 4064*sum(m) = 69088*259 - 4064*261 = 16,833,088 (even,
+    so exact in f32 above 2^24)."""
+    sc = [63, 1, 32, 17, 48, 5, 60, 33]
+    m = [0, 63, 16, 47, 31, 62, 2, 40]
+    blk = pack_q5K_block(1.0, 1.0, sc, m, np.full(256, 17))
+    x = np.full((1, 256), 127.0, np.float32)
+    qs, ds = orc.quantize_q8_1(x)
+    assert np.all(orc.subdots("q5_K", blk, qs, 1) == 69088)
+    assert orc.gemm("q5_K", blk, qs, ds, 1)[0, 0] == 16833088.0
+    assert orc.gemm_dequant("q5_K", blk, qs, ds, 1)[0, 0] == 16833088.0
+
+
+def test_q8_0_every_byte_value(orc):
+    """Every int8 value at every position of a block reads back, with its d."""
+    for shift in range(0, 256, 32):
+        q = ((np.arange(32) + shift) % 256) - 128
+        blk = pack_q8_0_block(0.5, q)
+        d, got = orc.q8_0_block(blk)
+        assert d == 0.5 and np.array_equal(got, q)
+
+
+def test_q8_0_one_hot_reads_back_weights(orc):
+    """K = 256 (8 blocks with different d): Y/127 = d_b * q for every k."""
+    rng = np.random.default_rng(23)
+    ds_w = [0.25, 0.5, 1.0, 2.0, 0.125, 4.0, 1.5, 0.75]
+    qv = rng.integers(-128, 128, (8, 32))
+    blk = np.concatenate([pack_q8_0_block(ds_w[b], qv[b]) for b in range(8)])
+    x = 127.0 * np.eye(256, dtype=np.float32)
+    qs, ds = orc.quantize_q8_1(x)
+    y = orc.gemm("q8_0", blk, qs, ds, 1)[:, 0]
+    want = np.array([ds_w[k // 32] * qv[k // 32, k % 32] for k in range(256)], np.float64)
+    assert np.array_equal(y / 127.0, want)
+    assert np.array_equal(orc.dequant("q8_0", blk, 1, 256)[0], want)
+
+
+@pytest.mark.parametrize("T,O,K", [(1, 1, 256), (2, 3, 256), (3, 2, 512)])
+def test_q5K_q8_0_subdots_brute_force(orc, T, O, K):
+    rng = np.random.default_rng(T * 100 + O * 10 + K + 1)
+    nsb = K // 256
+    q5 = rng.integers(0, 32, (O, K))
+    q8 = rng.integers(-128, 128, (O, K))
+    w5 = np.concatenate([pack_q5K_block(1.0, 1.0, rng.integers(0, 64, 8), rng.integers(0, 64, 8),
+                                        q5[o, 256 * s: 256 * s + 256]) for o in range(O) for s in range(nsb)])
+    w8 = np.concatenate([pack_q8_0_block(1.0, q8[o, 32 * b: 32 * b + 32]) for o in range(O) for b in range(K // 32)])
+    a = rng.integers(-127, 128, (T, K)).astype(np.int8)
+    got5 = orc.subdots("q5_K", w5, a, O)
+    got8 = orc.subdots("q8_0", w8, a, O)
+    for t in range(T):
+        for o in range(O):
+            for b in range(K // 32):
+                sl = slice(32 * b, 32 * b + 32)
+                assert got5[t, o, b] == int(np.dot(q5[o, sl], a[t, sl].astype(np.int64)))
+                assert got8[t, o, b] == int(np.dot(q8[o, sl], a[t, sl].astype(np.int64)))
