@@ -3,7 +3,7 @@
  *
  *     Y[T x O] = X[T x K] . W[O x K]^T
  *
- * with W stored in a k-quant format (q4_K or q6_K) and X quantised per
+ * with W stored in a k-quant format (q4_K, q6_K, q5_K) or q8_0 and X quantised per
  * 32-element block to q8_1.  The method is the one described on the
  * "minfer" CUDA optimisation pages for the q4_K MMQ line:
  *   - "31 . r28 -- Direction-A raw-nibble NB kernel, 2 blocks/SM", section
@@ -305,6 +305,37 @@ int mmq_gemm_q6K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds,
                           float *y, int T, int O, int K, mmq_stream_t stream);
 
 /*
+ * q5_K x q8_1 GEMM, the sibling of q4_K in the same k-quant family (the pages
+ * run the "q4_K line" and "q6_K line" of one skeleton, "43 . r40", 6; the
+ * q5_K bytes are the GGUF layout, a reading): 176-byte super-blocks of 256
+ * weights, d and dmin (f16) and the 12 scale/min bytes exactly as q4_K,
+ * qh[32] at bytes 16-47, qs[128] at 48-175; weight 32j+i of a super-block
+ * has q = (q4_K's nibble of qs for element 32j+i) + 16 * (bit j of qh[i]),
+ * 0..31, and w = d*sc_j*q - dmin*m_j.
+ * The q4_K fold and the production form of mmq_gemm_q4K (sc*q <= 1953 is
+ * exact in f16).  w: O*(K/256)*176 bytes; xa, ds, y, limits as mmq_gemm_q4K.
+ * mmq_gemm_q5K_subblock: the pages' per-sub-block form (exact integer dots
+ * C_b, f32 fold per 32-weight sub-block) from xh, as mmq_gemm_q4K_subblock.
+ */
+int mmq_gemm_q5K(const void *w, const uint16_t *xa, const uint32_t *ds,
+                 float *y, int T, int O, int K, mmq_stream_t stream);
+int mmq_gemm_q5K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds,
+                          float *y, int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * q8_0 x q8_1 GEMM: 34-byte blocks of 32 weights (f16 d, then 32 int8 values,
+ * w = d*q; GGUF's q8_0, a reading), rows of K/32 blocks.  The pages' fold
+ * with the weight block's scale in place of d*sc and no min term:
+ * y[t][o] = sum_b (dx_b*d_b)*C_b, C_b the exact integer dot of the 32 int8
+ * weights with the 32 int8 activations, formed by the tensor core (exact f16
+ * operands) per block and folded in f32.  xh, ds: as written by
+ * mmq_quantize_q8_1.  w: O*(K/32)*34 bytes, K % 256 == 0; other limits as
+ * mmq_gemm_q4K.
+ */
+int mmq_gemm_q8_0(const void *w, const uint16_t *xh, const uint32_t *ds,
+                  float *y, int T, int O, int K, mmq_stream_t stream);
+
+/*
  * Diagnostic: the per-sub-block exact integer dots the GEMMs fold, through
  * the same tensor-core pipeline.  out: int32 [T][O][K/32] for q4_K
  * (C_b = sum q*a over 32 weights) or [T][O][K/16] for q6_K
@@ -315,6 +346,11 @@ int mmq_debug_subdots_q4K(const void *w, const uint16_t *xh, int32_t *out,
                           int T, int O, int K, mmq_stream_t stream);
 int mmq_debug_subdots_q6K(const void *w, const uint16_t *xh, int32_t *out,
                           int T, int O, int K, mmq_stream_t stream);
+/* The same for q5_K and q8_0: int32 [T][O][K/32]. */
+int mmq_debug_subdots_q5K(const void *w, const uint16_t *xh, int32_t *out,
+                          int T, int O, int K, mmq_stream_t stream);
+int mmq_debug_subdots_q8_0(const void *w, const uint16_t *xh, int32_t *out,
+                           int T, int O, int K, mmq_stream_t stream);
 
 /*
  * Diagnostic: measured warp-level tensor throughput of the current device,

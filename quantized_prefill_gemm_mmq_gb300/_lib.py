@@ -34,6 +34,11 @@ SIGNATURES = {
     "mmq_gemm_q4K_splitk_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "mmq_gemm_q4K_swiglu": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_gemm_q5K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_gemm_q5K_subblock": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_gemm_q8_0": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_debug_subdots_q5K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
+    "mmq_debug_subdots_q8_0": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemm_q6K_subblock": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q4K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_debug_subdots_q6K": (_I, [_P, _P, _P, _I, _I, _I, _P]),

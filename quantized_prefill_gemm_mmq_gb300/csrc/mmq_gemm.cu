@@ -43,7 +43,7 @@
 namespace mmq {
 namespace {
 
-enum { kQ4K = 0, kQ6K = 1 };
+enum { kQ4K = 0, kQ6K = 1, kQ5K = 2, kQ8_0 = 3 };
 enum { kFold = 0, kSubdots = 1 };
 
 constexpr int BM = 128;           // tokens per tile: MMA M, TMEM lanes
@@ -76,6 +76,20 @@ struct Fmt<kQ6K> {
     static constexpr int kRawRow = 224;     // 210 bytes + up to 14 bytes of lead-in
     static constexpr int kKSub = 16;
     static constexpr int kSdsEntry = 4;     // float d*sc
+};
+template <>
+struct Fmt<kQ5K> {                          // d, dmin, scales as q4_K; qh[32] at +16, qs[128] at +48
+    static constexpr int kBlockBytes = 176;
+    static constexpr int kRawRow = 176;
+    static constexpr int kKSub = 32;
+    static constexpr int kSdsEntry = 8;     // float2 (d*sc, -dmin*m)
+};
+template <>
+struct Fmt<kQ8_0> {                         // per 256 weights: eight 34-byte blocks (f16 d, 32 int8)
+    static constexpr int kBlockBytes = 272;
+    static constexpr int kRawRow = 272;
+    static constexpr int kKSub = 32;
+    static constexpr int kSdsEntry = 4;     // float d of the block
 };
 
 template <int FMT>
@@ -163,6 +177,15 @@ __device__ __forceinline__ uint32_t nib_hi2(uint32_t w, uint32_t sel)
     return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// two f16 values from the low 5 bits of bytes (sel) of w (each byte 0..31), exact
+__device__ __forceinline__ uint32_t u5_2(uint32_t w, uint32_t sel)
+{
+    const uint32_t p = __byte_perm(w, 0u, sel);
+    const uint32_t h = (p & 0x001F001Fu) | 0x64006400u;           // 1024 + v in each half
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&h), __half2half2(__ushort_as_half(0x6400)));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 __device__ __forceinline__ uint32_t pack_h2(int a, int b)
 {
     const __half2 h = __halves2half2(__int2half_rn(a), __int2half_rn(b));
@@ -176,7 +199,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 {
     using F = Fmt<FMT>;
     using L = Layout<FMT>;
-    constexpr int kKid = 1 + FMT * 2 + MODE;
+    constexpr int kKid = FMT < 2 ? 1 + FMT * 2 + MODE : 20 + (FMT - 2) * 2 + MODE;
     constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -211,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(st_empty(s), 1);
         }
         for (int s = 0; s < RAW_STAGES; ++s) {
-            mbar_init(r_full(s), FMT == kQ4K ? 1 : 32);   // q6_K: every producer lane arrives
+            mbar_init(r_full(s), FMT == kQ6K ? 32 : 1);   // q6_K: every producer lane arrives
             mbar_init(r_empty(s), 128);
         }
         for (int s = 0; s < SDS_STAGES; ++s) {
@@ -239,7 +262,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------ TMA producer --
         if (lane == 0) {
             tma_prefetch(&tmA);
-            if (FMT == kQ4K) tma_prefetch(&tmW);
+            if (FMT != kQ6K) tma_prefetch(&tmW);
         }
         int n_a = 0, n_r = 0;   // loads issued, for the drain on abort
         bool ok = true;
@@ -249,10 +272,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ok = mbar_wait_warp(r_empty(rs), ((sb / RAW_STAGES) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
                 if (!ok) break;
                 const uint32_t dst = sbase + L::oRaw + rs * L::kRawBytes;
-                if (FMT == kQ4K) {
+                if (FMT != kQ6K) {
+                    // one 2-D box of 128 rows x the super-block's bytes (q8_0: counted in
+                    // 16-bit elements, the box's inner extent being limited to 256 elements)
                     if (lane == 0) {
                         mbar_arrive_expect_tx(r_full(rs), L::kRawBytes);
-                        tma_load_2d(dst, &tmW, r_full(rs), sb * F::kBlockBytes, o0);
+                        tma_load_2d(dst, &tmW, r_full(rs), sb * (FMT == kQ8_0 ? F::kBlockBytes / 2 : F::kBlockBytes),
+                                    o0);
                     }
                 } else {
                     // one bulk copy per row: the 16-byte-aligned 224-byte window
@@ -348,7 +374,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             const uint8_t *raw = smem + L::oRaw + rs * L::kRawBytes + r * F::kRawRow;
             uint8_t *sds = smem + L::oSds + ss * L::kSdsBytes;
-            if (FMT == kQ4K) {
+            if (FMT == kQ8_0) {
+                // the eight blocks' d (rows past O arrive zero-filled)
+                float *sd1 = reinterpret_cast<float *>(sds);
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    sd1[g * BN + r] = __half2float(__ushort_as_half(
+                        (unsigned short)(raw[34 * g] | (raw[34 * g + 1] << 8))));
+            } else if (FMT == kQ4K || FMT == kQ5K) {
                 // header: d, dmin (f16), 12 bytes of 6-bit scales / mins
                 const uint4 hd = *reinterpret_cast<const uint4 *>(raw);
                 const float d = __half2float(__ushort_as_half((unsigned short)(hd.x & 0xFFFFu)));
@@ -380,7 +413,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ok = mbar_wait(st_empty(s), ((ks / STAGES) & 1) ^ 1, abort_flag, kKid, SITE_U_STAGE);
                 if (!ok) break;
                 uint8_t *brow = smem + L::oB + s * B_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
-                if (FMT == kQ4K) {
+                if (FMT == kQ8_0) {
+                    // stage p4 = blocks 2*p4, 2*p4 + 1: 64 int8 values (2-byte aligned), exact in f16
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint8_t *qb = raw + 34 * (2 * p4 + (c >> 2)) + 2 + 8 * (c & 3);
+                        int v[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i += 2) {
+                            const uint32_t two = *reinterpret_cast<const uint16_t *>(qb + i);
+                            v[i] = (int)(int8_t)(two & 0xFFu);
+                            v[i + 1] = (int)(int8_t)(two >> 8);
+                        }
+                        uint4 q;
+                        q.x = pack_h2(v[0], v[1]);
+                        q.y = pack_h2(v[2], v[3]);
+                        q.z = pack_h2(v[4], v[5]);
+                        q.w = pack_h2(v[6], v[7]);
+                        *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = q;
+                    }
+                } else if (FMT == kQ5K) {
+                    // stage p4 = sub-blocks 2*p4 (low nibbles) and 2*p4+1 (high nibbles) of quant
+                    // bytes 32*p4 .. +31 at +48, each with its fifth bit from qh at +16 (bit 2*p4 or
+                    // 2*p4 + 1 of qh[l])
+                    const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + 48 + 32 * p4);
+                    const uint4 w1 = *reinterpret_cast<const uint4 *>(raw + 48 + 32 * p4 + 16);
+                    const uint4 h0 = *reinterpret_cast<const uint4 *>(raw + 16);
+                    const uint4 h1 = *reinterpret_cast<const uint4 *>(raw + 32);
+                    const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int j = 2 * p4 + (c >> 2);            // sub-block
+                        const uint32_t qa = wv[2 * (c & 3)], qb = wv[2 * (c & 3) + 1];
+                        const uint32_t ba = ((hv[2 * (c & 3)] >> j) & 0x01010101u) << 4;
+                        const uint32_t bb = ((hv[2 * (c & 3) + 1] >> j) & 0x01010101u) << 4;
+                        const uint32_t va = ((c < 4 ? qa : (qa >> 4)) & 0x0F0F0F0Fu) | ba;
+                        const uint32_t vb = ((c < 4 ? qb : (qb >> 4)) & 0x0F0F0F0Fu) | bb;
+                        uint4 v;
+                        v.x = u5_2(va, 0x4140u);
+                        v.y = u5_2(va, 0x4342u);
+                        v.z = u5_2(vb, 0x4140u);
+                        v.w = u5_2(vb, 0x4342u);
+                        *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = v;
+                    }
+                } else if (FMT == kQ4K) {
                     // stage p4 = sub-blocks 2*p4 (low nibbles, k 0..31) and 2*p4+1
                     // (high nibbles, k 32..63) of quant bytes 32*p4 .. 32*p4+31
                     const uint4 w0 = *reinterpret_cast<const uint4 *>(raw + 16 + 32 * p4);
@@ -462,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ok = mbar_wait_warp(acc_full(slot), (acc / ACC_SLOTS) & 1, abort_flag, kKid, SITE_E_ACC);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t dword = dsrow ? __ldg(dsrow + (FMT == kQ4K ? g : (g >> 1))) : 0u;
+                const uint32_t dword = dsrow ? __ldg(dsrow + (F::kKSub == 32 ? g : (g >> 1))) : 0u;
                 const float dx = __half2float(__ushort_as_half((unsigned short)(dword & 0xFFFFu)));
                 const float dma = dx * (float)(int)(int16_t)(dword >> 16);
 #pragma unroll
@@ -477,7 +554,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const int cbase = c0 + hh * 32;
                     if (MODE == kFold) {
-                        if (FMT == kQ4K) {
+                        if (FMT == kQ4K || FMT == kQ5K) {
                             const float2 *sd2 = reinterpret_cast<const float2 *>(sds) + g * BN + cbase;
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) {
@@ -1076,25 +1153,32 @@ constexpr uint32_t TM_EVEN = 0, TM_ODD = NACC * BN;
 static_assert(TM_ODD + NACC * BN <= 512, "TMEM budget");
 constexpr uint32_t A_STAGE = 2 * A_BYTES;         // hi and lo planes
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_BYTES;
-constexpr uint32_t RAW_BYTES = BN * 144;
 constexpr uint32_t MIN_OP_BYTES = 128 * 64;
 constexpr uint32_t SDS_D = 2 * MIN_OP_BYTES;
 constexpr uint32_t SDS_BYTES = SDS_D + BN * 4;
 constexpr int SBAR = 2 * STG;                     // full / empty barriers: stage ks uses ks % SBAR
 constexpr uint32_t oStage = 0;
-constexpr uint32_t oRaw = oStage + STG * STAGE_BYTES;
-constexpr uint32_t oSds = oRaw + RSTG * RAW_BYTES;
-constexpr uint32_t oBar = oSds + SSTG * SDS_BYTES;
+constexpr uint32_t oRaw = oStage + STG * STAGE_BYTES;   // then the raw ring, scale ring and barriers (SbLayout)
 // full, empty [SBAR]; s_full [SSTG]; acc_full, acc_empty [NACC] (shared by the
 // even and odd accumulators of a super-block); r_full, r_empty [RSTG];
 // done [2] (each issuer's stage completions); mma_done
 constexpr int kNumBars = 2 * SBAR + SSTG + 2 * NACC + 2 * RSTG + 2 + 1;
-constexpr uint32_t oMisc = oBar + kNumBars * 8;
-constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
-static_assert(kDynSmem <= 232448, "shared memory budget");
-static_assert(STAGE_BYTES % 1024 == 0 && oRaw % 1024 == 0 && RAW_BYTES % 1024 == 0, "ring alignment");
-static_assert(oSds % 16 == 0 && SDS_BYTES % 16 == 0, "min operands must be 16-byte aligned");
+static_assert(STAGE_BYTES % 1024 == 0 && oRaw % 1024 == 0 && SDS_BYTES % 16 == 0, "ring alignment");
 static_assert(NACC >= SSTG, "a scale slot is rewritten only after its accumulator was released");
+
+// Per-format part of the layout: the raw ring holds the rows' whole blocks
+// (q4_K 144 bytes, q5_K 176), everything after it moves with its size.
+template <int FMT>
+struct SbLayout {
+    static constexpr int RAW_ROW = FMT == kQ5K ? 176 : 144;
+    static constexpr uint32_t RAW_BYTES = BN * RAW_ROW;
+    static constexpr uint32_t oSds = oRaw + RSTG * RAW_BYTES;
+    static constexpr uint32_t oBar = oSds + SSTG * SDS_BYTES;
+    static constexpr uint32_t oMisc = oBar + kNumBars * 8;
+    static constexpr uint32_t kDynSmem = oMisc + 16 + 1024;
+    static_assert(kDynSmem <= 232448, "shared memory budget");
+    static_assert(RAW_BYTES % 1024 == 0 && oSds % 16 == 0, "ring alignment");
+};
 
 // Two f16 values sc*q from the two bytes of x selected by sel (x holds the
 // quants already masked: q in the low nibble, or 16q in the high nibble):
@@ -1136,12 +1220,17 @@ __device__ __forceinline__ int q8_round_quotient(float x, float d, float r)
 
 // SWIGLU: the tile's output is not stored as y but finished as silu(gate)*up and
 // quantised to q8_1 (Params::h_xa).
-template <bool SWIGLU>
+// FMT: kQ4K, or kQ5K (the same header and scale packing, a 5-bit quant whose
+// fifth bits come from a 32-byte qh plane: sc*q <= 1953 is still exact in f16).
+template <int FMT, bool SWIGLU>
 __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     mmq_q4K_sb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                       const Params p)
 {
     using namespace q4s;
+    using SL = SbLayout<FMT>;
+    constexpr int RAW_ROW = SL::RAW_ROW;
+    constexpr uint32_t RAW_BYTES = SL::RAW_BYTES, oSds = SL::oSds, oBar = SL::oBar, oMisc = SL::oMisc;
     constexpr int kKid = 9;
     constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
     constexpr uint32_t kIdescTf32 = idesc_tf32_f32(BM, BN);
@@ -1282,17 +1371,18 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         if (r == 0) {
             tma_prefetch(&tmW);
             mbar_arrive_expect_tx(r_full(0), RAW_BYTES);
-            tma_load_2d(sbase + oRaw, &tmW, r_full(0), sb_base * 144, o0);
+            tma_load_2d(sbase + oRaw, &tmW, r_full(0), sb_base * RAW_ROW, o0);
             n_raw = 1;
         }
         for (int sb = 0; sb < nsb && ok; ++sb) {
             const int rs = sb % RSTG;
             ok = mbar_wait(r_full(rs), (sb / RSTG) & 1, abort_flag, kKid, SITE_U_RAW);
             if (!ok) break;
-            uint4 cur[9];
-            const uint4 *raw = reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + r * 144);
+            constexpr int NCUR = RAW_ROW / 16;   // q4_K: header + 8 quant words; q5_K: + 2 qh words
+            uint4 cur[NCUR];
+            const uint4 *raw = reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + r * RAW_ROW);
 #pragma unroll
-            for (int i = 0; i < 9; ++i) cur[i] = raw[i];
+            for (int i = 0; i < NCUR; ++i) cur[i] = raw[i];
             fence_proxy_async_smem();   // these reads before the next TMA write into the slot
             mbar_arrive(r_empty(rs));
             if (r == 0 && sb + 1 < nsb) {
@@ -1300,7 +1390,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 ok = mbar_wait(r_empty(rn), (((sb + 1) / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
                 if (ok) {
                     mbar_arrive_expect_tx(r_full(rn), RAW_BYTES);
-                    tma_load_2d(sbase + oRaw + rn * RAW_BYTES, &tmW, r_full(rn), (sb_base + sb + 1) * 144, o0);
+                    tma_load_2d(sbase + oRaw + rn * RAW_BYTES, &tmW, r_full(rn), (sb_base + sb + 1) * RAW_ROW, o0);
                     n_raw = sb + 2;
                 }
             }
@@ -1313,16 +1403,37 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 const float slo = d_zero ? 0.0f : (float)sc_lo, shi = d_zero ? 0.0f : (float)sc_hi;
                 const __half2 mlo = __float2half2_rn(slo), alo = __float2half2_rn(-1024.0f * slo);
                 const __half2 mhi = __float2half2_rn(shi * 0.0625f), ahi = __float2half2_rn(-64.0f * shi);
+                if constexpr (FMT == kQ5K) {
+                    // 5-bit values: nibble | fifth bit (bit 2*p4 or 2*p4 + 1 of qh[l]) << 4, with
+                    // (m, a) = (sc, -1024 sc) for both sub-blocks
+                    const __half2 mh5 = __float2half2_rn(shi), ah5 = __float2half2_rn(-1024.0f * shi);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 q = cur[1 + 2 * p4 + (c >> 1)];
-                    const uint32_t w_a = (c & 1) ? q.z : q.x, w_b = (c & 1) ? q.w : q.y;
-                    const uint32_t la = w_a & 0x0F0F0F0Fu, lb = w_b & 0x0F0F0F0Fu;
-                    const uint32_t ha = w_a & 0xF0F0F0F0u, hb = w_b & 0xF0F0F0F0u;
-                    vv[c] = make_uint4(q4s::magic2(la, 0x4140u, mlo, alo), q4s::magic2(la, 0x4342u, mlo, alo),
-                                       q4s::magic2(lb, 0x4140u, mlo, alo), q4s::magic2(lb, 0x4342u, mlo, alo));
-                    vv[c + 4] = make_uint4(q4s::magic2(ha, 0x4140u, mhi, ahi), q4s::magic2(ha, 0x4342u, mhi, ahi),
-                                           q4s::magic2(hb, 0x4140u, mhi, ahi), q4s::magic2(hb, 0x4342u, mhi, ahi));
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 q = cur[3 + 2 * p4 + (c >> 1)];
+                        const uint4 hq = cur[1 + (c >> 1)];
+                        const uint32_t w_a = (c & 1) ? q.z : q.x, w_b = (c & 1) ? q.w : q.y;
+                        const uint32_t b_a = (c & 1) ? hq.z : hq.x, b_b = (c & 1) ? hq.w : hq.y;
+                        const uint32_t la = (w_a & 0x0F0F0F0Fu) | (((b_a >> (2 * p4)) & 0x01010101u) << 4);
+                        const uint32_t lb = (w_b & 0x0F0F0F0Fu) | (((b_b >> (2 * p4)) & 0x01010101u) << 4);
+                        const uint32_t ha = ((w_a >> 4) & 0x0F0F0F0Fu) | (((b_a >> (2 * p4 + 1)) & 0x01010101u) << 4);
+                        const uint32_t hb = ((w_b >> 4) & 0x0F0F0F0Fu) | (((b_b >> (2 * p4 + 1)) & 0x01010101u) << 4);
+                        vv[c] = make_uint4(q4s::magic2(la, 0x4140u, mlo, alo), q4s::magic2(la, 0x4342u, mlo, alo),
+                                           q4s::magic2(lb, 0x4140u, mlo, alo), q4s::magic2(lb, 0x4342u, mlo, alo));
+                        vv[c + 4] = make_uint4(q4s::magic2(ha, 0x4140u, mh5, ah5), q4s::magic2(ha, 0x4342u, mh5, ah5),
+                                               q4s::magic2(hb, 0x4140u, mh5, ah5), q4s::magic2(hb, 0x4342u, mh5, ah5));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 q = cur[1 + 2 * p4 + (c >> 1)];
+                        const uint32_t w_a = (c & 1) ? q.z : q.x, w_b = (c & 1) ? q.w : q.y;
+                        const uint32_t la = w_a & 0x0F0F0F0Fu, lb = w_b & 0x0F0F0F0Fu;
+                        const uint32_t ha = w_a & 0xF0F0F0F0u, hb = w_b & 0xF0F0F0F0u;
+                        vv[c] = make_uint4(q4s::magic2(la, 0x4140u, mlo, alo), q4s::magic2(la, 0x4342u, mlo, alo),
+                                           q4s::magic2(lb, 0x4140u, mlo, alo), q4s::magic2(lb, 0x4342u, mlo, alo));
+                        vv[c + 4] = make_uint4(q4s::magic2(ha, 0x4140u, mhi, ahi), q4s::magic2(ha, 0x4342u, mhi, ahi),
+                                               q4s::magic2(hb, 0x4140u, mhi, ahi), q4s::magic2(hb, 0x4342u, mhi, ahi));
+                    }
                 }
             };
             // stage p4's values are converted before waiting for its slot, and
@@ -1503,7 +1614,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             uint4 hdn[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                hdn[h] = *reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + (sr + 64 * h) * 144);
+                hdn[h] = *reinterpret_cast<const uint4 *>(smem + oRaw + rs * RAW_BYTES + (sr + 64 * h) * RAW_ROW);
             fence_proxy_async_smem();   // these reads before the next TMA write into the slot
             mbar_arrive(r_empty(rs));
             if (sb >= SSTG) {
@@ -1635,10 +1746,13 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
 // Production q4_K launch: activations as the [2T][K] f16 hi/lo planes.
 // ksplit <= 1 or part == nullptr: one CTA per output tile covers all of K.
 // With swiglu outputs (h_xa != nullptr): y unused, O = 2F gate/up rows interleaved by 64, no split.
+// fmt: kQ4K or kQ5K (plain y output only for kQ5K).
 int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K, int ksplit,
                   float *part, int *cnt, mmq_stream_t stream, uint16_t *h_xa = nullptr, uint32_t *h_ds = nullptr,
-                  int8_t *h_qs = nullptr)
+                  int8_t *h_qs = nullptr, int fmt = kQ4K)
 {
+    if (fmt == kQ5K && (h_xa || ksplit > 1)) return MMQ_ERR_SHAPE;
+    const int row_bytes = fmt == kQ5K ? 176 : 144;
     if (T < 0 || O < 1 || K < 256 || K > (1 << 20) || (K & 255)) return MMQ_ERR_SHAPE;
     if (h_xa && (O % 128 != 0 || ksplit > 1)) return MMQ_ERR_SHAPE;
     if (T == 0) return MMQ_OK;
@@ -1660,18 +1774,20 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     rc = make_tmap_2d(&tmA, xa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, 2ull * (uint64_t)T, (uint64_t)K * 2, BK,
                       BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MMQ_OK) return rc;
-    rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)nsb * 144, (uint64_t)O, (uint64_t)nsb * 144,
-                      144, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)nsb * row_bytes, (uint64_t)O,
+                      (uint64_t)nsb * row_bytes, row_bytes, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != MMQ_OK) return rc;
     static bool attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return MMQ_ERR_DEVICE;
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(mmq_q4K_sb_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)q4s::kDynSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(mmq_q4K_sb_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)q4s::kDynSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(mmq_q4K_sb_kernel<kQ4K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)q4s::SbLayout<kQ4K>::kDynSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(mmq_q4K_sb_kernel<kQ4K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)q4s::SbLayout<kQ4K>::kDynSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(mmq_q4K_sb_kernel<kQ5K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)q4s::SbLayout<kQ5K>::kDynSmem) != cudaSuccess)
             return launch_status();
         attr_done[dev] = true;
     }
@@ -1690,12 +1806,13 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     prm.h_ds = h_ds;
     prm.h_qs = h_qs;
     const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM), (unsigned)splits);
-    if (h_xa)
-        mmq_q4K_sb_kernel<true><<<grid, q4s::NTHREADS, q4s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
-            tmA, tmW, prm);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (fmt == kQ5K)
+        mmq_q4K_sb_kernel<kQ5K, false><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ5K>::kDynSmem, cs>>>(tmA, tmW, prm);
+    else if (h_xa)
+        mmq_q4K_sb_kernel<kQ4K, true><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ4K>::kDynSmem, cs>>>(tmA, tmW, prm);
     else
-        mmq_q4K_sb_kernel<false><<<grid, q4s::NTHREADS, q4s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(
-            tmA, tmW, prm);
+        mmq_q4K_sb_kernel<kQ4K, false><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ4K>::kDynSmem, cs>>>(tmA, tmW, prm);
     return launch_status();
 }
 
@@ -2950,9 +3067,16 @@ int launch(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int3
     rc = make_tmap_2d(&tmA, xh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK, BM,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MMQ_OK) return rc;
-    if (FMT == kQ4K) {
-        rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)(nsb * 144), (uint64_t)O,
-                          (uint64_t)(nsb * 144), 144, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (FMT == kQ4K || FMT == kQ5K) {
+        const uint64_t rb = (uint64_t)(nsb * Fmt<FMT>::kBlockBytes);
+        rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, rb, (uint64_t)O, rb, Fmt<FMT>::kBlockBytes, BN,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != MMQ_OK) return rc;
+    } else if (FMT == kQ8_0) {
+        // a row of K/32 34-byte blocks viewed as 16-bit elements (K % 256 == 0 makes it 16-byte aligned)
+        const uint64_t rb = (uint64_t)(nsb * 272);
+        rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT16, rb / 2, (uint64_t)O, rb, 136, BN,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != MMQ_OK) return rc;
     } else {
         std::memset(&tmW, 0, sizeof(tmW));   // q6_K stages its rows with plain bulk copies
@@ -2993,6 +3117,13 @@ extern "C" int mmq_gemm_q4K(const void *w, const uint16_t *xa, const uint32_t *d
                             mmq_stream_t stream)
 {
     return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, 1, nullptr, nullptr, stream);
+}
+
+extern "C" int mmq_gemm_q5K(const void *w, const uint16_t *xa, const uint32_t *ds, float *y, int T, int O, int K,
+                            mmq_stream_t stream)
+{
+    return mmq::launch_q4K_sb(w, xa, ds, y, T, O, K, 1, nullptr, nullptr, stream, nullptr, nullptr, nullptr,
+                              mmq::kQ5K);
 }
 
 extern "C" int mmq_gemm_q4K_small_imma(const void *w, const int8_t *qs, const uint32_t *ds, float *y, int T, int O,
@@ -3104,6 +3235,30 @@ extern "C" int mmq_debug_subdots_q4K(const void *w, const uint16_t *xh, int32_t 
                                      mmq_stream_t stream)
 {
     return mmq::launch<mmq::kQ4K, mmq::kSubdots>(w, xh, nullptr, nullptr, out, T, O, K, stream);
+}
+
+extern "C" int mmq_gemm_q5K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O,
+                                     int K, mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ5K, mmq::kFold>(w, xh, ds, y, nullptr, T, O, K, stream);
+}
+
+extern "C" int mmq_gemm_q8_0(const void *w, const uint16_t *xh, const uint32_t *ds, float *y, int T, int O, int K,
+                             mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ8_0, mmq::kFold>(w, xh, ds, y, nullptr, T, O, K, stream);
+}
+
+extern "C" int mmq_debug_subdots_q5K(const void *w, const uint16_t *xh, int32_t *out, int T, int O, int K,
+                                     mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ5K, mmq::kSubdots>(w, xh, nullptr, nullptr, out, T, O, K, stream);
+}
+
+extern "C" int mmq_debug_subdots_q8_0(const void *w, const uint16_t *xh, int32_t *out, int T, int O, int K,
+                                      mmq_stream_t stream)
+{
+    return mmq::launch<mmq::kQ8_0, mmq::kSubdots>(w, xh, nullptr, nullptr, out, T, O, K, stream);
 }
 
 extern "C" int mmq_debug_subdots_q6K(const void *w, const uint16_t *xh, int32_t *out, int T, int O, int K,

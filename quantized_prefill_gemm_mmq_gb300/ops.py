@@ -12,7 +12,7 @@ import torch
 
 from ._lib import MMQError, load
 
-BLOCK_BYTES = {"q4_K": 144, "q6_K": 210}
+BLOCK_BYTES = {"q4_K": 144, "q6_K": 210, "q5_K": 176, "q8_0": 272}   # bytes per 256 weights of a row
 
 
 def _stream(device: torch.device):
@@ -101,12 +101,14 @@ def _check_ds(ds, T, K):
 
 def gemm(fmt: str, w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: int,
          out: torch.Tensor | None = None) -> torch.Tensor:
-    """Production GEMM: Y [T][O] f32 from W (`fmt`) and the xa/ds activation planes
-    (q6_K does not read ds)."""
+    """Production GEMM: Y [T][O] f32 from W (`fmt`: q4_K, q5_K or q6_K) and the xa/ds
+    activation planes (q6_K does not read ds)."""
     T, K = _check_gemm_args(fmt, w, xa, O, planes=2)
     _check_ds(ds, T, K)
     out = _out(out, T, O, xa.device)
-    fn = load().mmq_gemm_q4K if fmt == "q4_K" else load().mmq_gemm_q6K
+    fn = {"q4_K": load().mmq_gemm_q4K, "q6_K": load().mmq_gemm_q6K, "q5_K": load().mmq_gemm_q5K}.get(fmt)
+    if fn is None:
+        raise ValueError(f"no production GEMM for {fmt!r} (q8_0: gemm_subblock)")
     with torch.cuda.device(xa.device):
         st = fn(_ptr(w), _ptr(xa), _ptr(ds), _ptr(out), T, O, K, _stream(xa.device))
     _check(f"gemm({fmt})", st)
@@ -280,11 +282,13 @@ def gemm_splitk_static(w: torch.Tensor, xa: torch.Tensor, ds: torch.Tensor, O: i
 
 def gemm_subblock(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
                   out: torch.Tensor | None = None) -> torch.Tensor:
-    """Per-sub-block GEMM (exact integer sub-block dots + f32 fold) from the xh/ds planes."""
+    """Per-sub-block GEMM (exact integer sub-block dots + f32 fold) from the xh/ds planes;
+    `fmt` q4_K, q5_K, q6_K or q8_0 (q8_0's only form)."""
     T, K = _check_gemm_args(fmt, w, xh, O, planes=1)
     _check_ds(ds, T, K)
     out = _out(out, T, O, xh.device)
-    fn = load().mmq_gemm_q4K_subblock if fmt == "q4_K" else load().mmq_gemm_q6K_subblock
+    fn = {"q4_K": load().mmq_gemm_q4K_subblock, "q6_K": load().mmq_gemm_q6K_subblock,
+          "q5_K": load().mmq_gemm_q5K_subblock, "q8_0": load().mmq_gemm_q8_0}[fmt]
     with torch.cuda.device(xh.device):
         st = fn(_ptr(w), _ptr(xh), _ptr(ds), _ptr(out), T, O, K, _stream(xh.device))
     _check(f"gemm_subblock({fmt})", st)
@@ -292,11 +296,12 @@ def gemm_subblock(fmt: str, w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor,
 
 
 def debug_subdots(fmt: str, w: torch.Tensor, xh: torch.Tensor, O: int) -> torch.Tensor:
-    """Per-sub-block integer dots: int32 [T][O][K/32] (q4_K) or [T][O][K/16] (q6_K)."""
+    """Per-sub-block integer dots: int32 [T][O][K/16] (q6_K) or [T][O][K/32] (the others)."""
     T, K = _check_gemm_args(fmt, w, xh, O, planes=1)
-    nsub = K // 32 if fmt == "q4_K" else K // 16
+    nsub = K // 16 if fmt == "q6_K" else K // 32
     out = torch.empty((T, O, nsub), dtype=torch.int32, device=xh.device)
-    fn = load().mmq_debug_subdots_q4K if fmt == "q4_K" else load().mmq_debug_subdots_q6K
+    fn = {"q4_K": load().mmq_debug_subdots_q4K, "q6_K": load().mmq_debug_subdots_q6K,
+          "q5_K": load().mmq_debug_subdots_q5K, "q8_0": load().mmq_debug_subdots_q8_0}[fmt]
     with torch.cuda.device(xh.device):
         st = fn(_ptr(w), _ptr(xh), _ptr(out), T, O, K, _stream(xh.device))
     _check("mmq_debug_subdots", st)

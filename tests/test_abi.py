@@ -20,7 +20,9 @@ def test_header_declares_the_boundary():
                      "mmq_status_str", "mmq_version", "mmq_debug_subdots_q4K", "mmq_debug_subdots_q6K",
                      "mmq_gemm_q4K_splitk", "mmq_splitk_sizes", "mmq_gemm_q4K_splitk_static",
                      "mmq_gemm_q6K_subblock", "mmq_gemm_q4K_small", "mmq_gemm_q4K_small_imma",
-                     "mmq_last_failure_info", "mmq_gemv_q4K", "mmq_gemv_q6K", "mmq_gemm_q4K_swiglu"):
+                     "mmq_last_failure_info", "mmq_gemv_q4K", "mmq_gemv_q6K", "mmq_gemm_q4K_swiglu",
+                     "mmq_gemm_q5K", "mmq_gemm_q5K_subblock", "mmq_gemm_q8_0", "mmq_debug_subdots_q5K",
+                     "mmq_debug_subdots_q8_0"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -90,6 +92,16 @@ def test_argument_errors_without_gpu():
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, p, null, null) == -6
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 0, p, p, null) == -1
     assert lib.mmq_gemm_q4K_splitk(p, p, p, p, 16, 256, 1024, 4, odd, p, null) == -2
+    # q5_K and q8_0 GEMMs: shapes, nulls, alignment, T == 0
+    for fn in (lib.mmq_gemm_q5K, lib.mmq_gemm_q5K_subblock, lib.mmq_gemm_q8_0):
+        assert fn(p, p, p, p, 1, 1, 300, null) == -1                            # K % 256
+        assert fn(p, p, p, p, 1, 0, 256, null) == -1                            # O < 1
+        assert fn(null, p, p, p, 1, 1, 256, null) == -6
+        assert fn(odd, p, p, p, 1, 1, 256, null) == -2
+        assert fn(p, p, p, p, 0, 1, 256, null) == 0
+    for fn in (lib.mmq_debug_subdots_q5K, lib.mmq_debug_subdots_q8_0):
+        assert fn(p, p, p, 1, 1, 300, null) == -1
+        assert fn(p, p, null, 1, 1, 256, null) == -6
     # fused gate/up + SwiGLU + q8_1: F a multiple of 64, outputs required, alignment
     assert lib.mmq_gemm_q4K_swiglu(p, p, p, p, p, null, 16, 96, 256, null) == -1       # F % 64
     assert lib.mmq_gemm_q4K_swiglu(p, p, p, p, p, null, 16, 0, 256, null) == -1        # F < 64

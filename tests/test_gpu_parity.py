@@ -12,7 +12,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 from quantized_prefill_gemm_mmq_gb300 import synth  # noqa: E402
-from tests.kquant_pack import pack_q4K_block, pack_q6K_block  # noqa: E402
+from tests.kquant_pack import pack_q4K_block, pack_q5K_block, pack_q6K_block, pack_q8_0_block  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -116,7 +116,7 @@ def test_quantize_strided_rows(ops, orc):
 
 # ---------------------------------------------------- sub-block dots ----
 
-@pytest.mark.parametrize("fmt", ["q4_K", "q6_K"])
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K", "q5_K", "q8_0"])
 @pytest.mark.parametrize("T,O,K", [(1, 1, 256), (64, 256, 512), (130, 200, 768), (200, 129, 256)])
 def test_subdots_bit_exact(ops, orc, fmt, T, O, K):
     w = synth.make_weights(fmt, O, K, seed=T + O + K)
@@ -157,7 +157,8 @@ def _run_gemm(ops, fmt, w, x, O, kernel="production"):
     return y.cpu().numpy()
 
 
-KERNELS = [("q4_K", "production"), ("q4_K", "subblock"), ("q6_K", "production"), ("q6_K", "subblock")]
+KERNELS = [("q4_K", "production"), ("q4_K", "subblock"), ("q6_K", "production"), ("q6_K", "subblock"),
+           ("q5_K", "production"), ("q5_K", "subblock"), ("q8_0", "subblock")]
 
 
 @pytest.mark.parametrize("fmt,kernel", KERNELS)
@@ -638,3 +639,59 @@ def test_swiglu_config2_chain(ops, orc, oracle_ref):
     ops.check_status()
     ref_down = orc.gemm("q4_K", gd.weights(), qs_r, ds_r, gd.O)
     assert _rel_err(yd.cpu().numpy(), ref_down) <= TOL
+
+
+
+# -------------------------------------------------------- q5_K, q8_0 ----
+
+def test_subdots_extremes_q5K_q8_0(ops, orc):
+    """The largest dots: 5-bit 31 everywhere, int8 -128 and 127, against +-127."""
+    O, K, T = 3, 256, 4
+    w5 = np.concatenate([pack_q5K_block(1.0, 1.0, [63] * 8, [63] * 8, np.full(256, 31))] * O)
+    w8 = np.concatenate([pack_q8_0_block(1.0, np.full(32, -128 if o % 2 else 127)) for o in range(O) for _ in range(8)])
+    x = np.full((T, K), 127.0, np.float32)
+    x[1] *= -1
+    x[2, ::2] *= -1
+    x[3, :] = 127.0 * ((np.arange(K) % 3) - 1)
+    qs_r, _ = orc.quantize_q8_1(x)
+    _, _, xh, _ = _gpu_quant(ops, x)
+    for fmt, w in (("q5_K", w5), ("q8_0", w8)):
+        assert np.array_equal(ops.debug_subdots(fmt, _dev(w), xh, O).cpu().numpy(), orc.subdots(fmt, w, qs_r, O))
+
+
+def test_q5K_closed_form_superblock(ops):
+    """All 5-bit values 17, d = dmin = 1, X = 127: Y = 16,833,088 exactly."""
+    sc = [63, 1, 32, 17, 48, 5, 60, 33]
+    m = [0, 63, 16, 47, 31, 62, 2, 40]
+    w = pack_q5K_block(1.0, 1.0, sc, m, np.full(256, 17))
+    x = np.full((1, 256), 127.0, np.float32)
+    assert float(_run_gemm(ops, "q5_K", w, x, 1, "production")[0, 0]) == 16833088.0
+    assert float(_run_gemm(ops, "q5_K", w, x, 1, "subblock")[0, 0]) == 16833088.0
+
+
+@pytest.mark.parametrize("fmt,kernel", [("q5_K", "production"), ("q5_K", "subblock"), ("q8_0", "subblock")])
+def test_gemm_q5K_q8_0_7b_shape(ops, orc, fmt, kernel):
+    """A 7B projection shape (T = 512, K = O = 4096) and the FFN down shape
+    (K = 11008) with q5_K and q8_0 weights, every output against the oracle."""
+    for (T, K, O, seed) in ((512, 4096, 4096, 61), (512, 11008, 4096, 62)):
+        w = synth.make_weights(fmt, O, K, seed)
+        x = synth.make_x(T, K, seed + 1, outliers=True)
+        qs_r, ds_r = orc.quantize_q8_1(x)
+        ref = orc.gemm(fmt, w, qs_r, ds_r, O)
+        y = _run_gemm(ops, fmt, w, x, O, kernel)
+        assert _rel_err(y, ref) <= TOL, (fmt, kernel, K)
+
+
+def test_gemm_q8_0_buffer_end_and_zero_scales(ops, orc):
+    """q8_0 rows whose last block ends the buffer (ragged O), blocks with d = 0,
+    and full-range int8 values (-128 included)."""
+    T, O, K = 33, 131, 768
+    w = synth.make_weights("q8_0", O, K, 64).reshape(O, K // 32, 34).copy()
+    rng = np.random.default_rng(65)
+    w[:, :, 2:] = rng.integers(0, 256, size=(O, K // 32, 32), dtype=np.uint8)
+    w[::3, 1, 0:2] = 0                                   # d = 0 in one block of every third row
+    w = w.reshape(-1)
+    x = synth.make_x(T, K, 66, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q8_0", w, qs_r, ds_r, O)
+    assert _rel_err(_run_gemm(ops, "q8_0", w, x, O, "subblock"), ref) <= TOL
