@@ -350,6 +350,37 @@ def sweep_lines(dev, hbm_gbs, mac_peak, fast=False):
     return out
 
 
+def format_lines(dev, mac_peak, T=512, K=4096, O=4096):
+    """Every weight format on one 7B projection shape (T x K -> O), device time
+    per launch with the weights cycled through > 320 MB of copies: the
+    production super-block GEMMs (q4_K, q5_K, q6_K; activation planes xa) and
+    the per-sub-block GEMMs (q4_K, q5_K, q6_K, q8_0; exact integer dots per
+    sub-block, activation plane xh)."""
+    import torch
+    from quantized_prefill_gemm_mmq_gb300 import ops, synth
+    x = torch.from_numpy(synth.make_x(T, K, 700)).to(dev)
+    _, ds, xh, xa = ops.quantize_q8_1(x, want_qs=False)
+    y = torch.empty((T, O), dtype=torch.float32, device=dev)
+    out = []
+    for fmt in ("q4_K", "q5_K", "q6_K", "q8_0"):
+        w0 = torch.from_numpy(synth.make_weights(fmt, O, K, 701)).to(dev)
+        copies = [w0] + [w0.clone() for _ in range(int(320e6 // w0.numel()))]
+        n = 2 * len(copies)
+        kern = {}
+        if fmt != "q8_0":
+            kern["production"] = graph_time_us([lambda w=w: ops.gemm(fmt, w, xa, ds, O, out=y) for w in copies], n=n)
+        kern["subblock"] = graph_time_us([lambda w=w: ops.gemm_subblock(fmt, w, xh, ds, O, out=y) for w in copies],
+                                         n=n)
+        best = min(kern, key=kern.get)
+        tm = T * K * O / (kern[best] * 1e-6) / 1e12
+        out.append({"fmt": fmt, "T": T, "K": K, "O": O, "us": {k: round(v, 2) for k, v in kern.items()}, "best": best,
+                    "tmacs": tm, "f16_dense_frac": tm / mac_peak,
+                    "weight_bytes": int(w0.numel())})
+        del copies
+    ops.check_status(dev)
+    return out
+
+
 def decode_line(dev, layers, groups, xs, hbm_gbs):
     """Side measurement: one decode step (T = 1) of the whole layer stack through
     the decode-shaped kernels: per layer the q8_1 quantisation of the four
@@ -906,9 +937,13 @@ def mmq_arm(args):
                  "bytes": "algorithmic: weights + q8_1 activations (1.125 B/element) + f32 Y",
                  "hbm_peak_gbs": hbm_gbs, "f16_dense_mac_peak_tmacs": mac_peak,
                  "lines": sweep_lines(dev, hbm_gbs, mac_peak)}
-    decode = None
+    decode = formats = None
     if not args.no_small_t and world == 1:
         decode = decode_line(dev, layers, groups, xs, hbm_gbs)
+        formats = {"kernels": "production: mmq_gemm_q4K / _q5K / _q6K; subblock: mmq_gemm_q4K_subblock / "
+                              "q5K_subblock / q6K_subblock and mmq_gemm_q8_0 (per-sub-block form)",
+                   "timing": "CUDA-graph replay cycling through >320 MB of weight copies, device events, best of 5",
+                   "lines": format_lines(dev, mac_peak)}
     line = {
         "metric": METRIC,
         "value": value,
@@ -939,6 +974,7 @@ def mmq_arm(args):
         "gpu_launches": launches_per_step * args.steps,
         "sweep": sweep,
         "decode": decode,
+        "formats": formats,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -373,6 +373,22 @@ int mmq_probe_tensor_peak(int kind, double *tmacs, mmq_stream_t stream);
 int mmq_check_status(mmq_stream_t stream, int *detail);
 
 /*
+ * Test-only: exercises the bounded pipeline waits (the pages' launcher never
+ * runs over its limits silently, "31 . r28", 3.3 Pitfalls; the waits and
+ * this knob are the library's own).  Sets, for the current device, the time a
+ * kernel's pipeline wait may take before it gives up (wait_limit_us > 0; <= 0
+ * restores the default of 2 s) and a mode: 0 = off; 1 = the production q4_K
+ * kernels (mmq_gemm_q4K, mmq_gemm_q4K_splitk*, mmq_gemm_q5K) withhold the raw
+ * weight copy of their second super-block (K >= 512), so the waits for it run
+ * out: the kernel records MMQ_ERR_TIMEOUT (see mmq_check_status), stops every
+ * role, drains the work it issued, frees its tensor memory and returns; its y
+ * is undefined.  Synchronous with respect to the host.  Returns MMQ_OK,
+ * MMQ_ERR_SHAPE (unknown mode) or MMQ_ERR_CUDA.  Leave it at mode 0 outside
+ * tests.
+ */
+int mmq_debug_fault_inject(int mode, int wait_limit_us);
+
+/*
  * More detail on the last failure that mmq_check_status reported (no
  * counterpart on the pages; a diagnostic of the library's own bounded waits): info
  * receives 4 ints: the time the failed wait had waited (microseconds), its

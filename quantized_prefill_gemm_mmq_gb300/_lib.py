@@ -44,6 +44,7 @@ SIGNATURES = {
     "mmq_debug_subdots_q6K": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "mmq_check_status": (_I, [_P, _P]),
     "mmq_last_failure_info": (_I, [_P]),
+    "mmq_debug_fault_inject": (_I, [_I, _I]),
     "mmq_probe_tensor_peak": (_I, [_I, _P, _P]),
 }
 

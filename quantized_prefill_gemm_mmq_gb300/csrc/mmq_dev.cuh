@@ -20,7 +20,14 @@ namespace mmq {
 static __device__ int g_status[8];
 
 constexpr int kStatusTimeout = -5;            // == MMQ_ERR_TIMEOUT
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait (the default)
+
+// Test-only knobs (mmq_debug_fault_inject): the time a pipeline wait may
+// take before it gives up, and a mode in which a kernel withholds one copy so
+// that a wait runs out (the production q4_K kernel skips the raw weight copy
+// of its second super-block).  One copy per translation unit, like g_status.
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+static __device__ int g_inject;
 
 __device__ __forceinline__ uint64_t globaltimer()
 {
@@ -107,8 +114,8 @@ constexpr uint32_t kWaitSleepNs = 20000;     // longest single hardware sleep of
 constexpr uint64_t kPollCreditNs = 1000000;    // most waiting time one poll may add (1 ms)
 
 // Wait for the phase with the given parity to complete.  Gives up (and
-// returns false) when *abort is set by another role, or after kWaitLimitNs
-// of waiting, in which case it records MMQ_ERR_TIMEOUT and raises *abort
+// returns false) when *abort is set by another role, or after g_wait_limit_ns
+// (2 s unless a test lowered it) of waiting, in which case it records MMQ_ERR_TIMEOUT and raises *abort
 // itself.  The time waited is the sum of the global timer's steps between
 // polls, each counted only if positive and at most kPollCreditNs, so that an
 // adjustment of the global timer (backwards or a jump forwards) cannot end a
@@ -125,7 +132,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         const int64_t step = (int64_t)(now - prev);
         prev = now;
         if (step > 0) waited += (uint64_t)step < kPollCreditNs ? (uint64_t)step : kPollCreditNs;
-        if (waited > kWaitLimitNs) {
+        if (waited > g_wait_limit_ns) {
             *abort = 1u;
             record_error(kStatusTimeout, kernel_id, site, (int)(waited / 1000u),
                          (int)(polls < 0x7FFFFFFFu ? polls : 0x7FFFFFFFu), (int)parity, (int)bar);

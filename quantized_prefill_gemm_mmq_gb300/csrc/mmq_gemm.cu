@@ -152,7 +152,7 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity)
         const int64_t step = (int64_t)(now - prev);
         prev = now;
         if (step > 0) waited += (uint64_t)step < kPollCreditNs ? (uint64_t)step : kPollCreditNs;
-        if (waited > kWaitLimitNs) return false;
+        if (waited > g_wait_limit_ns) return false;
     }
     return true;
 }
@@ -1388,7 +1388,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             if (r == 0 && sb + 1 < nsb) {
                 const int rn = (sb + 1) % RSTG;
                 ok = mbar_wait(r_empty(rn), (((sb + 1) / RSTG) & 1) ^ 1, abort_flag, kKid, SITE_P_RAW);
-                if (ok) {
+                if (ok && !(g_inject == 1 && sb == 0)) {   // (test-only: mode 1 withholds this copy)
                     mbar_arrive_expect_tx(r_full(rn), RAW_BYTES);
                     tma_load_2d(sbase + oRaw + rn * RAW_BYTES, &tmW, r_full(rn), (sb_base + sb + 1) * RAW_ROW, o0);
                     n_raw = sb + 2;
@@ -3265,6 +3265,19 @@ extern "C" int mmq_debug_subdots_q6K(const void *w, const uint16_t *xh, int32_t 
                                      mmq_stream_t stream)
 {
     return mmq::launch<mmq::kQ6K, mmq::kSubdots>(w, xh, nullptr, nullptr, out, T, O, K, stream);
+}
+
+extern "C" int mmq_debug_fault_inject(int mode, int wait_limit_us)
+{
+    if (mode < 0 || mode > 1) return MMQ_ERR_SHAPE;
+    const unsigned long long lim =
+        wait_limit_us > 0 ? (unsigned long long)wait_limit_us * 1000ull : mmq::kWaitLimitNs;
+    if (cudaMemcpyToSymbol(mmq::g_inject, &mode, sizeof(mode)) != cudaSuccess ||
+        cudaMemcpyToSymbol(mmq::g_wait_limit_ns, &lim, sizeof(lim)) != cudaSuccess) {
+        cudaGetLastError();
+        return MMQ_ERR_CUDA;
+    }
+    return MMQ_OK;
 }
 
 // extra detail of the last failure reported by mmq_check_status (host side)

@@ -22,7 +22,7 @@ def test_header_declares_the_boundary():
                      "mmq_gemm_q6K_subblock", "mmq_gemm_q4K_small", "mmq_gemm_q4K_small_imma",
                      "mmq_last_failure_info", "mmq_gemv_q4K", "mmq_gemv_q6K", "mmq_gemm_q4K_swiglu",
                      "mmq_gemm_q5K", "mmq_gemm_q5K_subblock", "mmq_gemm_q8_0", "mmq_debug_subdots_q5K",
-                     "mmq_debug_subdots_q8_0"):
+                     "mmq_debug_subdots_q8_0", "mmq_debug_fault_inject"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -76,6 +76,7 @@ def test_argument_errors_without_gpu():
         assert gemv(p, odd, p, p, 16, 8, 256, null) == -2
         assert gemv(p, p, p, p, 0, 8, 256, null) == 0                         # T == 0 no-op
     assert lib.mmq_last_failure_info(null) == -6
+    assert lib.mmq_debug_fault_inject(2, 1000) == -1                         # unknown mode
     info = (ctypes.c_int * 4)(7, 7, 7, 7)
     assert lib.mmq_last_failure_info(info) == 0 and list(info) == [0, 0, 0, 0]   # nothing reported yet
     assert lib.mmq_gemm_q4K(p, p, p, p, -1, 1, 256, null) == -1              # T < 0
