@@ -16,6 +16,30 @@
  *   - "43 . r40 -- __launch_bounds__(256,3) third resident block", 5:
  *     q6_K, w = d*sc*(q-32) on 16-weight sub-blocks.
  *
+ * Which call for which job
+ * ------------------------
+ *   prefill, T >= ~256 ....... mmq_gemm_q4K / mmq_gemm_q5K / mmq_gemm_q6K
+ *                              (whole-super-block accumulation on the tensor
+ *                              core; Y to the f32 tolerance, the sub-block
+ *                              dots are never formed as numbers)
+ *   FFN gate + up + SwiGLU ... mmq_gemm_q4K_swiglu (writes the down
+ *                              projection's q8_1 operands)
+ *   few output tiles ......... mmq_gemm_q4K_splitk (caller scratch) or
+ *                              mmq_gemm_q4K_splitk_static (no allocation)
+ *   17 <= T <= 64 ............ mmq_gemm_q4K_small
+ *   T <= 16 (decode) ......... mmq_gemv_q4K / mmq_gemv_q6K (per-sub-block
+ *                              integer dots, exact); mmq_gemm_q4K_small_imma
+ *                              takes qs + ds as the pages' q8_1 does, at the
+ *                              int8 warp-MMA rate
+ *   the pages' literal form .. mmq_gemm_q4K_subblock / _q5K_subblock /
+ *                              _q6K_subblock / mmq_gemm_q8_0 (one exact
+ *                              integer dot per sub-block, folded in f32 per
+ *                              sub-block); slower, kept as the reference form
+ *                              on the GPU and for q8_0
+ *   diagnostics .............. mmq_debug_subdots_* (the int32 dots themselves),
+ *                              mmq_probe_tensor_peak, mmq_debug_fault_inject
+ *                              (test-only)
+ *
  * Conventions for every call
  * --------------------------
  *   - All array arguments are DEVICE pointers allocated and owned by the
