@@ -14,73 +14,65 @@ namespace {
 // value v = f32(d16)*q split into two exact f16 planes (v = hi + lo, see the
 // quantiser), the weight operand is sc*q (exact), so each product is exact in
 // f32 and one TMEM accumulator per super-block receives
-//     D_sb[t][o] = sum_{k in sb} v[t][k] * sc_b(o)*q[o][k]
-// through two MMAs per 16-k step (hi plane, lo plane).  The epilogue then
-// needs one packed FMA per output per super-block, Y += d*D_sb (Y held in
-// registers).  The min term rides in the same accumulator: the tensor core
-// also adds sum_j (dx_j*ssum_j) * (-(dmin*m_j)/d) (split-tf32 MMAs over the
-// sub-block index), so that d*D_sb carries both terms of the super-block.
-// For rows with d == 0 the weight operand is zero and the min operand is
-// divided by 1 instead.  The per-sub-block integer dots are not formed here
-// (see mmq_q4K_kernel / the sub-block diagnostics for those); the result
-// differs from them only in f32 rounding.
+//     D_sb[o][t]     = sum_{k in sb} sc_b(o)*q[o][k] * hi[t][k]
+//     D_sb[o][T + t] = sum_{k in sb} sc_b(o)*q[o][k] * lo[t][k]
+// The weight tile is the MMA's A operand (M = 128 weight rows = TMEM lanes)
+// and the two activation planes of the 128 tokens, stacked, its B operand
+// (N = 256), so one 128x256x16 MMA per 16-k step covers both planes and the
+// weight tile is read from shared memory once per step.  The epilogue needs
+// one add and one FMA per output per super-block, Y += d*(D_hi + D_lo) (Y
+// held in registers, d a per-thread scalar since a thread owns a weight row).
+// The min term rides in the same accumulator: the tensor core also adds
+// sum_j (-(dmin*m_j)/d) * (dx_j*ssum_j) (split-tf32 MMAs over the sub-block
+// index, into the hi half), so that d*D_sb carries both terms of the
+// super-block.  For rows with d == 0 the weight operand is zero and the min
+// operand is divided by 1 instead.  The per-sub-block integer dots are not
+// formed here (see mmq_q4K_kernel / the sub-block diagnostics for those);
+// the result differs from them only in f32 rounding.
 //
-// Two issuing threads.  On sm_103a issuing a 128x128x16 MMA occupies the
-// issuing thread for most of the 64 cycles the MMA executes, and any
-// dependent shared-memory access of that thread (an mbarrier wait included)
-// waits behind its queued MMAs, so a single issuer that synchronises once
-// per stage leaves the tensor pipe idle for a good part of every stage.  Two
-// threads in warps on different SM sub-partitions therefore issue the 64-k
-// stages alternately (even stages / odd stages), each into accumulators of
-// its own, and the epilogue adds the two: while one synchronises, the other's
-// MMAs keep the pipe busy, and every accumulator still sees its MMAs in one
-// fixed order, so results are reproducible bit for bit.
-// Each stage has a single "full" barrier (TMA bytes of both activation
-// planes + the 128 unpack threads' arrivals) and a single "empty" barrier.
-// The MMA issuers request the activation tiles: when an issuer has seen its
-// previous stage ks - 2 complete, the slot of stage ks + 1 is free, and it
-// issues that stage's TMA before its own stage ks, the earliest moment the
-// slot allows (an unpack warp, busy converting, would reach it later and put
-// the copy's latency on the critical path).  Stage ks uses
-// operand slot ks % STG but barriers ks % (2 STG): a parity wait can only
-// tell apart phases one apart, so every waiter must see each phase of the
-// barriers it waits on.  With one barrier per slot and an odd ring, stages
-// ks and ks + STG belong to different issuers, and an issuer waiting for
-// stage ks + 2 STG while stage ks + STG was still filling would pass at once
-// on the parity of the phase before it.  With 2 STG barriers all stages on
-// one barrier belong to one issuer.  The raw weight
-// super-blocks (128 rows x 144 bytes) arrive by TMA one super-block ahead;
-// the unpack and scale threads copy what they need to registers at the
-// start of a super-block and release the raw slot at once.
-// TMEM: [0,256) even-stage accumulators, [256,512) odd-stage accumulators,
-// two super-blocks each (rotating).
-// Warps: 1 and 14 MMA issuers (even / odd stages; + activation TMA), 2-5
-// unpack (+ raw weight TMA), 6-13 epilogue, 0 and 15 scale.
+// One MMA-issuing thread; every accumulator sees its MMAs in one fixed order,
+// so results are reproducible bit for bit.  Measured on sm_103a: 128x256x16
+// MMAs issued back to back from distinct shared-memory tiles run at the full
+// 128 cycles each and a commit that nobody waits for costs nothing, but an
+// mbarrier wait by the issuing thread (even on a completed phase) returns
+// only after that thread's queued MMAs have completed, so each wait between
+// two stages leaves the tensor core idle for the wait's own latency.  The
+// issuer therefore waits once per stage, on the stage's single "full"
+// barrier (the activation tiles' TMA bytes and the 128 unpack threads'
+// arrivals), and then issues the four MMAs and one commit.  (Splitting that
+// barrier in two, handing the accumulator between two issuers after every
+// stage, or two issuers on halves of the tokens were each measured slower.)
+// Per 64-k stage the activation tiles (hi rows, then lo rows: one B operand
+// of 256 K-major rows) are requested by a producer warp as soon as the slot
+// is free.  The raw weight super-blocks (128 rows x 144 bytes) arrive by TMA
+// one super-block ahead; the unpack and scale threads copy what they need to
+// registers at the start of a super-block and release the raw slot at once.
+// TMEM: two rotating super-block accumulators of 256 columns.
+// Warps: 1 MMA issuer, 14 activation TMA, 2-5 unpack (+ raw weight TMA),
+// 6-13 epilogue, 0 and 15 scale.
 // =========================================================================
 namespace q4s {
 
 constexpr int NWARPS = 16;
 constexpr int NTHREADS = NWARPS * 32;
-constexpr int MMA_WARP_ODD = 14;
+constexpr int MMA_WARP = 1;
+constexpr int ACT_WARP = 14;                      // activation TMA producer
 constexpr int SCALE_WARP_B = 15;                  // scale warps: 0 and 15
-constexpr int STG = 3;                            // operand ring: A hi, A lo, B per 64-k stage
+constexpr int STG = 3;                            // operand ring: act hi, act lo, weights per 64-k stage
 constexpr int RSTG = 2;                           // raw weight super-block ring
 constexpr int SSTG = 2;                           // scale / min-operand ring
-constexpr int NACC = 2;                           // rotating super-block accumulators per issuer
-constexpr uint32_t TM_EVEN = 0, TM_ODD = NACC * BN;
-static_assert(TM_ODD + NACC * BN <= 512, "TMEM budget");
-constexpr uint32_t A_STAGE = 2 * A_BYTES;         // hi and lo planes
-constexpr uint32_t STAGE_BYTES = A_STAGE + B_BYTES;
+constexpr int NACC = 2;                           // rotating super-block accumulators
+constexpr uint32_t ACC_COLS = 2 * BM;             // hi tokens, then lo tokens
+static_assert(NACC * ACC_COLS <= 512, "TMEM budget");
+constexpr uint32_t ACT_STAGE = 2 * A_BYTES;       // hi and lo planes of BM tokens
+constexpr uint32_t STAGE_BYTES = ACT_STAGE + B_BYTES;
 constexpr uint32_t MIN_OP_BYTES = 128 * 64;
 constexpr uint32_t SDS_D = 2 * MIN_OP_BYTES;
 constexpr uint32_t SDS_BYTES = SDS_D + BN * 4;
-constexpr int SBAR = 2 * STG;                     // full / empty barriers: stage ks uses ks % SBAR
 constexpr uint32_t oStage = 0;
 constexpr uint32_t oRaw = oStage + STG * STAGE_BYTES;   // then the raw ring, scale ring and barriers (SbLayout)
-// full, empty [SBAR]; s_full [SSTG]; acc_full, acc_empty [NACC] (shared by the
-// even and odd accumulators of a super-block); r_full, r_empty [RSTG];
-// done [2] (each issuer's stage completions); mma_done
-constexpr int kNumBars = 2 * SBAR + SSTG + 2 * NACC + 2 * RSTG + 2 + 1;
+// full, empty [STG]; s_full [SSTG]; acc_full, acc_empty [NACC]; r_full, r_empty [RSTG]; mma_done
+constexpr int kNumBars = 2 * STG + SSTG + 2 * NACC + 2 * RSTG + 1;
 static_assert(STAGE_BYTES % 1024 == 0 && oRaw % 1024 == 0 && SDS_BYTES % 16 == 0, "ring alignment");
 static_assert(NACC >= SSTG, "a scale slot is rewritten only after its accumulator was released");
 
@@ -150,8 +142,8 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     constexpr int RAW_ROW = SL::RAW_ROW;
     constexpr uint32_t RAW_BYTES = SL::RAW_BYTES, oSds = SL::oSds, oBar = SL::oBar, oMisc = SL::oMisc;
     constexpr int kKid = 9;
-    constexpr uint32_t kIdesc = idesc_f16_f32(BM, BN);
-    constexpr uint32_t kIdescTf32 = idesc_tf32_f32(BM, BN);
+    constexpr uint32_t kIdesc = idesc_f16_f32(BN, ACC_COLS);      // M = weight rows, N = hi + lo tokens
+    constexpr uint32_t kIdescTf32 = idesc_tf32_f32(BN, BM);       // min term: weight rows x tokens
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -167,40 +159,37 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     const int nks = nsb * 4;
 
     const uint32_t bar0 = sbase + oBar;
-    auto full = [&](int b) { return bar0 + 8u * b; };
-    auto empty = [&](int b) { return bar0 + 8u * (SBAR + b); };
-    auto s_full = [&](int s) { return bar0 + 8u * (2 * SBAR + s); };
-    auto acc_full = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + s); };
-    auto acc_empty = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + NACC + s); };
-    auto r_full = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + 2 * NACC + s); };
-    auto r_empty = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + 2 * NACC + RSTG + s); };
-    auto done = [&](int s) { return bar0 + 8u * (2 * SBAR + SSTG + 2 * NACC + 2 * RSTG + s); };
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STG + s); };
+    auto s_full = [&](int s) { return bar0 + 8u * (2 * STG + s); };
+    auto acc_full = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + s); };
+    auto acc_empty = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + NACC + s); };
+    auto r_full = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + s); };
+    auto r_empty = [&](int s) { return bar0 + 8u * (2 * STG + SSTG + 2 * NACC + RSTG + s); };
     const uint32_t mma_done = bar0 + 8u * (kNumBars - 1);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + oMisc);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + oMisc + 4);
     auto stage_a = [&](int s) { return sbase + oStage + (uint32_t)s * STAGE_BYTES; };
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < SBAR; ++b) {
-            mbar_init(full(b), 1 + 128);                    // TMA issue (with its bytes) + unpack threads
-            mbar_init(empty(b), 1);                         // the commit of the stage's issuer
+        for (int s = 0; s < STG; ++s) {
+            mbar_init(full(s), 1 + 128);                    // the TMA request (with its bytes) + unpack threads
+            mbar_init(empty(s), 1);                         // the issuer's commit
         }
         for (int s = 0; s < SSTG; ++s) mbar_init(s_full(s), 64);   // scale threads
         for (int s = 0; s < NACC; ++s) {
-            mbar_init(acc_full(s), 2);                      // both issuers' commits
+            mbar_init(acc_full(s), 1);                      // the issuer's commit
             mbar_init(acc_empty(s), NUM_EPI_WARPS);         // after the epilogue has also read d
         }
         for (int s = 0; s < RSTG; ++s) {
             mbar_init(r_full(s), 1);
             mbar_init(r_empty(s), 128 + 64);                // unpack and scale threads
         }
-        mbar_init(done(0), 1);
-        mbar_init(done(1), 1);
-        mbar_init(mma_done, 2);
+        mbar_init(mma_done, 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == MMA_WARP) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -209,71 +198,65 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 1 || warp == MMA_WARP_ODD) {
-        // ----------------------------------------------------- MMA issuers --
+    if (warp == MMA_WARP) {
+        // ------------------------------------------------------ MMA issuer --
         if (lane == 0) {
-            const int me = warp == 1 ? 0 : 1;   // stages with ks % 2 == me
             bool ok = true;
-            // activation tiles of stage k: [2T][K] tensor, hi plane rows 0..T-1, lo plane rows T..2T-1
-            auto load_a = [&](int k) {
-                mbar_arrive_expect_tx(full(k % SBAR), A_STAGE);
-                tma_load_2d(stage_a(k % STG), &tmA, full(k % SBAR), (sb_base * 4 + k) * BK, t0);
-                tma_load_2d(stage_a(k % STG) + A_BYTES, &tmA, full(k % SBAR), (sb_base * 4 + k) * BK, T + t0);
-            };
-            int last_a = -1;   // last stage whose activation tiles this thread requested
-            if (me == 0) {
-                tma_prefetch(&tmA);
-                for (int k = 0; k < STG && k < nks; ++k) load_a(k);
-                last_a = min(STG, nks) - 1;
-            }
-            for (int ks = me; ks < nks && ok; ks += 2) {
-                const int s = ks % STG, fb = ks % SBAR;
+            for (int ks = 0; ks < nks && ok; ++ks) {
+                const int s = ks % STG;
                 const int sb = ks >> 2, p4 = ks & 3, slot = sb % NACC;
-                // Throttle: this issuer's previous stage has completed.  At most two stages
-                // are then queued in the tensor pipe (the other issuer's, executing, and this
-                // one), and the rest of the ring is free for loading.
-                const int n_mine = ks >> 1;   // stages this issuer has issued so far
-                ok = n_mine == 0 || mbar_wait(done(me), (n_mine - 1) & 1, abort_flag, kKid, SITE_M_A);
-                if (!ok) break;
-                // stage ks - 2 has completed, so the slot of stage ks + 1 is free
-                if (ks >= 2 && ks + 1 < nks) {
-                    load_a(ks + 1);
-                    last_a = ks + 1;
-                }
-                ok = mbar_wait(full(fb), (ks / SBAR) & 1, abort_flag, kKid, SITE_M_A) &&
-                     (p4 > 1 || mbar_wait(acc_empty(slot), ((sb / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC));
+                ok = (p4 != 0 || mbar_wait(acc_empty(slot), ((sb / NACC) & 1) ^ 1, abort_flag, kKid, SITE_M_ACC)) &&
+                     mbar_wait(full(s), (ks / STG) & 1, abort_flag, kKid, SITE_M_A);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a_hi = stage_a(s);
-                const uint64_t dh = sdesc_k_sw128(a_hi), dl = sdesc_k_sw128(a_hi + A_BYTES),
-                               db = sdesc_k_sw128(a_hi + A_STAGE);
-                const uint32_t d_acc = tmem_base + (me ? TM_ODD : TM_EVEN) + slot * BN;
+                const uint32_t st = stage_a(s);
+                const uint64_t dw = sdesc_k_sw128(st + ACT_STAGE);   // weight tile: A, 128 rows
+                const uint64_t dx = sdesc_k_sw128(st);               // hi rows then lo rows: B, 256 rows
+                const uint32_t d_acc = tmem_base + slot * ACC_COLS;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
+                for (int kk = 0; kk < 4; ++kk)
                     // +32 bytes along K within the 128-byte swizzled rows = +2 in the address field
-                    umma_f16(d_acc, dh + 2 * kk, db + 2 * kk, kIdesc, (p4 <= 1 && kk == 0) ? 0u : 1u);
-                    umma_f16(d_acc, dl + 2 * kk, db + 2 * kk, kIdesc, 1u);
-                }
+                    umma_f16(d_acc, dw + 2 * kk, dx + 2 * kk, kIdesc, (p4 == 0 && kk == 0) ? 0u : 1u);
                 if (p4 == 3) {
-                    // min term of this super-block, into the odd accumulator
+                    // min term of this super-block, into the hi half
                     const int ss = sb % SSTG;
                     ok = mbar_wait(s_full(ss), (sb / SSTG) & 1, abort_flag, kKid, SITE_E_SDS);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t am = sbase + oSds + ss * SDS_BYTES, bm = am + MIN_OP_BYTES;
-                    umma_tf32(d_acc, sdesc_k_none(am, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
-                    umma_tf32(d_acc, sdesc_k_none(am, 128, 512), sdesc_k_none(bm + 256, 128, 512), kIdescTf32, 1u);
-                    umma_tf32(d_acc, sdesc_k_none(am + 256, 128, 512), sdesc_k_none(bm, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(d_acc, sdesc_k_none(bm, 128, 512), sdesc_k_none(am, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(d_acc, sdesc_k_none(bm, 128, 512), sdesc_k_none(am + 256, 128, 512), kIdescTf32, 1u);
+                    umma_tf32(d_acc, sdesc_k_none(bm + 256, 128, 512), sdesc_k_none(am, 128, 512), kIdescTf32, 1u);
+                    umma_commit(acc_full(slot));
                 }
-                if (p4 >= 2) umma_commit(acc_full(slot));   // this issuer's last stage of the super-block
-                umma_commit(empty(fb));
-                umma_commit(done(me));
+                umma_commit(empty(s));
             }
             umma_commit(mma_done);
             if (!wait_drain(mma_done, 0)) record_error(kStatusTimeout, kKid, SITE_DRAIN);
-            if (!ok)   // let this thread's activation copies in flight land before the CTA exits
-                for (int i = max(0, last_a - 2 * STG + 1); i <= last_a; ++i)
-                    if (i < STG ? me == 0 : ((i - 1) & 1) == me) wait_drain(full(i % SBAR), (i / SBAR) & 1);
+        }
+        __syncwarp();
+    } else if (warp == ACT_WARP) {
+        // ------------------------------------------- activation TMA producer --
+        // activation tiles of stage k: [2T][K] tensor, hi plane rows 0..T-1, lo plane rows T..2T-1
+        if (lane == 0) {
+            tma_prefetch(&tmA);
+            bool ok = true;
+            int n_a = 0;   // stages requested, for the drain on abort
+            for (int ks = 0; ks < nks && ok; ++ks) {
+                const int s = ks % STG;
+                // slot s is free once stage ks - STG's MMAs have completed
+                ok = ks < STG || mbar_wait(empty(s), ((ks / STG) - 1) & 1, abort_flag, kKid, SITE_P_STAGE);
+                if (!ok) break;
+                mbar_arrive_expect_tx(full(s), ACT_STAGE);
+                tma_load_2d(stage_a(s), &tmA, full(s), (sb_base * 4 + ks) * BK, t0);
+                tma_load_2d(stage_a(s) + A_BYTES, &tmA, full(s), (sb_base * 4 + ks) * BK, T + t0);
+                n_a = ks + 1;
+            }
+            // On abort: let the copies in flight land before the CTA exits.  A
+            // stage's barrier also counts the unpack threads' arrivals, so
+            // where those stopped first this wait ends at its time limit.
+            if (!ok)
+                for (int i = max(0, n_a - STG); i < n_a; ++i) wait_drain(full(i % STG), (i / STG) & 1);
         }
         __syncwarp();
     } else if (warp >= UNPACK_WARP0 && warp < EPI_WARP0) {
@@ -281,8 +264,8 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         // Thread = one weight row (rows past O arrive zero-filled).  At the
         // start of a super-block it copies the row's 144 raw bytes to
         // registers; per 64-k stage it writes the row's 64 values sc*q as f16
-        // into the swizzled B tile (zeros when the row's d is zero).  Thread 0
-        // also issues the raw tile one super-block ahead.
+        // into the swizzled weight tile (zeros when the row's d is zero).
+        // Thread 0 also issues the raw tile one super-block ahead.
         const int r = threadIdx.x - UNPACK_WARP0 * 32;
         bool ok = true;
         int n_raw = 0;     // raw super-blocks requested (thread 0), for the drain on abort
@@ -360,33 +343,31 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
             convert(0, va);
 #pragma unroll
             for (int p4 = 0; p4 < 4; ++p4) {
-                const int ks = sb * 4 + p4, s = ks % STG, fb = ks % SBAR;
+                const int ks = sb * 4 + p4, s = ks % STG;
                 uint4 (&vc)[8] = (p4 & 1) ? vb : va;
                 uint4 (&vn)[8] = (p4 & 1) ? va : vb;
                 // slot s is free once stage ks - STG's MMAs have completed
-                ok = ks < STG ||
-                     mbar_wait(empty((ks - STG) % SBAR), ((ks - STG) / SBAR) & 1, abort_flag, kKid, SITE_U_STAGE);
+                ok = ks < STG || mbar_wait(empty(s), ((ks / STG) - 1) & 1, abort_flag, kKid, SITE_U_STAGE);
                 if (!ok) break;
-                uint8_t *brow = smem + oStage + s * STAGE_BYTES + A_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
+                uint8_t *brow = smem + oStage + s * STAGE_BYTES + ACT_STAGE + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(brow + ((c ^ (r & 7)) << 4)) = vc[c];
                 if (p4 < 3) convert(p4 + 1, vn);
                 fence_proxy_async_smem();
-                mbar_arrive(full(fb));
+                mbar_arrive(full(s));
             }
         }
-        if (!ok && r == 0)
+        if (!ok && r == 0)   // let the copies in flight land before the CTA exits
             for (int i = max(0, n_raw - RSTG); i < n_raw; ++i) wait_drain(r_full(i % RSTG), (i / RSTG) & 1);
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
         // --------------------------------------------------------- epilogue --
-        // Thread = one token (TMEM lane) x 64 weight rows; Y += d*(D_even +
-        // D_odd) per super-block in registers.
+        // Thread = one weight row (TMEM lane) x 64 tokens; Y += d*(D_hi + D_lo)
+        // per super-block in registers.
         const int ew = warp - EPI_WARP0;
-        const int quarter = warp & 3;
-        const int c0 = (ew >> 2) * 64;
-        const int tl = quarter * 32 + lane;
-        const int t = t0 + tl;
-        const bool tok_ok = t < T;
+        const int quarter = warp & 3;         // TMEM lanes 32*quarter.. are this warp's
+        const int c0 = (ew >> 2) * 64;        // first token of this thread within the tile
+        const int row = quarter * 32 + lane;  // weight row within the tile
+        const int o = o0 + row;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         float yv[64];
 #pragma unroll
@@ -398,31 +379,26 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                  mbar_wait_warp(acc_full(slot), (sb / NACC) & 1, abort_flag, kKid, SITE_E_ACC);
             if (!ok) break;
             tc_fence_after();
-            const float *dv = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + SDS_D) + c0;
-            const uint32_t col = tmem_base + lane_off + slot * BN + c0;
+            const float d = reinterpret_cast<const float *>(smem + oSds + ss * SDS_BYTES + SDS_D)[row];
+            const float2 d2 = make_float2(d, d);
+            const uint32_t col = tmem_base + lane_off + slot * ACC_COLS + c0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t ra[16], rb[16];
-                tmem_ld16(col + TM_EVEN + q * 16, ra);
-                tmem_ld16(col + TM_ODD + q * 16, rb);
+                tmem_ld16(col + q * 16, ra);        // hi-plane products of tokens c0 + 16q ..
+                tmem_ld16(col + BM + q * 16, rb);   // lo-plane products of the same tokens
                 tmem_ld_wait2(ra, rb);
 #pragma unroll
-                for (int i = 0; i < 16; i += 4) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(dv + q * 16 + i);
-                    const float2 s0 = __fadd2_rn(make_float2(__uint_as_float(ra[i]), __uint_as_float(ra[i + 1])),
-                                                 make_float2(__uint_as_float(rb[i]), __uint_as_float(rb[i + 1])));
-                    const float2 s1 = __fadd2_rn(make_float2(__uint_as_float(ra[i + 2]), __uint_as_float(ra[i + 3])),
-                                                 make_float2(__uint_as_float(rb[i + 2]), __uint_as_float(rb[i + 3])));
+                for (int i = 0; i < 16; i += 2) {
+                    const float2 s = __fadd2_rn(make_float2(__uint_as_float(ra[i]), __uint_as_float(ra[i + 1])),
+                                                make_float2(__uint_as_float(rb[i]), __uint_as_float(rb[i + 1])));
                     const int e = q * 16 + i;
-                    const float2 y0 = __ffma2_rn(s0, make_float2(d4.x, d4.y), make_float2(yv[e], yv[e + 1]));
-                    const float2 y1 = __ffma2_rn(s1, make_float2(d4.z, d4.w), make_float2(yv[e + 2], yv[e + 3]));
-                    yv[e] = y0.x;
-                    yv[e + 1] = y0.y;
-                    yv[e + 2] = y1.x;
-                    yv[e + 3] = y1.y;
+                    const float2 y = __ffma2_rn(s, d2, make_float2(yv[e], yv[e + 1]));
+                    yv[e] = y.x;
+                    yv[e + 1] = y.y;
                 }
             }
-            // both accumulators and this super-block's d have been read
+            // the accumulator and this super-block's d have been read
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(slot));
@@ -430,33 +406,29 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         if constexpr (SWIGLU) {
             // Park the tile in shared memory for the CTA-wide SwiGLU pass at the
             // end (the operand ring is idle now that every MMA has completed):
-            // columns 0..63 are the gate rows of features 64*bx .., columns
-            // 64..127 the up rows of the same features.
-            float *gu = reinterpret_cast<float *>(smem + oStage) + (c0 ? BM * q4s::GU_STRIDE : 0) + tl * q4s::GU_STRIDE;
+            // rows 0..63 are the gate rows of features 64*bx .., rows 64..127 the
+            // up rows of the same features; stored [token][feature].
+            float *gu = reinterpret_cast<float *>(smem + oStage) + (row >= 64 ? BM * q4s::GU_STRIDE : 0) + (row & 63) +
+                        c0 * q4s::GU_STRIDE;
 #pragma unroll
-            for (int i = 0; i < 64; i += 4)
-                *reinterpret_cast<float4 *>(gu + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+            for (int i = 0; i < 64; ++i) gu[i * q4s::GU_STRIDE] = yv[i];
         }
-        const bool vec = (O & 3) == 0 && o0 + c0 + 64 <= O;
-        auto store_row = [&](float *row) {
-            if (vec) {
+        // this thread's outputs: column o of rows t0 + c0 .. t0 + c0 + 63 of a [T][O] array
+        const int nt = min(64, T - t0 - c0);
+        const bool col_ok = o < O;
+        auto store_col = [&](float *base) {
 #pragma unroll
-                for (int i = 0; i < 64; i += 4)
-                    *reinterpret_cast<float4 *>(row + i) = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    if (o0 + c0 + i < O) row[i] = yv[i];
-            }
+            for (int i = 0; i < 64; ++i)
+                if (i < nt) base[(size_t)i * O] = yv[i];
         };
         if (SWIGLU) {
             // written above
         } else if (p.part == nullptr || gridDim.z == 1) {
-            if (ok && tok_ok) store_row(p.y + (size_t)t * O + o0 + c0);
+            if (ok && col_ok) store_col(p.y + (size_t)(t0 + c0) * O + o);
         } else {
             // split-K: publish this split's partial sums; the last CTA of the
             // tile to arrive adds all splits in z order (deterministic)
-            if (ok && tok_ok) store_row(p.part + ((size_t)blockIdx.z * T + t) * O + o0 + c0);
+            if (ok && col_ok) store_col(p.part + ((size_t)blockIdx.z * T + t0 + c0) * O + o);
             __threadfence();
             named_bar_sync(1, NUM_EPI_WARPS * 32);
             uint32_t *last_flag = reinterpret_cast<uint32_t *>(smem + oMisc + 8);
@@ -468,37 +440,31 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 *last_flag = last ? 1u : 0u;
             }
             named_bar_sync(1, NUM_EPI_WARPS * 32);
-            if (*last_flag && ok && tok_ok) {
+            if (*last_flag && ok && col_ok) {
                 __threadfence();
+                // eight outputs at a time, the other splits' eight loads issued together
 #pragma unroll
-                for (int i = 0; i < 64; i += 4) {
-                    float4 a4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int c = 0; c < 64; c += 8) {
+                    float a[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) a[i] = 0.0f;
                     for (int z = 0; z < (int)gridDim.z; ++z) {
-                        float4 v;
+                        float v[8];
                         if (z == (int)blockIdx.z) {
-                            v = make_float4(yv[i], yv[i + 1], yv[i + 2], yv[i + 3]);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[i] = yv[c + i];
                         } else {
-                            const float *prow = p.part + ((size_t)z * T + t) * O + o0 + c0 + i;
-                            if (vec) {
-                                v = __ldcg(reinterpret_cast<const float4 *>(prow));
-                            } else {
-                                v.x = o0 + c0 + i < O ? __ldcg(prow) : 0.0f;
-                                v.y = o0 + c0 + i + 1 < O ? __ldcg(prow + 1) : 0.0f;
-                                v.z = o0 + c0 + i + 2 < O ? __ldcg(prow + 2) : 0.0f;
-                                v.w = o0 + c0 + i + 3 < O ? __ldcg(prow + 3) : 0.0f;
-                            }
+                            const float *pz = p.part + ((size_t)z * T + t0 + c0 + c) * O + o;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v[i] = c + i < nt ? __ldcg(pz + (size_t)i * O) : 0.0f;
                         }
-                        a4.x += v.x;
-                        a4.y += v.y;
-                        a4.z += v.z;
-                        a4.w += v.w;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) a[i] += v[i];
                     }
-                    yv[i] = a4.x;
-                    yv[i + 1] = a4.y;
-                    yv[i + 2] = a4.z;
-                    yv[i + 3] = a4.w;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) yv[c + i] = a[i];
                 }
-                store_row(p.y + (size_t)t * O + o0 + c0);
+                store_col(p.y + (size_t)(t0 + c0) * O + o);
             }
         }
     } else if (warp == 0 || warp == SCALE_WARP_B) {
@@ -507,9 +473,9 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         // where d == 0) and the min-term operand row (-(dmin*m_j)/d, split
         // hi/lo); for tokens r and r + 64: the min-term operand row
         // (dx_j*ssum_j split hi/lo).  Slot sb % SSTG is rewritten once
-        // super-block sb - SSTG's accumulators have been released: its
-        // min-term MMAs completed before they were handed to the epilogue,
-        // and the epilogue releases them after reading d.  The weight headers
+        // super-block sb - SSTG's accumulator has been released: its
+        // min-term MMAs completed before it was handed to the epilogue,
+        // and the epilogue releases it after reading d.  The weight headers
         // come from the raw tile, the q8_1 scale words are fetched one
         // super-block ahead.
         const int sr = (warp == 0 ? 0 : 32) + lane;   // 0..63
@@ -655,7 +621,7 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
                 *reinterpret_cast<uint4 *>(p.h_qs + (size_t)t * F + f0) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
         }
     }
-    if (warp == 1) {
+    if (warp == MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);
     }
