@@ -283,8 +283,10 @@ def sweep_lines(dev, hbm_gbs, mac_peak, fast=False):
     1024 and 4096, device time per launch with the weights streamed from HBM
     (the timed launches cycle through copies of W larger than L2 together).
     Every kernel that takes the shape is timed: the weight-stationary small-T
-    GEMM and the int8 warp-MMA form (T <= 64 / 16), the decode-shaped product
-    (T <= 16), split-K (T <= 256) and the one-CTA-per-tile production GEMM.
+    GEMM and the int8 warp-MMA form (T <= 64 / 16), the decode-shaped products
+    (T <= 16, and T <= 4 with the quantisation built in: that line's time
+    includes quantising the f32 tokens, the others' do not), split-K
+    (T <= 256) and the one-CTA-per-tile production GEMM.
     Each line reports TMAC/s, the fraction of the f16 dense MAC peak and of
     this route's own ceiling, and algorithmic GB/s (weights + q8_1 activations
     at 1.125 B/element + f32 output) as a fraction of the HBM copy rate."""
@@ -308,6 +310,9 @@ def sweep_lines(dev, hbm_gbs, mac_peak, fast=False):
                                                     for w in copies], n=n)
             if g.T <= ops.GEMV_T_MAX:
                 kern["gemv"] = graph_time_us([lambda w=w: ops.gemv(w, xh, ds, g.O, out=y) for w in copies], n=n)
+            if g.T <= ops.DECODE_T_MAX:
+                # f32 tokens in, the q8_1 quantisation inside the launch
+                kern["gemv_f32"] = graph_time_us([lambda w=w: ops.gemv_f32(w, x, g.O, out=y) for w in copies], n=n)
             ks = None
             if g.T <= 256:
                 ks = ops.choose_ksplit(g.T, g.O, g.K)
@@ -382,11 +387,14 @@ def format_lines(dev, mac_peak, T=512, K=4096, O=4096):
 
 
 def decode_line(dev, layers, groups, xs, hbm_gbs):
-    """Side measurement: one decode step (T = 1) of the whole layer stack through
-    the decode-shaped kernels: per layer the q8_1 quantisation of the four
-    one-token inputs and the seven projections (gate and up as one launch over
-    their concatenated rows), every layer's weights streamed from HBM; one
-    CUDA graph per three steps, device time per step (best of 5)."""
+    """Side measurement: one decode step (T = 1) of the whole layer stack, every
+    layer's weights streamed from HBM; one CUDA graph per three steps, device
+    time per step (best of 5).  Per layer the seven projections (gate and up as
+    one launch over their concatenated rows) run as mmq_gemv_q4K_f32 /
+    mmq_gemv_q6K_f32 on the f32 token, the q8_1 quantisation inside each
+    launch.  The same step with every input quantised by its own launch and
+    the products on mmq_gemv_q4K / mmq_gemv_q6K is timed beside it
+    (`unfused`)."""
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     kk = {s: x.shape[1] for s, x in xs.items()}
@@ -397,6 +405,11 @@ def decode_line(dev, layers, groups, xs, hbm_gbs):
 
     def step():
         for lw in layers:
+            for g in groups:
+                ops.gemv_f32(lw[g.name], x1[g.x_seed], g.O, out=yb[g.name], fmt=g.fmt)
+
+    def step_unfused():
+        for lw in layers:
             for s, x in x1.items():
                 ops.quantize_q8_1(x, out=qb[s])
             for g in groups:
@@ -404,12 +417,17 @@ def decode_line(dev, layers, groups, xs, hbm_gbs):
                 ops.gemv(lw[g.name], xh, ds, g.O, out=yb[g.name], fmt=g.fmt)
 
     us = graph_time_us(step, n=3)
+    us_unfused = graph_time_us(step_unfused, n=3)
     ops.check_status(dev)
     wbytes = sum(t.numel() for lw in layers for t in lw.values())
-    return {"kernels": "mmq_quantize_q8_1 + mmq_gemv_q4K / mmq_gemv_q6K", "tokens": 1, "layers": len(layers),
+    return {"kernels": "mmq_gemv_q4K_f32 / mmq_gemv_q6K_f32 (q8_1 quantisation inside the launch)",
+            "tokens": 1, "layers": len(layers),
             "us_per_step": us, "tok_s": 1e6 / us, "weight_bytes_per_step": wbytes,
             "hbm_gbs": wbytes / (us * 1e-6) / 1e9, "hbm_frac": wbytes / (us * 1e-6) / 1e9 / hbm_gbs,
-            "launches_per_step": len(layers) * (len(x1) + len(groups)),
+            "launches_per_step": len(layers) * len(groups),
+            "unfused": {"kernels": "mmq_quantize_q8_1 + mmq_gemv_q4K / mmq_gemv_q6K", "us_per_step": us_unfused,
+                        "launches_per_step": len(layers) * (len(x1) + len(groups)),
+                        "hbm_frac": wbytes / (us_unfused * 1e-6) / 1e9 / hbm_gbs},
             "timing": "CUDA-graph replay of 3 steps, device events, best of 5; weights from HBM (the stack "
                       "exceeds L2)"}
 
@@ -584,7 +602,8 @@ def small_t_launches(T):
 
 def decode_launches(args):
     """One eager decode step (T = 1) of args.layers layers through the decode-shaped
-    kernels, as timed by the bench's decode line (after one warm-up step)."""
+    kernels with the q8_1 quantisation inside each launch, as timed by the
+    bench's decode line (after one warm-up step)."""
     import numpy as np
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
@@ -596,16 +615,11 @@ def decode_launches(args):
                for gr in groups}
     layers = [w_layer] + [{n: t.clone() for n, t in w_layer.items()} for _ in range(args.layers - 1)]
     x1 = {s: torch.from_numpy(synth.make_x(1, x.shape[1], 900 + s)).to(dev) for s, x in xs.items()}
-    qb = {s: (None, torch.empty((1, x.shape[1] // 32), dtype=torch.int32, device=dev),
-              torch.empty((1, x.shape[1]), dtype=torch.float16, device=dev), None) for s, x in xs.items()}
     yb = {g.name: torch.empty((1, g.O), dtype=torch.float32, device=dev) for g in groups}
     for _ in range(2):
         for lw in layers:
-            for s, x in x1.items():
-                ops.quantize_q8_1(x, out=qb[s])
             for g in groups:
-                _, ds, xh, _ = qb[g.x_seed]
-                ops.gemv(lw[g.name], xh, ds, g.O, out=yb[g.name], fmt=g.fmt)
+                ops.gemv_f32(lw[g.name], x1[g.x_seed], g.O, out=yb[g.name], fmt=g.fmt)
     torch.cuda.synchronize()
     ops.check_status(dev)
     print(json.dumps({"decode_launches": args.layers, "status": "ok"}))

@@ -27,6 +27,9 @@
  *   few output tiles ......... mmq_gemm_q4K_splitk (caller scratch) or
  *                              mmq_gemm_q4K_splitk_static (no allocation)
  *   17 <= T <= 64 ............ mmq_gemm_q4K_small
+ *   T <= 4 (decode), f32 in .. mmq_gemv_q4K_f32 / mmq_gemv_q6K_f32 (q8_1
+ *                              quantisation built in; per-sub-block integer
+ *                              dots on the SIMT cores)
  *   T <= 16 (decode) ......... mmq_gemv_q4K / mmq_gemv_q6K (per-sub-block
  *                              integer dots, exact); mmq_gemm_q4K_small_imma
  *                              takes qs + ds as the pages' q8_1 does, at the
@@ -244,6 +247,39 @@ int mmq_gemm_q4K_small_imma(const void *w, const int8_t *qs, const uint32_t *ds,
  */
 int mmq_gemv_q4K(const void *w, const uint16_t *xh, const uint32_t *ds, float *y,
                  int T, int O, int K, mmq_stream_t stream);
+
+/*
+ * Decode-shaped q4_K product for 1 <= T <= 4 tokens with the q8_1
+ * quantisation of the f32 tokens built in: y = mmq_gemm_q4K applied to
+ * mmq_quantize_q8_1(x), without the separate quantise launch.  Every CTA
+ * quantises the tokens into shared memory with the same arithmetic as
+ * mmq_quantize_q8_1 (bit-identical codes, scales and sums), then forms the
+ * pages' per-sub-block exact integer dots ("31 . r28", 2.3) with __dp4a on
+ * the SIMT cores and folds them in f32 as (dx*(d*sc))*C_b + (dx*ssum)*
+ * (-(dmin*m)); one warp per weight row, the rows dealt over the CTAs so that
+ * every SM streams the same share of W.  Result as mmq_gemm_q4K up to f32
+ * summation order; the same on every call.  Allocates nothing.
+ * x: f32 [T][ldx] (ldx >= K, ldx % 4 == 0), finite.  w: as mmq_gemm_q4K.
+ * y: f32 [T][O], overwritten.  T <= 4, 256 <= K <= 32768, K % 256 == 0
+ * (MMQ_ERR_SHAPE otherwise), O >= 1.
+ * Launched with programmatic stream serialisation like mmq_gemv_q4K: W must
+ * not be written by the kernel launched immediately before on the same
+ * stream; x and y are touched only after that kernel has completed.
+ */
+int mmq_gemv_q4K_f32(const void *w, const float *x, int64_t ldx, float *y, int T, int O, int K,
+                     mmq_stream_t stream);
+
+/*
+ * The same for q6_K ("43 . r40", 5: w = d*sc_u*(q-32) on 16-weight
+ * sub-blocks; the pages' per-16 fold y += (dx*(d*sc_u))*C16_u with C16_u the
+ * exact integer dot of (q - 32) with the int8 activations, __dp4a).  The
+ * 210-byte blocks are only 2-byte aligned: every chunk is copied as the
+ * 16-byte-aligned window around it, and the bytes of a window past the end
+ * of W are read one by one, never beyond it.  w: O*(K/256)*210 bytes; other
+ * arguments, limits and launch behaviour as mmq_gemv_q4K_f32.
+ */
+int mmq_gemv_q6K_f32(const void *w, const float *x, int64_t ldx, float *y, int T, int O, int K,
+                     mmq_stream_t stream);
 
 /*
  * Decode-shaped q6_K product for 1 <= T <= 16 tokens ("43 . r40", 5:

@@ -30,6 +30,8 @@ SIGNATURES = {
     "mmq_gemm_q4K_small": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemv_q4K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "mmq_gemv_q6K": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "mmq_gemv_q4K_f32": (_I, [_P, _P, _I64, _P, _I, _I, _I, _P]),
+    "mmq_gemv_q6K_f32": (_I, [_P, _P, _I64, _P, _I, _I, _I, _P]),
     "mmq_gemm_q4K_splitk": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "mmq_gemm_q4K_splitk_static": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "mmq_gemm_q4K_swiglu": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),

@@ -26,6 +26,9 @@
 #include "mmq_host.h"
 
 #include "mmq_common.cuh"
+#include "mmq_kquant.cuh"
+#include "mmq_q8_1.cuh"
+#include "mmq_pdl.cuh"
 #include "mmq_subblock.cuh"
 #include "mmq_prod_q4K.cuh"
 #include "mmq_prod_q6K.cuh"
@@ -234,3 +237,4 @@ extern "C" int mmq_last_failure_info(int *info)
 // and the status word
 #include "mmq_gemv.cuh"
 #include "mmq_gemv_q6.cuh"
+#include "mmq_decode.cuh"

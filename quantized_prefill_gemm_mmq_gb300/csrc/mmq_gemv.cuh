@@ -120,13 +120,7 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&lo)[2], uint3
     hi[1] = (t8 & 0x00F000F0u) | 0x64006400u;
 }
 
-// Programmatic dependent launch: let the next kernel in the stream start its
-// launch now (its CTAs still wait for this grid to complete before reading
-// what it writes), and wait for the previous kernel in the stream to complete
-// with its writes visible.  Both are no-ops for a launch without the
-// programmatic-serialisation attribute.
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// pdl_launch_dependents / pdl_wait: mmq_pdl.cuh
 
 // D = A (16 x 16, f16, row) * B (16 x 8, f16, col) + D, f32
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,

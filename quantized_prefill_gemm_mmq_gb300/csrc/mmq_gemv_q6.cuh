@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
         }
         fence_mbar_init();
     }
-    gv::pdl_launch_dependents();
+    pdl_launch_dependents();
     __syncthreads();
 
     int issued = 0;   // producer: stages issued
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
         // scale words after
         const int first = nst < C::S ? nst : C::S;
         for (int j = 0; j < first; ++j) stage_w(j, sbase + j * C::STAGE, full0 + 8 * j, sm + j * C::STAGE);
-        gv::pdl_wait();
+        pdl_wait();
         if (lane == 0)
             for (int j = 0; j < first; ++j) stage_x(j, sbase + j * C::STAGE, full0 + 8 * j);
         issued = first;
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(gv6::Cfg<NT>::NTHREADS, 2)
         __syncthreads();
         return;
     }
-    gv::pdl_wait();   // y is written only once the previous kernel in the stream has completed
+    pdl_wait();   // y is written only once the previous kernel in the stream has completed
     for (int i = tid; i < C::TOK * ROWS; i += NTHREADS) {
         const int t = i / ROWS, r = i % ROWS;
         if (t < T && o0 + r < O) {

@@ -105,7 +105,7 @@ int make_tmap_4d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, 
 
 }  // namespace mmq
 
-extern "C" int mmq_version(void) { return 7; }
+extern "C" int mmq_version(void) { return 8; }
 
 extern "C" const char *mmq_status_str(int status)
 {

@@ -112,20 +112,6 @@ __device__ __forceinline__ float swiglu_f32(float g, float u)
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
-// round_half_away(x / d) with the quotient rounded to f32 as IEEE division
-// does, without the division where the result cannot depend on it: with
-// r = fl(1/d), z = fl(x * r) is within |y| * 2^-22 of the correctly rounded
-// quotient fl(y) (y = x / d), which for |y| <= 127.5 is below 2^-14; unless z
-// lies within 2^-14 of a half-integer (or r is not a finite normal number)
-// both round to the same integer, and otherwise the IEEE quotient is taken.
-__device__ __forceinline__ int q8_round_quotient(float x, float d, float r)
-{
-    const float z = x * r;
-    const float a = fabsf(z);
-    if (r < 1e30f && a < 128.0f && fabsf(a - floorf(a) - 0.5f) > 0x1p-14f) return (int)roundf(z);
-    return (int)roundf(__fdiv_rn(x, d));
-}
-
 }  // namespace q4s
 
 // SWIGLU: the tile's output is not stored as y but finished as silu(gate)*up and
@@ -587,8 +573,8 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         for (int c = 0; c < 16; c += 2) {
             int qa = 0, qb = 0;
             if (amax != 0.0f) {
-                qa = min(127, max(-127, q4s::q8_round_quotient(h[c], d32, rd)));
-                qb = min(127, max(-127, q4s::q8_round_quotient(h[c + 1], d32, rd)));
+                qa = min(127, max(-127, q8::round_quotient(h[c], d32, rd)));
+                qb = min(127, max(-127, q8::round_quotient(h[c + 1], d32, rd)));
             }
             ssum += qa + qb;
             const uint32_t pair = (uint32_t)(uint8_t)qa | ((uint32_t)(uint8_t)qb << 8);

@@ -6,8 +6,9 @@
 //   amax = max|x|, d32 = amax/127, q = clamp(round_half_away(x/d32), +-127),
 //   ssum = sum q, stored d = f16_rne(d32); all-zero block -> 0, 0, 0.
 // d32 is an IEEE round-to-nearest division (__fdiv_rn), and every quotient
-// x/d32 is rounded exactly as its IEEE division would be (round_quotient), so
-// the result does not depend on fast-math flags.
+// x/d32 is rounded exactly as its IEEE division would be (q8::round_quotient
+// in mmq_q8_1.cuh, shared with every other q8_1 writer), so the result does
+// not depend on fast-math flags.
 //
 // Optional outputs: qs (int8 values), xh (the same values as f16, the integer
 // operand form) and xa (the dequantised activation f32(d16)*q as an exact
@@ -22,27 +23,12 @@
 #include <cuda_fp16.h>
 
 #include "mmq_host.h"
+#include "mmq_q8_1.cuh"
 
 namespace mmq {
 namespace {
 
 constexpr int kThreads = 256;
-
-// round_half_away(x / d), the quotient rounded to f32 as IEEE division does,
-// without the division where the result cannot depend on it.  With
-// r = fl(1/d), z = fl(x * r) differs from the exact quotient y by at most
-// |y| * 2^-23 (two roundings), and the correctly rounded fl(y) from y by at
-// most |y| * 2^-24, so |z - fl(y)| < |y| * 2^-22 <= 3.1e-5 for |y| <= 127.5.
-// Unless z lies within 2^-14 (> that bound) of a half-integer, fl(y) is on
-// the same side of it and both round to the same integer; near a half-integer
-// (and when r is not a finite normal number) the quotient is taken exactly.
-__device__ __forceinline__ int round_quotient(float x, float d, float r)
-{
-    const float z = x * r;
-    const float a = fabsf(z);
-    if (r < 1e30f && a < 128.0f && fabsf(a - floorf(a) - 0.5f) > 0x1p-14f) return (int)roundf(z);
-    return (int)roundf(__fdiv_rn(x, d));
-}
 
 __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
     const float *__restrict__ x, int64_t ldx, int T, int K, int8_t *__restrict__ qs,
@@ -66,22 +52,8 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
         const int k = b * 32 + sub * 4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live) v = __ldg(reinterpret_cast<const float4 *>(x + (int64_t)t * ldx + k));
-        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-#pragma unroll
-        for (int m = 4; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m, 8));
-        int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-        float d32 = 0.0f;
-        if (amax != 0.0f) {
-            d32 = __fdiv_rn(amax, 127.0f);
-            const float r = __frcp_rn(d32);
-            q0 = min(127, max(-127, round_quotient(v.x, d32, r)));
-            q1 = min(127, max(-127, round_quotient(v.y, d32, r)));
-            q2 = min(127, max(-127, round_quotient(v.z, d32, r)));
-            q3 = min(127, max(-127, round_quotient(v.w, d32, r)));
-        }
-        int ssum = q0 + q1 + q2 + q3;
-#pragma unroll
-        for (int m = 4; m >= 1; m >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, m, 8);
+        const q8::Quad qd = q8::block8(v);
+        const int q0 = qd.q0, q1 = qd.q1, q2 = qd.q2, q3 = qd.q3;
         const int64_t e = (int64_t)t * K + k, blk_here = blk;
         blk += warp_step;
         t += step_t;
@@ -104,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
             hv.y = *reinterpret_cast<const uint32_t *>(&h23);
             *reinterpret_cast<uint2 *>(xh + e) = hv;
         }
-        const __half dh = __float2half_rn(d32);
+        const __half dh = qd.d16;
         if (xa) {
             // v = f32(d16) * q is exact in f32; hi = f16(v), lo = f16(v - hi), both exact
             const float df = __half2float(dh);
@@ -122,7 +94,7 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(
             *reinterpret_cast<uint2 *>(xa + e) = hv;
             *reinterpret_cast<uint2 *>(xa + (int64_t)T * K + e) = lv;
         }
-        if (sub == 0) ds[blk_here] = (uint32_t)__half_as_ushort(dh) | ((uint32_t)(uint16_t)(int16_t)ssum << 16);
+        if (sub == 0) ds[blk_here] = q8::scale_word(dh, qd.ssum);
     }
 }
 

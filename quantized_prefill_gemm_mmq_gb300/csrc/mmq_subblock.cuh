@@ -541,19 +541,7 @@ __device__ __forceinline__ uint32_t nib2(uint32_t w, uint32_t sel, uint32_t mask
     return h2bits(__hfma2(*reinterpret_cast<const __half2 *>(&h), m, a));
 }
 
-// the 6-bit scale (sc) and min (mm) of sub-block j from the 12 packed bytes
-// held in three words s0 (bytes 0-3), s1 (4-7), s2 (8-11)
-__device__ __forceinline__ void q4K_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int &sc, int &mm)
-{
-    if (j < 4) {
-        sc = (s0 >> (8 * j)) & 63;
-        mm = (s1 >> (8 * j)) & 63;
-    } else {
-        const int i = j - 4;
-        sc = ((s2 >> (8 * i)) & 15) | (((s0 >> (8 * i + 6)) & 3) << 4);
-        mm = ((s2 >> (8 * i + 4)) & 15) | (((s1 >> (8 * i + 6)) & 3) << 4);
-    }
-}
+using kq::q4K_scale_min;   // the 6-bit scale and min of sub-block j (mmq_kquant.cuh)
 
 }  // namespace q4
 

@@ -167,6 +167,31 @@ def gemv(w: torch.Tensor, xh: torch.Tensor, ds: torch.Tensor, O: int,
     return out
 
 
+DECODE_T_MAX = 4          # mmq_gemv_q4K_f32
+DECODE_K_MAX = 32768
+
+
+def gemv_f32(w: torch.Tensor, x: torch.Tensor, O: int, out: torch.Tensor | None = None,
+             fmt: str = "q4_K") -> torch.Tensor:
+    """Decode-shaped product for T <= 4 f32 tokens x [T][K] with the q8_1
+    quantisation built into the kernel (no quantise launch), W in q4_K or q6_K;
+    same result as gemm(fmt) on quantize_q8_1(x) up to f32 summation order."""
+    _need_cuda(w, x)
+    if x.dim() != 2 or x.dtype != torch.float32 or x.stride(1) != 1:
+        raise ValueError("x must be a row-major f32 [T][K] tensor")
+    T, K = x.shape
+    if fmt not in ("q4_K", "q6_K"):
+        raise ValueError(f"no decode product for {fmt!r}")
+    if w.dtype != torch.uint8 or w.numel() != O * (K // 256) * BLOCK_BYTES[fmt]:
+        raise ValueError(f"w must hold O*(K/256) {fmt} super-blocks (uint8)")
+    out = _out(out, T, O, x.device)
+    fn = load().mmq_gemv_q4K_f32 if fmt == "q4_K" else load().mmq_gemv_q6K_f32
+    with torch.cuda.device(x.device):
+        st = fn(_ptr(w), _ptr(x), x.stride(0), _ptr(out), T, O, K, _stream(x.device))
+    _check(f"gemv_f32({fmt})", st)
+    return out
+
+
 def interleave_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor, F: int) -> torch.Tensor:
     """The weight layout of gemm_swiglu: gate and up q4_K rows interleaved in groups
     of 64 rows (a permutation of whole rows; no arithmetic)."""

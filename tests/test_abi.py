@@ -22,7 +22,8 @@ def test_header_declares_the_boundary():
                      "mmq_gemm_q6K_subblock", "mmq_gemm_q4K_small", "mmq_gemm_q4K_small_imma",
                      "mmq_last_failure_info", "mmq_gemv_q4K", "mmq_gemv_q6K", "mmq_gemm_q4K_swiglu",
                      "mmq_gemm_q5K", "mmq_gemm_q5K_subblock", "mmq_gemm_q8_0", "mmq_debug_subdots_q5K",
-                     "mmq_debug_subdots_q8_0", "mmq_debug_fault_inject"):
+                     "mmq_debug_subdots_q8_0", "mmq_debug_fault_inject", "mmq_gemv_q4K_f32",
+                     "mmq_gemv_q6K_f32"):
         assert required in names
     assert set(names) == set(_lib.SIGNATURES), "binding signatures and header out of sync"
 
@@ -39,7 +40,7 @@ def test_library_exports_every_header_symbol():
 @needs_lib
 def test_library_loads_and_reports():
     lib = _lib.load()
-    assert lib.mmq_version() == 7
+    assert lib.mmq_version() == 8
     assert lib.mmq_status_str(0) == b"ok"
     for code in range(-10, 0):
         assert lib.mmq_status_str(code) not in (b"", b"unknown status")
@@ -75,6 +76,17 @@ def test_argument_errors_without_gpu():
         assert gemv(p, p, null, p, 16, 8, 256, null) == -6
         assert gemv(p, odd, p, p, 16, 8, 256, null) == -2
         assert gemv(p, p, p, p, 0, 8, 256, null) == 0                         # T == 0 no-op
+    for dec in (lib.mmq_gemv_q4K_f32, lib.mmq_gemv_q6K_f32):                 # decode with built-in q8_1
+        assert dec(p, p, 256, p, 5, 8, 256, null) == -1                       # T > 4
+        assert dec(p, p, 300, p, 1, 8, 300, null) == -1                       # K % 256
+        assert dec(p, p, 65536, p, 1, 8, 65536, null) == -1                   # K > 32768
+        assert dec(p, p, 256, p, 1, 0, 256, null) == -1                       # O < 1
+        assert dec(p, p, 252, p, 1, 8, 256, null) == -1                       # ldx < K
+        assert dec(null, p, 256, p, 1, 8, 256, null) == -6
+        assert dec(p, p, 256, null, 1, 8, 256, null) == -6
+        assert dec(p, odd, 256, p, 1, 8, 256, null) == -2
+        assert dec(p, p, 258, p, 1, 8, 256, null) == -2                       # ldx % 4
+        assert dec(p, p, 256, p, 0, 8, 256, null) == 0                        # T == 0 no-op
     assert lib.mmq_last_failure_info(null) == -6
     assert lib.mmq_debug_fault_inject(2, 1000) == -1                         # unknown mode
     info = (ctypes.c_int * 4)(7, 7, 7, 7)

@@ -298,6 +298,90 @@ def test_gemv_full_size(ops, oracle_ref, T):
         assert _rel_err(y.cpu().numpy(), ref) <= TOL, g.name
 
 
+@pytest.mark.parametrize("fmt", ["q4_K", "q6_K"])
+@pytest.mark.parametrize("T,O,K", [(1, 1, 256), (1, 7, 768), (2, 300, 512), (3, 33, 2816), (4, 64, 4096),
+                                   (1, 5000, 256), (4, 9, 11008), (2, 1, 32768), (3, 257, 1280), (1, 2047, 4096),
+                                   (1, 131, 2816), (2, 17, 512)])
+def test_gemv_f32(ops, orc, fmt, T, O, K):
+    """Decode product with the quantisation built in: every output against the
+    oracle's quantise-then-GEMM; ragged O (partial last warp pass, more rows
+    than resident warps at O = 5000), short last chunks (K = 11008: 43
+    super-blocks), odd super-block counts, the largest K, T = 1..4 (T = 3 runs
+    the 4-token instantiation with a padded token).  For q6_K the byte size of
+    W, O*(K/256)*210, is 2, 4, 6, 8, 10, 12 or 14 mod 16 in most cases, so the
+    last chunk's 16-byte window ends past W and its last bytes are read one by
+    one."""
+    w = synth.make_weights(fmt, O, K, seed=3 * T + O)
+    x = synth.make_x(T, K, seed=K + 5 * T, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm(fmt, w, qs_r, ds_r, O)
+    y1 = ops.gemv_f32(_dev(w), _dev(x), O, fmt=fmt)
+    y2 = ops.gemv_f32(_dev(w), _dev(x), O, fmt=fmt)
+    ops.check_status()
+    assert _rel_err(y1.cpu().numpy(), ref) <= TOL
+    assert torch.equal(y1, y2)                       # fixed summation order
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_gemv_q6K_f32_full_size(ops, orc, T):
+    """The 7B attn_v shape (q6_K, K = O = 4096) with full-range int8 sub-block
+    scales (-128..127), every output against the oracle."""
+    rng = np.random.default_rng(6262 + T)
+    O, K = 4096, 4096
+    w = synth.make_weights("q6_K", O, K, seed=35 + T).reshape(O * (K // 256), 210)
+    w[:, 192:208] = rng.integers(0, 256, size=(w.shape[0], 16), dtype=np.uint8)
+    w = w.reshape(-1)
+    x = synth.make_x(T, K, seed=36 + T, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q6_K", w, qs_r, ds_r, O)
+    y = ops.gemv_f32(_dev(w), _dev(x), O, fmt="q6_K")
+    ops.check_status()
+    assert _rel_err(y.cpu().numpy(), ref) <= TOL
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_gemv_f32_full_size(ops, orc, oracle_ref, T):
+    """The 7B decode shapes: K = 4096 and 11008 at O = 4096 (config 4's GEMMs),
+    and the chained gate+up rows (O = 22016, K = 4096), every output against
+    the oracle; the built-in quantisation against mmq_quantize_q8_1 through the
+    unfused path (the same sub-block dots, so the two agree to f32 rounding)."""
+    for g in synth.config(4, T).gemms:
+        _, _, ref = oracle_ref(g)
+        y = ops.gemv_f32(_dev(g.weights()), _dev(g.x()), g.O)
+        _, ds, xh, _ = ops.quantize_q8_1(_dev(g.x()), want_qs=False, want_xa=False)
+        y_unfused = ops.gemv(_dev(g.weights()), xh, ds, g.O)
+        ops.check_status()
+        assert _rel_err(y.cpu().numpy(), ref) <= TOL, g.name
+        assert _rel_err(y.cpu().numpy(), y_unfused.cpu().numpy()) <= 1e-6, g.name
+    O, K = 22016, 4096
+    w = synth.make_weights("q4_K", O, K, seed=71)
+    x = synth.make_x(T, K, seed=72, outliers=True)
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q4_K", w, qs_r, ds_r, O)
+    y = ops.gemv_f32(_dev(w), _dev(x), O)
+    ops.check_status()
+    assert _rel_err(y.cpu().numpy(), ref) <= TOL
+
+
+def test_gemv_f32_zero_and_extreme_tokens(ops, orc):
+    """An all-zero token (q8_1 d = 0: every term 0), a token with one nonzero
+    element per 32-block, and a token at +-1e4 (codes +-127): bit-exact codes
+    through the built-in quantisation show up as exact agreement with the
+    unfused path where every sub-block term is an exact f32 number."""
+    O, K = 130, 1024
+    w = synth.make_weights("q4_K", O, K, seed=81)
+    x = np.zeros((4, K), np.float32)
+    x[1, ::32] = np.arange(K // 32, dtype=np.float32) - 16.0
+    x[2] = np.where(np.arange(K) % 2 == 0, 1e4, -1e4).astype(np.float32)
+    x[3] = synth.make_x(1, K, seed=82)[0]
+    qs_r, ds_r = orc.quantize_q8_1(x)
+    ref = orc.gemm("q4_K", w, qs_r, ds_r, O)
+    y = ops.gemv_f32(_dev(w), _dev(x), O).cpu().numpy()
+    ops.check_status()
+    assert np.all(y[0] == 0.0)
+    assert _rel_err(y, ref) <= TOL
+
+
 @pytest.mark.parametrize("T,O,K", [(1, 1, 256), (8, 256, 1024), (9, 131, 2816), (16, 200, 768), (3, 17, 512),
                                    (16, 512, 4096), (5, 8, 11008), (1, 1000, 512), (12, 33, 3072), (2, 7, 256)])
 def test_gemv_q6K(ops, orc, T, O, K):
