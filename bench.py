@@ -386,17 +386,22 @@ def format_lines(dev, mac_peak, T=512, K=4096, O=4096):
     return out
 
 
-def decode_line(dev, layers, groups, xs, hbm_gbs):
+def decode_line(dev, layers, wl, xs, hbm_gbs):
     """Side measurement: one decode step (T = 1) of the whole layer stack, every
     layer's weights streamed from HBM; one CUDA graph per three steps, device
-    time per step (best of 5).  Per layer the seven projections (gate and up as
-    one launch over their concatenated rows) run as mmq_gemv_q4K_f32 /
-    mmq_gemv_q6K_f32 on the f32 token, the q8_1 quantisation inside each
-    launch.  The same step with every input quantised by its own launch and
-    the products on mmq_gemv_q4K / mmq_gemv_q6K is timed beside it
-    (`unfused`)."""
+    time per step (best of 5).  Per layer the seven projections run in five
+    launches (decode_groups: q and k, and gate and up, over their concatenated
+    rows) as mmq_gemv_q4K_f32 / mmq_gemv_q6K_f32 on the f32 token, the q8_1
+    quantisation inside each launch.  The same launches with every input
+    quantised by its own launch and the products on mmq_gemv_q4K /
+    mmq_gemv_q6K are timed beside it (`unfused`).  `layers` holds the prefill
+    step's weights (the chained FFN's gate/up rows interleaved: the same bytes
+    for a product with one token)."""
     import torch
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
+    groups = decode_groups(wl)
+    layers = [{g.name: (torch.cat([lw[m.name] for m in g.members]) if g.name == "q+k" else lw[g.name])
+               for g in groups} for lw in layers]
     kk = {s: x.shape[1] for s, x in xs.items()}
     x1 = {s: torch.from_numpy(synth.make_x(1, k, 900 + s)).to(dev) for s, k in kk.items()}
     qb = {s: (None, torch.empty((1, k // 32), dtype=torch.int32, device=dev),
@@ -458,6 +463,24 @@ def launch_groups(wl):
             out.append(LaunchGroup("gate+up", [g, byname["up"]]))
         else:
             out.append(LaunchGroup(g.name, [g]))
+    return out
+
+
+def decode_groups(wl):
+    """The decode step's launches: as launch_groups, and q and k, which read
+    the same token and are both q4_K, as one launch over their concatenated
+    rows (at T = 1 every launch carries a few microseconds of fixed cost, so
+    the fewer the better; v is q6_K and stays its own launch)."""
+    out, qk = [], []
+    for g in launch_groups(wl):
+        if g.name in ("q", "k") and g.fmt == "q4_K":
+            qk.extend(g.members)
+        else:
+            out.append(g)
+    if len(qk) == 2:
+        out.insert(0, LaunchGroup("q+k", qk))
+    else:
+        out = launch_groups(wl)
     return out
 
 
@@ -609,7 +632,7 @@ def decode_launches(args):
     from quantized_prefill_gemm_mmq_gb300 import ops, synth
     dev = torch.device("cuda", 0)
     wl, xs = build_inputs(args.tokens)
-    groups = launch_groups(wl)
+    groups = decode_groups(wl)
     host_w = {g.name: g.weights() for g in wl.gemms}
     w_layer = {gr.name: torch.from_numpy(np.concatenate([host_w[m.name] for m in gr.members])).to(dev)
                for gr in groups}
@@ -953,7 +976,7 @@ def mmq_arm(args):
                  "lines": sweep_lines(dev, hbm_gbs, mac_peak)}
     decode = formats = None
     if not args.no_small_t and world == 1:
-        decode = decode_line(dev, layers, groups, xs, hbm_gbs)
+        decode = decode_line(dev, layers, wl, xs, hbm_gbs)
         formats = {"kernels": "production: mmq_gemm_q4K / _q5K / _q6K; subblock: mmq_gemm_q4K_subblock / "
                               "q5K_subblock / q6K_subblock and mmq_gemm_q8_0 (per-sub-block form)",
                    "timing": "CUDA-graph replay cycling through >320 MB of weight copies, device events, best of 5",
