@@ -334,8 +334,8 @@ def sweep_lines(dev, hbm_gbs, mac_peak, fast=False):
                 line["ksplit"] = ks
             out.append(line)
             del copies
-    # the decode-shaped q6_K product on the 7B attn_v shape (K = O = 4096)
-    for T in (1, 16):
+    # the decode-shaped q6_K products on the 7B attn_v shape (K = O = 4096)
+    for T in (1, 4, 16):
         w0 = torch.from_numpy(synth.make_weights("q6_K", 4096, 4096, 301)).to(dev)
         copies = [w0] + [w0.clone() for _ in range(int(320e6 // w0.numel()))]
         n = 2 * len(copies)
@@ -345,6 +345,9 @@ def sweep_lines(dev, hbm_gbs, mac_peak, fast=False):
         kern = {"gemv": graph_time_us([lambda w=w: ops.gemv(w, xh, ds, 4096, out=y, fmt="q6_K") for w in copies], n=n),
                 "production": graph_time_us([lambda w=w: ops.gemm("q6_K", w, xa, ds, 4096, out=y) for w in copies],
                                             n=n)}
+        if T <= ops.DECODE_T_MAX:   # f32 token in, the q8_1 quantisation inside the launch
+            kern["gemv_f32"] = graph_time_us([lambda w=w: ops.gemv_f32(w, x, 4096, out=y, fmt="q6_K")
+                                              for w in copies], n=n)
         abytes = algorithmic_bytes("q6_K", T, 4096, 4096)
         us = min(kern.values())
         out.append({"fmt": "q6_K", "T": T, "K": 4096, "O": 4096, "us": {k: round(v, 3) for k, v in kern.items()},

@@ -97,7 +97,9 @@ __device__ __forceinline__ void quantize_tokens(const float *__restrict__ x, int
             const int t = blk / nb, b = blk - t * nb;
             v[g] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (blk < total && t < T)
-                v[g] = __ldg(reinterpret_cast<const float4 *>(x + (int64_t)t * ldx + 32 * b + 4 * sub));
+                // L2 loads, not the read-only path: under programmatic dependent launch this
+                // kernel starts before x (the previous kernel's output) is written
+                v[g] = __ldcg(reinterpret_cast<const float4 *>(x + (int64_t)t * ldx + 32 * b + 4 * sub));
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {

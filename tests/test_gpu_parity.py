@@ -322,6 +322,53 @@ def test_gemv_f32(ops, orc, fmt, T, O, K):
     assert torch.equal(y1, y2)                       # fixed summation order
 
 
+def test_gemv_f32_chained_launches(ops, orc):
+    """Decode launches back to back on one stream, each reading the previous
+    launch's output as its token: with programmatic dependent launch the next
+    kernel starts before the previous one has finished and may read its
+    weights early, but x only after the previous kernel has completed, and it
+    writes y only then.  The chain must equal the same chain with a device
+    synchronisation after every launch, bit for bit, and every link the
+    oracle's product of the link's input."""
+    O = K = 4096
+    fmts = ["q4_K", "q6_K", "q4_K", "q4_K", "q6_K", "q4_K"]
+
+    def tame(w, f):
+        # the f16 scales of every block / 16 (exact), so that a link's output is of the
+        # order of its input and six links stay in the f16 range of the q8_1 scales
+        size, at = (144, (0, 4)) if f == "q4_K" else (210, (208, 210))
+        b = w.reshape(-1, size)
+        d = b[:, at[0]:at[1]].copy().view(np.float16) / np.float16(16)
+        b[:, at[0]:at[1]] = d.astype(np.float16).view(np.uint8).reshape(b.shape[0], -1)
+        return w
+
+    ws = [_dev(tame(synth.make_weights(f, O, K, seed=500 + i), f)) for i, f in enumerate(fmts)]
+    x0 = _dev(synth.make_x(1, K, seed=499))
+
+    def chain(sync):
+        y, outs = x0, []
+        for w, f in zip(ws, fmts):
+            y = ops.gemv_f32(w, y, O, fmt=f)
+            outs.append(y)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return outs
+
+    a, b = chain(False), chain(True)
+    ops.check_status()
+    for ya, yb in zip(a, b):
+        assert torch.isfinite(ya).all() and ya.abs().max() > 0
+        assert torch.equal(ya, yb)
+    # every link against the oracle on the link's own input (its predecessor's output)
+    prev = x0.cpu().numpy()
+    for y, w, f in zip(a, ws, fmts):
+        qs_r, ds_r = orc.quantize_q8_1(prev)
+        ref = orc.gemm(f, w.cpu().numpy(), qs_r, ds_r, O)
+        assert _rel_err(y.cpu().numpy(), ref) <= TOL
+        prev = y.cpu().numpy()
+
+
 @pytest.mark.parametrize("T", [1, 4])
 def test_gemv_q6K_f32_full_size(ops, orc, T):
     """The 7B attn_v shape (q6_K, K = O = 4096) with full-range int8 sub-block
