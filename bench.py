@@ -101,10 +101,10 @@ def load_peaks():
 
 # Bytes per weight of each k-quant format (one super-block per 256 weights).
 WEIGHT_BYTES = {"q4_K": 144 / 256, "q6_K": 210 / 256}
-# f16 tensor-core MMAs per algorithmic MAC on this route: q4_K multiplies the
-# exact hi and lo activation planes (2), q6_K also splits the weight value
-# into hi and lo and runs hi*hi, lo*hi, hi*lo (3).
-ROUTE_MMAS = {"q4_K": 2, "q6_K": 3}
+# f16 tensor-core MMA products per algorithmic MAC on this route: q4_K
+# multiplies the exact hi and lo activation planes (2), q6_K also splits the
+# weight value into hi and lo planes and forms all four products (4).
+ROUTE_MMAS = {"q4_K": 2, "q6_K": 4}
 
 
 def algorithmic_bytes(fmt, T, K, O):
@@ -949,8 +949,9 @@ def mmq_arm(args):
                             "reads the activations as exact f16 hi/lo planes (4 B per element) + scale words",
         "peak_source": f"{peak_src} bf16 dense, {peak_kind}; f16 runs at the bf16 rate",
         "route_ceiling_frac": sq_line["route_ceiling_frac"] if sq_line else None,
-        "route_ceiling_note": "exact results take 2 f16 MMAs per 16-k step for q4_K (activation hi and lo planes), "
-                              "3 for q6_K: the route's ceiling is 1/2 (1/3) of the dense peak",
+        "route_ceiling_note": "exact results take 2 f16 MMA products per useful one for q4_K (activation hi and "
+                              "lo planes), 4 for q6_K (weight hi and lo planes too): the route's ceiling is 1/2 "
+                              "(1/4) of the dense peak",
         "timing": kernel_timing,
         "avg_launch_us": sq_line["avg_launch_us"] if sq_line else None,
         "shapes": shapes,

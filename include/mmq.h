@@ -344,9 +344,9 @@ int mmq_gemm_q4K_subblock(const void *w, const uint16_t *xh, const uint32_t *ds,
  * (rounding order unspecified).
  * Production form: the tensor core accumulates each 256-weight super-block
  * from the exact activation planes xa (hi + lo) and the weight values
- * sc*(q-32) as exact f16 hi + lo planes (three MMAs per 16-k step; the
- * dropped lo*lo product is below 2^-22 of each product); d is applied per
- * super-block.
+ * sc*(q-32) as exact f16 hi + lo planes (two MMAs per 16-k step, weight hi
+ * and weight lo against both activation planes: every product exact in f32);
+ * d is applied per super-block.
  * w: O*(K/256)*210 bytes.  xa: as written by mmq_quantize_q8_1.  ds: not
  * read (q6_K has no min term; may be NULL).  y: f32 [T][O], overwritten.
  * T >= 0, O >= 1, 256 <= K <= 2^20, K % 256 == 0.

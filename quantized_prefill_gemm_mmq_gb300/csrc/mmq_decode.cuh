@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(dec::NTHREADS) mmq_q4K_decode_kernel(const uin
                                                                        float *__restrict__ y, int T, int O, int K)
 {
     using namespace dec;
-    extern __shared__ __align__(128) uint8_t sm[];
-    const uint32_t sbase = smem_u32(sm);
+    extern __shared__ __align__(128) uint8_t dec_sm[];
+    const uint32_t sbase = smem_u32(dec_sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsb = K >> 8, nb = K >> 5;
     const int nch_row = (nsb + CH - 1) / CH;                 // chunks per row
@@ -133,9 +133,9 @@ __global__ void __launch_bounds__(dec::NTHREADS) mmq_q4K_decode_kernel(const uin
     const int row0 = (int)blockIdx.x + (int)gridDim.x * warp;   // this warp's rows: row0, row0 + nwarps, ...
     const int nrows = row0 < O ? (O - 1 - row0) / nwarps + 1 : 0;
     const int nchunks = nrows * nch_row;
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + oMisc);
-    int8_t *xq = reinterpret_cast<int8_t *>(sm + oX);                                // [NT][nsb][XSB]
-    uint32_t *xd = reinterpret_cast<uint32_t *>(sm + oX + (size_t)NT * nsb * XSB);    // [NT][nb]
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(dec_sm + oMisc);
+    int8_t *xq = reinterpret_cast<int8_t *>(dec_sm + oX);                                // [NT][nsb][XSB]
+    uint32_t *xd = reinterpret_cast<uint32_t *>(dec_sm + oX + (size_t)NT * nsb * XSB);    // [NT][nb]
     const uint32_t bar0 = sbase + oBar + warp * NCH * 8;
 
     if (threadIdx.x == 0) *abort_flag = 0u;
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(dec::NTHREADS) mmq_q4K_decode_kernel(const uin
 #pragma unroll
         for (int sl = lane & 7; sl < CH; sl += 8) {
             if (sl >= nsb - k0) break;   // a row's last chunk may be short
-            const uint8_t *blk = sm + warp * WARP_RING + slot * CHUNK_BYTES + sl * 144;
+            const uint8_t *blk = dec_sm + warp * WARP_RING + slot * CHUNK_BYTES + sl * 144;
             const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
             const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * p);   // quant bytes 32p .. 32p + 15
             const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * p);   // 32p + 16 .. 32p + 31
@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(dec::NTHREADS) mmq_q6K_decode_kernel(const uin
                                                                        float *__restrict__ y, int T, int O, int K)
 {
     using namespace dec;
-    extern __shared__ __align__(128) uint8_t sm[];
-    const uint32_t sbase = smem_u32(sm);
+    extern __shared__ __align__(128) uint8_t dec_sm[];
+    const uint32_t sbase = smem_u32(dec_sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsb = K >> 8, nb = K >> 5;
     const int nch_row = (nsb + CH6 - 1) / CH6;
@@ -284,10 +284,10 @@ __global__ void __launch_bounds__(dec::NTHREADS) mmq_q6K_decode_kernel(const uin
     const int nrows = row0 < O ? (O - 1 - row0) / nwarps + 1 : 0;
     const int nchunks = nrows * nch_row;
     const size_t total = (size_t)O * nsb * 210;   // bytes of W
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sm + oMisc6);
-    int8_t *xq = reinterpret_cast<int8_t *>(sm + oX6);
-    uint32_t *xd = reinterpret_cast<uint32_t *>(sm + oX6 + (size_t)NT * nsb * XSB);
-    uint8_t *ring = sm + warp * WARP_RING6;
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(dec_sm + oMisc6);
+    int8_t *xq = reinterpret_cast<int8_t *>(dec_sm + oX6);
+    uint32_t *xd = reinterpret_cast<uint32_t *>(dec_sm + oX6 + (size_t)NT * nsb * XSB);
+    uint8_t *ring = dec_sm + warp * WARP_RING6;
     const uint32_t bar0 = sbase + oBar6 + warp * NCH6 * 8;
 
     if (threadIdx.x == 0) *abort_flag = 0u;
