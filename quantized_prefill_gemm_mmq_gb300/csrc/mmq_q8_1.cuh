@@ -67,6 +67,42 @@ __device__ __forceinline__ Quad block8(float4 v)
     return o;
 }
 
+// The same block held by four consecutive lanes (an aligned group of 4),
+// eight values each (a and b: values 0-3 and 4-7 of this lane's eight).
+// Every lane of the warp must call it; q[] are this lane's codes.
+struct Oct {
+    int q[8];
+    __half d16;
+    int ssum;
+};
+
+__device__ __forceinline__ Oct block4(float4 a, float4 b)
+{
+    float amax = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                       fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1, 4));
+    Oct o;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o.q[i] = 0;
+    float d32 = 0.0f;
+    if (amax != 0.0f) {
+        d32 = __fdiv_rn(amax, 127.0f);
+        const float r = __frcp_rn(d32);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o.q[i] = min(127, max(-127, round_quotient(v[i], d32, r)));
+    }
+    int ssum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ssum += o.q[i];
+    ssum += __shfl_xor_sync(0xffffffffu, ssum, 2, 4);
+    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1, 4);
+    o.ssum = ssum;
+    o.d16 = __float2half_rn(d32);
+    return o;
+}
+
 // the scale word: low 16 bits f16 d, high 16 bits int16 ssum
 __device__ __forceinline__ uint32_t scale_word(__half d16, int ssum)
 {
