@@ -99,6 +99,9 @@ struct Params {
     uint16_t *h_xa;
     uint32_t *h_ds;
     int8_t *h_qs;
+    // production q4_K / q6_K, one split: nonzero when y is written by tensor
+    // stores of the tile (y's row stride O*4 bytes a multiple of 16)
+    int y_tma;
 };
 
 // wait sites recorded with a timeout

@@ -121,7 +121,7 @@ __device__ __forceinline__ float swiglu_f32(float g, float u)
 template <int FMT, bool SWIGLU>
 __global__ void __launch_bounds__(q4s::NTHREADS, 1)
     mmq_q4K_sb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                      const Params p)
+                      const __grid_constant__ CUtensorMap tmY, const Params p)
 {
     using namespace q4s;
     using SL = SbLayout<FMT>;
@@ -409,6 +409,24 @@ __global__ void __launch_bounds__(q4s::NTHREADS, 1)
         };
         if (SWIGLU) {
             // written above
+        } else if ((p.part == nullptr || gridDim.z == 1) && p.y_tma) {
+            // The tile staged in the idle operand ring as four [128 tokens][32 rows]
+            // boxes (one per TMEM lane quarter; a warp's 32 rows are one 128-byte
+            // row of its box), then written by four tensor stores; rows past O and
+            // tokens past T are clipped by the map.
+            float *ys = reinterpret_cast<float *>(smem + oStage) + quarter * (BM * 32) + c0 * 32 + lane;
+            if (ok) {   // (after an abort, copies in flight may still land in the ring)
+#pragma unroll
+                for (int i = 0; i < 64; ++i) ys[i * 32] = yv[i];
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, NUM_EPI_WARPS * 32);
+            if (warp == EPI_WARP0 && lane == 0 && *abort_flag == 0u) {
+                for (int q = 0; q < 4 && o0 + 32 * q < O; ++q)
+                    tma_store_2d(&tmY, sbase + oStage + (uint32_t)q * (BM * 32 * 4), o0 + 32 * q, t0);
+                bulk_commit_group();
+                bulk_wait_all();
+            }
         } else if (p.part == nullptr || gridDim.z == 1) {
             if (ok && col_ok) store_col(p.y + (size_t)(t0 + c0) * O + o);
         } else {
@@ -640,13 +658,21 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     }
     int rc = check_arch();
     if (rc != MMQ_OK) return rc;
-    CUtensorMap tmA, tmW;
+    CUtensorMap tmA, tmW, tmY;
     rc = make_tmap_2d(&tmA, xa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, 2ull * (uint64_t)T, (uint64_t)K * 2, BK,
                       BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MMQ_OK) return rc;
     rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)nsb * row_bytes, (uint64_t)O,
                       (uint64_t)nsb * row_bytes, row_bytes, BN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != MMQ_OK) return rc;
+    // y by tensor stores ([T][O] f32, boxes of 32 rows x 128 tokens) when its row stride allows
+    const bool y_tma = !h_xa && splits == 1 && (O % 4) == 0;
+    std::memset(&tmY, 0, sizeof(tmY));
+    if (y_tma) {
+        rc = make_tmap_2d(&tmY, y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (uint64_t)O, (uint64_t)T, (uint64_t)O * 4, 32, BM,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != MMQ_OK) return rc;
+    }
     static bool attr_done[64];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -675,14 +701,15 @@ int launch_q4K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     prm.h_xa = h_xa;
     prm.h_ds = h_ds;
     prm.h_qs = h_qs;
+    prm.y_tma = y_tma ? 1 : 0;
     const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM), (unsigned)splits);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (fmt == kQ5K)
-        mmq_q4K_sb_kernel<kQ5K, false><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ5K>::kDynSmem, cs>>>(tmA, tmW, prm);
+        mmq_q4K_sb_kernel<kQ5K, false><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ5K>::kDynSmem, cs>>>(tmA, tmW, tmY, prm);
     else if (h_xa)
-        mmq_q4K_sb_kernel<kQ4K, true><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ4K>::kDynSmem, cs>>>(tmA, tmW, prm);
+        mmq_q4K_sb_kernel<kQ4K, true><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ4K>::kDynSmem, cs>>>(tmA, tmW, tmY, prm);
     else
-        mmq_q4K_sb_kernel<kQ4K, false><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ4K>::kDynSmem, cs>>>(tmA, tmW, prm);
+        mmq_q4K_sb_kernel<kQ4K, false><<<grid, q4s::NTHREADS, q4s::SbLayout<kQ4K>::kDynSmem, cs>>>(tmA, tmW, tmY, prm);
     return launch_status();
 }
 

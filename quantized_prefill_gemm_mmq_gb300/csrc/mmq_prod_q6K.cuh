@@ -131,7 +131,8 @@ __device__ __forceinline__ void q6_pairs(uint32_t q4, __half2 sc2, uint32_t &h0,
 }  // namespace q6s
 
 __global__ void __launch_bounds__(q6s::NTHREADS, 1)
-    mmq_q6K_sb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const Params p)
+    mmq_q6K_sb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmY, const Params p)
 {
     using namespace q6s;
     constexpr int kKid = 10;
@@ -401,13 +402,32 @@ __global__ void __launch_bounds__(q6s::NTHREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(slot));
         }
-        // this thread's outputs: column o of rows t0 + c0 .. t0 + c0 + 63 of the [T][O] array
-        const int nt = min(64, T - t0 - c0);
-        if (ok && o < O) {
-            float *base = p.y + (size_t)(t0 + c0) * O + o;
+        if (p.y_tma) {
+            // the tile staged in the idle operand ring as four [128 tokens][32 rows]
+            // boxes (one per TMEM lane quarter), written by four tensor stores; rows
+            // past O and tokens past T are clipped by the map
+            float *ys = reinterpret_cast<float *>(smem + oStage) + quarter * (BM * 32) + c0 * 32 + lane;
+            if (ok) {   // (after an abort, copies in flight may still land in the ring)
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
-                if (i < nt) base[(size_t)i * O] = yv[i];
+                for (int i = 0; i < 64; ++i) ys[i * 32] = yv[i];
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, NUM_EPI_WARPS * 32);
+            if (warp == EPI_WARP0 && lane == 0 && *abort_flag == 0u) {
+                for (int q = 0; q < 4 && o0 + 32 * q < O; ++q)
+                    tma_store_2d(&tmY, sbase + oStage + (uint32_t)q * (BM * 32 * 4), o0 + 32 * q, t0);
+                bulk_commit_group();
+                bulk_wait_all();
+            }
+        } else {
+            // this thread's outputs: column o of rows t0 + c0 .. t0 + c0 + 63 of the [T][O] array
+            const int nt = min(64, T - t0 - c0);
+            if (ok && o < O) {
+                float *base = p.y + (size_t)(t0 + c0) * O + o;
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (i < nt) base[(size_t)i * O] = yv[i];
+            }
         }
     }
 
@@ -430,7 +450,7 @@ int launch_q6K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     if (!aligned16(w) || !aligned16(xa) || !aligned16(y)) return MMQ_ERR_ALIGN;
     int rc = check_arch();
     if (rc != MMQ_OK) return rc;
-    CUtensorMap tmA, tmW;
+    CUtensorMap tmA, tmW, tmY;
     rc = make_tmap_2d(&tmA, xa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)K, 2ull * (uint64_t)T, (uint64_t)K * 2,
                       BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != MMQ_OK) return rc;
@@ -440,6 +460,14 @@ int launch_q6K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     if (O >= 8) {
         rc = make_tmap_2d(&tmW, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, group_bytes, (uint64_t)(O / 8), group_bytes,
                           q6s::RAW_COPY, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc != MMQ_OK) return rc;
+    }
+    // y by tensor stores ([T][O] f32, boxes of 32 rows x 128 tokens) when its row stride allows
+    const bool y_tma = (O % 4) == 0;
+    std::memset(&tmY, 0, sizeof(tmY));
+    if (y_tma) {
+        rc = make_tmap_2d(&tmY, y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (uint64_t)O, (uint64_t)T, (uint64_t)O * 4, 32, BM,
+                          CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc != MMQ_OK) return rc;
     }
     static bool attr_done[64];
@@ -463,8 +491,9 @@ int launch_q6K_sb(const void *w, const uint16_t *xa, const uint32_t *ds, float *
     prm.sb_per_split = K / 256;
     prm.part = nullptr;
     prm.cnt = nullptr;
+    prm.y_tma = y_tma ? 1 : 0;
     const dim3 grid((unsigned)((O + BN - 1) / BN), (unsigned)((T + BM - 1) / BM));
-    mmq_q6K_sb_kernel<<<grid, q6s::NTHREADS, q6s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, prm);
+    mmq_q6K_sb_kernel<<<grid, q6s::NTHREADS, q6s::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmW, tmY, prm);
     return launch_status();
 }
 
