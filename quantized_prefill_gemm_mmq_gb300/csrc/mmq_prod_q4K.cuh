@@ -47,7 +47,9 @@ namespace {
 // is free.  The raw weight super-blocks (128 rows x 144 bytes) arrive by TMA
 // one super-block ahead; the unpack and scale threads copy what they need to
 // registers at the start of a super-block and release the raw slot at once.
-// TMEM: two rotating super-block accumulators of 256 columns.
+// TMEM: two rotating super-block accumulators of 256 columns.  The finished
+// output tile leaves through TMA tensor stores from the idle operand ring
+// (one split, O a multiple of 4; otherwise every thread stores its column).
 // Warps: 1 MMA issuer, 14 activation TMA, 2-5 unpack (+ raw weight TMA),
 // 6-13 epilogue, 0 and 15 scale.
 // =========================================================================

@@ -35,7 +35,8 @@ namespace {
 // each unpack thread realigns its row's 208 bytes of quants and scales into
 // registers and releases the slot at once.
 // One MMA-issuing thread waiting once per stage on a merged "full" barrier;
-// TMEM: two rotating super-block accumulators of 256 columns.
+// TMEM: two rotating super-block accumulators of 256 columns; the output
+// tile leaves through TMA tensor stores when O is a multiple of 4.
 // Warps: 0 raw-weight producer, 1 MMA issuer, 14 activation TMA producer,
 // 2-5 unpack (thread = weight row), 6-13 epilogue (weight row x 64 tokens).
 // =========================================================================
